@@ -1,0 +1,10 @@
+"""CPU oracle for the DoRA factored row norm and stable compose.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and ``bench.py``'s CPU-baseline / reference legs, never by the library.
+"""
+from .dora_oracle import (  # noqa: F401
+    BF16, F32, compose, compose_stored, decode, dense_ba_bytes,
+    factored_intermediate_bytes, magnitude_scale, naive_compose_f32,
+    norm_and_scale, round_to, round_to_bf16_bits, row_norm,
+)
