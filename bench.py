@@ -1,0 +1,470 @@
+"""Benchmark of the DoRA per-module hot path on one GB300 (or N, one process each).
+
+One step = the whole hot path for one adapted module at d_out = d_in = 8192,
+r = 384, bf16: dora_factored_norm (G = A A^T, the BA-norm term, the fused
+U = W A^T main pass, finalize) followed by dora_compose on 2048 x 8192
+activations with the g just computed.  Inputs are seeded synthetic tensors
+resident in HBM; three input/output sets rotate so no step finds its operands
+in the 129 MB L2.
+
+Printed (rank 0, one JSON line):
+  value      factored-norm TFLOP/s: algorithmic norm FLOPs of all ranks divided
+             by the norm part of the step (CUDA events on the launching stream,
+             averaged over the K timed steps, max over ranks)
+  compose    compose GB/s over the compose part of the same steps
+  roofline   the dominant kernel (the U = W A^T main pass) against the measured
+             bf16 peak; roofline_compose the compose kernel against HBM copy BW
+  e2e        the same metrics through the public API from pinned host buffers,
+             host<->device copies inside the timed region
+  cpu_baseline  the float64 CPU oracle on the host cores, bounded sample
+
+--impl reference times the CPU oracle (the only reference this build has) on
+the same metric, per step a bounded sample sized so the run ends in minutes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import configs, gen  # noqa: E402
+
+CFG_INDEX = 1
+N_SETS = 3
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def main_pass_flops(d_out, d_in, r):
+    """U = W A^T (2 d_out d_in r), sum of squares of W (2 d_out d_in), rowsum(B o U) (2 d_out r)."""
+    return 2 * d_out * d_in * r + 2 * d_out * d_in + 2 * d_out * r
+
+
+def file_digest(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_src, profile_name):
+    """dram bytes per launch recorded in profiles/<profile_name>, if the kernel
+    source it was measured on is unchanged."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_bytes or not m_src:
+        return None
+    if m_src.group(1) != file_digest(kernel_src):
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((t, float(parts[2]), float(parts[3]), parts[6:10], parts[5]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        inside = [r for r in rows if self.t_start is not None and self.t_start <= r[0] <= self.t_end]
+        use = inside if inside else rows[-3:]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(cfg, norm_x, comp_x, g32, rows, tokens):
+    """Time the float64 oracle on `rows` norm rows and `tokens` compose rows."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.norm_and_scale(norm_x["W"][rows], norm_x["A"], norm_x["B"][rows], norm_x["m"][rows],
+                          cfg.s, float(np.float32(cfg.eps)), cfg.dtype)
+    t1 = time.perf_counter()
+    oracle.compose_stored(comp_x["base"][tokens], comp_x["lora"][tokens], g32, cfg.s, cfg.dtype)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def cpu_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = configs.get(CFG_INDEX)
+    mod = cfg.module
+    norm_x = gen.norm_inputs(cfg)
+    comp_x = gen.compose_inputs(cfg)
+    g32 = np.full(mod.d_out, 1.0, np.float32)
+    # calibrate: cost per norm row and per compose token row
+    tn, tc = oracle_sample(cfg, norm_x, comp_x, g32, np.arange(64), np.arange(64))
+    per_row, per_tok = tn / 64, tc / 64
+    budget = 90.0 / max(1, args.steps + args.warmup)          # seconds per step
+    rows = int(np.clip(budget * 0.8 / per_row, 1, mod.d_out))
+    toks = int(np.clip(budget * 0.2 / per_tok, 1, cfg.tokens))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, norm_x, comp_x, g32, np.sort(rng.choice(mod.d_out, rows, False)),
+                      np.sort(rng.choice(cfg.tokens, toks, False)))
+    tn_tot = tc_tot = 0.0
+    for _ in range(args.steps):
+        a, b = oracle_sample(cfg, norm_x, comp_x, g32, np.sort(rng.choice(mod.d_out, rows, False)),
+                             np.sort(rng.choice(cfg.tokens, toks, False)))
+        tn_tot += a
+        tc_tot += b
+    norm_flops_row = configs.norm_flops(mod.d_out, mod.d_in, cfg.r) / mod.d_out
+    value = norm_flops_row * rows * args.steps / tn_tot / 1e12
+    comp_bytes_tok = configs.compose_bytes(1, mod.d_out, cfg.dtype)
+    comp_gbs = comp_bytes_tok * toks * args.steps / tc_tot / 1e9
+    sample = (f"per step: oracle norm on {rows} random rows of the {mod.d_out}x{mod.d_in} r={cfg.r} "
+              f"module + compose on {toks} random token rows of {cfg.tokens}x{mod.d_out}; "
+              f"scaled to TFLOP/s by the method's algorithmic FLOPs per row")
+    line = {
+        "impl": "reference", "metric": json.loads(BASELINE_METRIC), "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (tn_tot + tc_tot) / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "d_out": mod.d_out, "d_in": mod.d_in, "r": cfg.r,
+                   "tokens": cfg.tokens, "dtype_inputs": cfg.dtype},
+        "compose": {"value": comp_gbs, "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+BASELINE_METRIC = json.dumps("factored-norm TFLOP/s + compose GB/s (% of GB300 peak) at 8192², r=384")
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from dora_parameter_efficient_gb300 import _lib, api
+
+    cfg = configs.get(CFG_INDEX)
+    mod = cfg.module
+    d_out, d_in, r, T = mod.d_out, mod.d_in, cfg.r, cfg.tokens
+    peaks, peak_src = load_peaks()
+
+    # ---- inputs: this rank's module (weak scaling: one independent module per rank)
+    norm_x = gen.norm_inputs(cfg, seed=rank)
+    comp_x = gen.compose_inputs(cfg, seed=rank)
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    set0 = {k: to_dev(v) for k, v in {**norm_x, **comp_x}.items()}
+    sets = [set0] + [{k: v.clone() for k, v in set0.items()} for _ in range(N_SETS - 1)]
+    wn = [torch.empty(d_out, dtype=torch.float32, device=dev) for _ in range(N_SETS)]
+    gg = [torch.empty(d_out, dtype=torch.float32, device=dev) for _ in range(N_SETS)]
+    outs = [torch.empty((T, d_out), dtype=torch.bfloat16, device=dev) for _ in range(N_SETS)]
+    ws = [api.alloc_workspace(d_out, d_in, r, torch.bfloat16, dev) for _ in range(N_SETS)]
+    stream = torch.cuda.current_stream()
+    set_bytes = sum(v.numel() * v.element_size() for v in set0.values())
+
+    def step(i, evs=None):
+        k = i % N_SETS
+        s = sets[k]
+        api.dora_factored_norm(s["W"], s["A"], s["B"], cfg.s, s["m"], cfg.eps, wnorm=wn[k],
+                               g=gg[k], workspace=ws[k],
+                               main_events=None if evs is None else (evs[1], evs[2]))
+        if evs is not None:
+            evs[3].record(stream)
+        api.dora_compose(s["base"], s["lora"], gg[k], cfg.s, out=outs[k])
+
+    # ---- warm-up (also starts the clock sampler so it is running by the timed region)
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t_spin = time.time()
+    i = args.warmup
+    while time.time() - t_spin < 0.6:          # keep the GPU loaded until the sampler reports
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    for k in range(N_SETS):
+        assert api.dora_check_status(ws[k]) == 0, "device pipeline reported a timeout"
+
+    # ---- timed region: exactly K steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in evs:            # create the CUDA events before the timed region
+        for x in e:
+            x.record(stream)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    launches0 = _lib.load().dora_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.t_start = time.time()
+    t_begin.record(stream)
+    for i in range(args.steps):
+        e = evs[i]
+        e[0].record(stream)
+        step(i, e)
+        e[4].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    sampler.t_end = time.time()
+    barrier(world)
+    launches = _lib.load().dora_launch_count() - launches0
+    total_ms = t_begin.elapsed_time(t_end)
+    norm_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    main_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    comp_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    sampler.stop()
+    clocks = sampler.summary()
+
+    mean = statistics.fmean
+    ms_per_step = max_over_ranks(total_ms / args.steps, world, dev)
+    norm_ms_m = max_over_ranks(mean(norm_ms), world, dev)
+    main_ms_m = max_over_ranks(mean(main_ms), world, dev)
+    comp_ms_m = max_over_ranks(mean(comp_ms), world, dev)
+
+    nflops = configs.norm_flops(d_out, d_in, r)
+    cbytes = configs.compose_bytes(T, d_out, cfg.dtype)
+    value = nflops * world / (norm_ms_m * 1e-3) / 1e12
+    comp_gbs = cbytes * world / (comp_ms_m * 1e-3) / 1e9
+    mflops = main_pass_flops(d_out, d_in, r)
+    main_tflops = mflops / (main_ms_m * 1e-3) / 1e12
+    main_src = os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "gemm_tc.cu")
+    comp_src = os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "compose.cu")
+    roofline = {"kernel": "k_gemm_tc main pass (U = W A^T + sum W^2 + rowsum(B o U))",
+                "bound": "tensor", "achieved": main_tflops,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": main_tflops / peaks["bf16_tflops_sustained"],
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)",
+                "frac_of_nominal": main_tflops / NOMINAL["bf16_tflops"],
+                "flops_per_launch": mflops, "ms_per_launch": main_ms_m,
+                "traffic": recorded_traffic(main_src, "main_pass_8192x8192_r384.md"),
+                "algorithmic_bytes_per_launch": 2 * (d_out * d_in + r * d_in + d_out * r) + 8 * d_out}
+    roofline_compose = {"kernel": "k_compose<bf16>", "bound": "hbm", "achieved": cbytes / (comp_ms_m * 1e-3) / 1e9,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": cbytes / (comp_ms_m * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                        "frac_of_nominal": cbytes / (comp_ms_m * 1e-3) / 1e9 / NOMINAL["hbm_gbs"],
+                        "peak_source": f"{peak_src} HBM copy", "bytes_per_launch": cbytes,
+                        "traffic": recorded_traffic(comp_src, "compose_2048x8192_bf16.md")}
+
+    # ---- end to end through the public API, from pinned host buffers
+    e2e_steps = max(3, min(args.steps, 20))
+    host = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
+            for k, v in {**norm_x, **comp_x}.items()}
+    out_h = torch.empty((T, d_out), dtype=torch.bfloat16).pin_memory()
+    g_h = torch.empty(d_out, dtype=torch.float32).pin_memory()
+    wn_h = torch.empty(d_out, dtype=torch.float32).pin_memory()
+    dbuf = sets[0]
+    norm_keys = ("W", "A", "B", "m")
+    comp_keys = ("base", "lora")
+
+    def e2e_step(ev):
+        ev[0].record(stream)
+        for k in norm_keys:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        api.dora_factored_norm(dbuf["W"], dbuf["A"], dbuf["B"], cfg.s, dbuf["m"], cfg.eps,
+                               wnorm=wn[0], g=gg[0], workspace=ws[0])
+        g_h.copy_(gg[0], non_blocking=True)
+        wn_h.copy_(wn[0], non_blocking=True)
+        ev[1].record(stream)
+        for k in comp_keys:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        api.dora_compose(dbuf["base"], dbuf["lora"], gg[0], cfg.s, out=outs[0])
+        out_h.copy_(outs[0], non_blocking=True)
+        ev[2].record(stream)
+
+    for _ in range(2):
+        e2e_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+    e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(e2e_steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for ev in e2e_evs:
+        e2e_step(ev)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_norm_ms = max_over_ranks(mean(e[0].elapsed_time(e[1]) for e in e2e_evs), world, dev)
+    e2e_comp_ms = max_over_ranks(mean(e[1].elapsed_time(e[2]) for e in e2e_evs), world, dev)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in norm_keys + comp_keys)
+    d2h = out_h.numel() * 2 + 8 * d_out
+    e2e = {"value": nflops * world / (e2e_norm_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "ms_per_step": e2e_norm_ms + e2e_comp_ms,
+           "compose": {"value": cbytes * world / (e2e_comp_ms * 1e-3) / 1e9, "unit": "GB/s"},
+           "api": "dora_factored_norm + dora_compose (Python binding of the C ABI) with "
+                  "pinned-host H2D of W, A, B, m, base, lora and D2H of wnorm, g, out"}
+
+    # ---- CPU baseline: the oracle on this host, bounded sample (rank 0, N = 1 only)
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = np.arange(0, d_out, 4)               # 2048 of 8192 rows
+        toks = np.arange(0, T, 4)                   # 512 of 2048 token rows
+        g32 = gg[0].cpu().numpy()
+        tn, tc = oracle_sample(cfg, norm_x, comp_x, g32, rows, toks)
+        cpu_value = nflops * len(rows) / d_out / tn / 1e12
+        cpu_baseline = {"value": cpu_value, "unit": "TFLOP/s", "cores": cpu_threads(),
+                        "kind": "oracle",
+                        "sample": f"float64 oracle (dense W+sBA row norms via numpy/OpenBLAS) on "
+                                  f"{len(rows)} of {d_out} rows ({tn:.2f} s), compose on "
+                                  f"{len(toks)} of {T} token rows ({tc:.2f} s); TFLOP/s uses the "
+                                  f"method's algorithmic FLOPs per row",
+                        "compose": {"value": cbytes * len(toks) / T / tc / 1e9, "unit": "GB/s"}}
+
+    if rank == 0:
+        line = {
+            "metric": json.loads(BASELINE_METRIC), "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "d_out": d_out, "d_in": d_in, "r": r, "s": cfg.s,
+                       "tokens": T, "modules_per_rank": 1,
+                       "l2": f"{N_SETS} rotating input/output sets, {set_bytes / 1e6:.0f} MB "
+                             f"of inputs each (> 129 MB L2)",
+                       "parallelism": f"replicas x{world} (one independent module per rank)"},
+            "value_definition": "algorithmic factored-norm FLOPs (2 d_out d_in r + 2 r^2 d_in + "
+                                "2 d_out r^2 + 2 d_out d_in) / norm part of each timed step",
+            "norm": {"tflops": value, "ms": norm_ms_m, "modules_per_s": world / (norm_ms_m * 1e-3),
+                     "frac_of_measured_bf16": value / peaks["bf16_tflops"],
+                     "frac_of_nominal_bf16": value / NOMINAL["bf16_tflops"]},
+            "compose": {"value": comp_gbs, "unit": "GB/s", "ms": comp_ms_m,
+                        "elements_per_s": T * d_out * world / (comp_ms_m * 1e-3),
+                        "frac_of_measured_hbm": comp_gbs / world / peaks["hbm_gbs"],
+                        "frac_of_nominal_hbm": comp_gbs / world / NOMINAL["hbm_gbs"]},
+            "roofline": roofline, "roofline_compose": roofline_compose,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
+            "cpu_baseline": cpu_baseline,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,124 @@
+"""Python binding of the dora C ABI with the same names, for torch tensors.
+
+Argument marshalling only: every step of the norm and the compose runs in the
+CUDA kernels of ``libdora.so``.  torch supplies device memory, streams and
+events; nothing here computes on tensor values.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import DORA_BF16, DORA_F32, DoraError, check
+
+_DTYPES = {torch.bfloat16: DORA_BF16, torch.float32: DORA_F32}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"dtype {t.dtype} is not supported (bfloat16 or float32)") from None
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def workspace_size(d_out: int, d_in: int, r: int, dtype: torch.dtype) -> int:
+    return int(_lib.load().dora_norm_workspace_size(d_out, d_in, r, _DTYPES[dtype]))
+
+
+def alloc_workspace(d_out: int, d_in: int, r: int, dtype: torch.dtype,
+                    device="cuda") -> torch.Tensor:
+    n = workspace_size(d_out, d_in, r, dtype)
+    if n == 0:
+        raise ValueError("invalid shape for dora_factored_norm")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def dora_factored_norm(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
+                       m: torch.Tensor, eps: float,
+                       wnorm: Optional[torch.Tensor] = None, g: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None,
+                       main_events: Optional[Tuple[torch.cuda.Event, torch.cuda.Event]] = None,
+                       ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """wnorm = ||W + s B A||_row and g = m / max(wnorm, eps), both fp32 [d_out].
+
+    W [d_out, d_in], A [r, d_in], B [d_out, r], m [d_out], all one dtype
+    (bfloat16 or float32), contiguous, on the current CUDA device."""
+    code = _dtype_code(W)
+    for t, name in ((A, "A"), (B, "B"), (m, "m")):
+        if t.dtype != W.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, W has {W.dtype}")
+    d_out, d_in = W.shape
+    r = A.shape[0]
+    if A.shape != (r, d_in) or B.shape != (d_out, r) or m.shape != (d_out,):
+        raise ValueError(f"shape mismatch: W{tuple(W.shape)} A{tuple(A.shape)} "
+                         f"B{tuple(B.shape)} m{tuple(m.shape)}")
+    if wnorm is None:
+        wnorm = torch.empty(d_out, dtype=torch.float32, device=W.device)
+    if g is None:
+        g = torch.empty(d_out, dtype=torch.float32, device=W.device)
+    if workspace is None:
+        workspace = alloc_workspace(d_out, d_in, r, W.dtype, W.device)
+    lib = _lib.load()
+    args = (_dev(W, "W"), _dev(A, "A"), _dev(B, "B"), code, d_out, d_in, r, float(s),
+            _dev(m, "m"), float(eps), _dev(wnorm, "wnorm"), _dev(g, "g"),
+            _dev(workspace, "workspace"), workspace.numel(), _stream_handle(stream))
+    if main_events is None:
+        st = lib.dora_factored_norm(*args)
+    else:
+        st = lib.dora_factored_norm_timed(*args, main_events[0].cuda_event,
+                                          main_events[1].cuda_event)
+    check(st, "dora_factored_norm")
+    return wnorm, g
+
+
+def dora_compose(base: torch.Tensor, lora: torch.Tensor, g: torch.Tensor, s: float,
+                 out: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out = (g - 1) * base + g * (s * lora); base/lora/out [T, d_out], g fp32 [d_out]."""
+    code = _dtype_code(base)
+    if lora.dtype != base.dtype or lora.shape != base.shape:
+        raise ValueError("base and lora must have the same dtype and shape")
+    if base.dim() != 2:
+        raise ValueError("base must be 2-D [T, d_out]")
+    T, d_out = base.shape
+    if g.dtype != torch.float32 or g.shape != (d_out,):
+        raise ValueError("g must be float32 [d_out]")
+    if out is None:
+        out = torch.empty_like(base)
+    elif out.dtype != base.dtype or out.shape != base.shape:
+        raise ValueError("out must match base")
+    if T == 0 or d_out == 0:
+        return out
+    st = _lib.load().dora_compose(_dev(base, "base"), _dev(lora, "lora"), _dev(g, "g"),
+                                  float(s), code, T, d_out, _dev(out, "out"),
+                                  _stream_handle(stream))
+    check(st, "dora_compose")
+    return out
+
+
+def dora_check_status(workspace: torch.Tensor,
+                      stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Device status word of the last dora_factored_norm on this workspace
+    (waits for the stream)."""
+    return int(_lib.load().dora_check_status(_dev(workspace, "workspace"),
+                                             _stream_handle(stream)))
+
+
+__all__ = ["dora_factored_norm", "dora_compose", "dora_check_status", "workspace_size",
+           "alloc_workspace", "DoraError"]

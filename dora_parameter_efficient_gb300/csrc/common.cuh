@@ -1,0 +1,99 @@
+// common.cuh -- shared declarations of the kernels behind the dora C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dora {
+
+// device status word values (same numbers as dora_status)
+constexpr int kStatusOk = 0;
+constexpr int kStatusTimeout = 5;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+// float -> bf16 bits, round to nearest even (finite inputs; NaN stays NaN)
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return static_cast<uint16_t>((u >> 16) | 0x40u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Compensated accumulation (Kahan): sum += x with the lost low part kept in c.
+__device__ __forceinline__ void kahan_add(float& sum, float& c, float x) {
+  const float y = __fsub_rn(x, c);
+  const float t = __fadd_rn(sum, y);
+  c = __fsub_rn(__fsub_rn(t, sum), y);
+  sum = t;
+}
+
+// every kernel launch of the library is counted here (dora_launch_count)
+void note_launches(int n);
+
+// ------------------------------------------------------------------ tcgen05 GEMM
+// D[128 x n_pad] = X[128-row tile x K] * Y[n_pad x K]^T in tensor memory, with
+// the epilogues of the factored norm.
+constexpr int kTcBlockM = 128;
+constexpr int kTcBlockK = 64;                 // bf16 elements per 128-byte smem row
+constexpr int kTcThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr uint32_t kTcXTileBytes = kTcBlockM * 128;
+constexpr int kTcMaxStages = 8;
+
+enum TcMode : int {
+  kTcSumSq = 1,   // per-row sum of squares of the X tiles, from shared memory
+  kTcDotB = 2,    // per-row dot of the accumulator row with the matching row of B
+  kTcStore = 4,   // store the accumulator tile, transposed, as an fp32 partial
+};
+
+struct TcParams {
+  int rows;              // valid rows of X
+  int n_pad;             // N: multiple of 16, <= 512
+  int y_box_rows;        // rows per Y TMA box (divides n_pad)
+  int k_tiles;           // K tiles in the whole K loop
+  int k_tiles_pass;      // K tiles per pass: tile kt >= k_tiles_pass reads Y1 at kt - k_tiles_pass
+  int stages;            // shared-memory pipeline depth
+  int mode;              // TcMode bits
+  int r;                 // valid accumulator columns (DotB, Store)
+  uint32_t tmem_cols;    // power of two >= max(32, n_pad)
+  const uint16_t* B;     // DotB: [rows x r] bf16
+  float* out_sumsq;      // [splits][rows]
+  float* out_dot;        // [splits][rows]
+  float* out_store;      // [splits][n_pad][n_pad]
+  int* status;
+  unsigned long long timeout_ns;
+  int inject_fault;      // test hook: the producer issues no loads
+};
+
+size_t tc_smem_bytes(int n_pad, int stages);
+int tc_pick_stages(int n_pad);
+cudaError_t launch_gemm_tc(const CUtensorMap& tx, const CUtensorMap& ty0, const CUtensorMap& ty1,
+                           const TcParams& p, int row_tiles, int splits, cudaStream_t stream);
+
+// ------------------------------------------------------------------ SIMT (fp32 inputs)
+enum SimtMode : int { kSimtSumSq = 1, kSimtDotB = 2, kSimtStore = 4 };
+constexpr int kSimtTile = 64;
+
+cudaError_t launch_gemm_simt(const float* X, const float* Y, int rows, int ncols, int K,
+                             const float* B, int ldb, float* out_sumsq, float* out_dot,
+                             float* out_store, int mode, cudaStream_t stream);
+
+// ------------------------------------------------------------------ small kernels
+cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,
+                             float* out, cudaStream_t stream);
+cudaError_t launch_gram_reduce(const float* parts, int splits, int n_pad, float* G,
+                               uint16_t* G_hi, uint16_t* G_lo, cudaStream_t stream);
+cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
+                            int n_cross, const float* pba, int n_ba, double s, const void* m,
+                            int is_bf16, double eps, float* wnorm, float* g,
+                            cudaStream_t stream);
+cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
+                           int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,
+                           cudaStream_t stream);
+
+}  // namespace dora

@@ -1,0 +1,134 @@
+// compose.cu -- the stable fused DoRA compose, a pure HBM stream.
+//
+//   out = (g - 1) * base + g * (s * lora)       ("Scaling DoRA", Chinese
+//   write-up sections 2.1 / 2.1.1; English summary "Fused Kernels")
+//
+// One read of base, one of lora, one write of out; g (one fp32 per output
+// feature, broadcast over tokens) stays in L1/L2.  The evaluation follows the
+// write-up's order -- s * lora first, then g * (.) -- and keeps the small
+// correction (g - 1) explicit, in fp32 registers.  Both products carry their
+// exact rounding error (an error-free product via FMA, Dekker's TwoProduct),
+// so the fp32 result is within about one fp32 ulp of the exact value before
+// the single rounding to the output type, even where the two terms cancel.
+//
+// Layout: base/lora/out are [T x d_out] row-major.  Rows whose byte length is
+// a multiple of 16 with 16-byte aligned pointers stream as 16-byte vectors
+// (8 bf16 or 4 fp32 per load); anything else takes the element-wise loop of
+// the same kernel.  Grid-stride, grid sized to the SM count.
+#include "common.cuh"
+
+namespace dora {
+
+namespace {
+
+__device__ __forceinline__ float compose1(float b, float l, float g, float s) {
+  const float gm1 = __fsub_rn(g, 1.0f);          // exact for g in [0.5, 2] (Sterbenz)
+  const float sl = __fmul_rn(s, l);
+  const float sl_err = fmaf(s, l, -sl);          // s*l = sl + sl_err exactly
+  const float p = __fmul_rn(gm1, b);
+  const float p_err = fmaf(gm1, b, -p);          // (g-1)*b = p + p_err exactly
+  return __fadd_rn(fmaf(g, sl, p), fmaf(g, sl_err, p_err));
+}
+
+constexpr int kUnroll = 4;
+
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+    k_compose(const void* __restrict__ base, const void* __restrict__ lora,
+              const float* __restrict__ g, float s, int64_t T, int64_t d_out,
+              void* __restrict__ out, int vec_ok) {
+  const int64_t n = T * d_out;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  constexpr int EPV = BF16 ? 8 : 4;   // elements per 16-byte vector
+  if (vec_ok) {
+    const int64_t nv = n / EPV;
+    const int64_t dv = d_out / EPV;    // vectors per row
+    const uint4* bp = static_cast<const uint4*>(base);
+    const uint4* lp = static_cast<const uint4*>(lora);
+    uint4* op = static_cast<uint4*>(out);
+    for (int64_t v0 = tid; v0 < nv; v0 += nthreads * kUnroll) {
+      uint4 bv[kUnroll], lv[kUnroll];
+      int64_t vi[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        vi[u] = v0 + u * nthreads;
+        if (vi[u] < nv) {
+          bv[u] = __ldcs(bp + vi[u]);
+          lv[u] = __ldcs(lp + vi[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (vi[u] >= nv) continue;
+        const int64_t col = (vi[u] % dv) * EPV;
+        if (BF16) {
+          const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + col));
+          const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + col) + 1);
+          const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          const uint32_t bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
+          const uint32_t lw[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = compose1(bf16_lo(bw[e]), bf16_lo(lw[e]), gv[2 * e], s);
+            const float hi = compose1(bf16_hi(bw[e]), bf16_hi(lw[e]), gv[2 * e + 1], s);
+            ow[e] = static_cast<uint32_t>(f32_to_bf16_rn(lo)) |
+                    (static_cast<uint32_t>(f32_to_bf16_rn(hi)) << 16);
+          }
+          __stcs(op + vi[u], make_uint4(ow[0], ow[1], ow[2], ow[3]));
+        } else {
+          const float4 gv = __ldg(reinterpret_cast<const float4*>(g + col));
+          float4 o;
+          o.x = compose1(__uint_as_float(bv[u].x), __uint_as_float(lv[u].x), gv.x, s);
+          o.y = compose1(__uint_as_float(bv[u].y), __uint_as_float(lv[u].y), gv.y, s);
+          o.z = compose1(__uint_as_float(bv[u].z), __uint_as_float(lv[u].z), gv.z, s);
+          o.w = compose1(__uint_as_float(bv[u].w), __uint_as_float(lv[u].w), gv.w, s);
+          __stcs(reinterpret_cast<float4*>(op) + vi[u], o);
+        }
+      }
+    }
+  } else {
+    for (int64_t i = tid; i < n; i += nthreads) {
+      const int64_t col = i % d_out;
+      if (BF16) {
+        const uint16_t b = static_cast<const uint16_t*>(base)[i];
+        const uint16_t l = static_cast<const uint16_t*>(lora)[i];
+        static_cast<uint16_t*>(out)[i] =
+            f32_to_bf16_rn(compose1(bf16_to_f32(b), bf16_to_f32(l), g[col], s));
+      } else {
+        const float b = static_cast<const float*>(base)[i];
+        const float l = static_cast<const float*>(lora)[i];
+        static_cast<float*>(out)[i] = compose1(b, l, g[col], s);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
+                           int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,
+                           cudaStream_t stream) {
+  const int64_t n = T * d_out;
+  if (n == 0) return cudaSuccess;
+  const int epv = is_bf16 ? 8 : 4;
+  const auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const int vec_ok = (d_out % epv == 0) && aligned(base) && aligned(lora) && aligned(out) &&
+                     aligned(g);
+  const int64_t work = vec_ok ? (n / epv + kUnroll - 1) / kUnroll : n;
+  int64_t blocks = (work + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (is_bf16)
+    k_compose<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(base, lora, g, s, T, d_out,
+                                                                       out, vec_ok);
+  else
+    k_compose<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(base, lora, g, s, T,
+                                                                        d_out, out, vec_ok);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dora

@@ -1,0 +1,397 @@
+// dora_api.cu -- the C ABI (include/dora.h): argument checks, workspace plan,
+// TMA descriptors and the launch sequence of the factored norm and compose.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dora.h"
+#include "common.cuh"
+
+namespace dora {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxMainSplits = 16;
+constexpr int kMaxGramSplits = 16;
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- device info
+struct DeviceInfo {
+  int sms = 0;
+  int ok = 0;   // 1: sm_10x device usable by this library, -1: not usable
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+int current_device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DORA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.ok == 0) {
+    int major = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DORA_ERR_CUDA;
+    d.sms = sms;
+    d.ok = (major == 10) ? 1 : -1;
+  }
+  if (d.ok < 0) return DORA_ERR_NO_DEVICE;
+  *out = d;
+  return DORA_OK;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major [outer x inner] bf16 matrix, box [box_outer x 64], 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTcBlockK), box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- workspace plan
+struct Plan {
+  bool bf16 = true;
+  int rp = 0;               // r rounded up to 16 (the MMA N extent)
+  int main_splits = 1;      // split-K of the main pass (tensor-core path)
+  int gram_splits = 1;
+  size_t off_status = 0, off_G = 0, off_Ghi = 0, off_Glo = 0, off_Gpart = 0;
+  size_t off_pbase = 0, off_pcross = 0, off_pba = 0, total = 0;
+  int cap_base = 0, cap_cross = 0, cap_ba = 0;
+};
+
+// Split-K count: minimise (waves x K tiles per CTA) plus a per-wave epilogue
+// cost of about two K tiles, for `units` row tiles on `sms` SMs.
+int pick_splits(int64_t row_tiles, int64_t k_tiles, int sms, int max_splits) {
+  int best = 1;
+  double best_cost = 1e300;
+  const int lim = static_cast<int>(k_tiles < max_splits ? k_tiles : max_splits);
+  for (int s = 1; s <= (lim > 0 ? lim : 1); ++s) {
+    const int64_t ctas = row_tiles * s;
+    const int64_t waves = ceil_div(ctas, sms);
+    const double cost = static_cast<double>(waves) * (ceil_div(k_tiles, s) + 2.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
+  Plan p;
+  p.bf16 = dtype == DORA_BF16;
+  p.rp = static_cast<int>(ceil_div(r, 16) * 16);
+  const int simt_cols = static_cast<int>(ceil_div(r, kSimtTile));
+  p.cap_base = kMaxMainSplits;
+  p.cap_cross = kMaxMainSplits > simt_cols ? kMaxMainSplits : simt_cols;
+  p.cap_ba = 2 > simt_cols ? 2 : simt_cols;
+  size_t off = 0;
+  p.off_status = off;
+  off += 256;
+  const size_t rp2 = static_cast<size_t>(p.rp) * p.rp;
+  p.off_G = off;
+  off = align_up(off + rp2 * 4, 256);
+  if (p.bf16) {
+    p.off_Ghi = off;
+    off = align_up(off + rp2 * 2, 256);
+    p.off_Glo = off;
+    off = align_up(off + rp2 * 2, 256);
+    p.off_Gpart = off;
+    off = align_up(off + kMaxGramSplits * rp2 * 4, 256);
+  }
+  p.off_pbase = off;
+  off = align_up(off + static_cast<size_t>(p.cap_base) * d_out * 4, 256);
+  p.off_pcross = off;
+  off = align_up(off + static_cast<size_t>(p.cap_cross) * d_out * 4, 256);
+  p.off_pba = off;
+  off = align_up(off + static_cast<size_t>(p.cap_ba) * d_out * 4, 256);
+  p.total = off;
+  (void)d_in;
+  return p;
+}
+
+bool shape_ok(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
+  return d_out >= 0 && d_in >= 0 && r >= 0 && r <= DORA_MAX_RANK &&
+         (dtype == DORA_BF16 || dtype == DORA_F32) && d_out < (int64_t(1) << 31) &&
+         d_in < (int64_t(1) << 31);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DORA_OK : DORA_ERR_CUDA; }
+
+#define DORA_TRY(expr)                       \
+  do {                                       \
+    const cudaError_t e_ = (expr);           \
+    if (e_ != cudaSuccess) return DORA_ERR_CUDA; \
+  } while (0)
+
+int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, int64_t d_out,
+                       int64_t d_in, int64_t r, float s, const void* m, float eps, float* wnorm,
+                       float* g, void* workspace, size_t workspace_bytes, void* stream_v,
+                       void* ev_begin, void* ev_end) {
+  // ------------------------------------------------ host-side checks, nothing enqueued yet
+  if (!shape_ok(d_out, d_in, r, dtype)) {
+    if (r > DORA_MAX_RANK && d_out >= 0 && d_in >= 0) return DORA_ERR_UNSUPPORTED;
+    return DORA_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(s) || !(eps > 0.f) || !std::isfinite(eps)) return DORA_ERR_INVALID_ARG;
+  if (d_out == 0) return DORA_OK;
+  const bool bf16 = dtype == DORA_BF16;
+  const size_t eb = bf16 ? 2 : 4;
+  const bool adapter = (r > 0) && (s != 0.f) && (d_in > 0);
+  if (!m || !wnorm || !g) return DORA_ERR_INVALID_ARG;
+  if (d_in > 0 && !W) return DORA_ERR_INVALID_ARG;
+  if (adapter && (!A || !B)) return DORA_ERR_INVALID_ARG;
+  const size_t vec_bytes = static_cast<size_t>(d_out) * 4;
+  if (overlap(wnorm, vec_bytes, g, vec_bytes)) return DORA_ERR_INVALID_ARG;
+  if (d_in > 0 && overlap(wnorm, vec_bytes, W, d_out * d_in * eb)) return DORA_ERR_INVALID_ARG;
+  if (d_in > 0 && overlap(g, vec_bytes, W, d_out * d_in * eb)) return DORA_ERR_INVALID_ARG;
+  if (overlap(wnorm, vec_bytes, m, d_out * eb) || overlap(g, vec_bytes, m, d_out * eb))
+    return DORA_ERR_INVALID_ARG;
+  if (d_in > 0 && ((d_in * eb) % 16 != 0 || !aligned16(W))) return DORA_ERR_UNSUPPORTED;
+  if (adapter && ((r * eb) % 16 != 0 || !aligned16(A) || !aligned16(B)))
+    return DORA_ERR_UNSUPPORTED;
+  const Plan plan = make_plan(d_out, d_in, r, dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < plan.total)
+    return DORA_ERR_WORKSPACE;
+
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + plan.off_status);
+  float* G = reinterpret_cast<float*>(ws + plan.off_G);
+  uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + plan.off_Ghi);
+  uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + plan.off_Glo);
+  float* Gpart = reinterpret_cast<float*>(ws + plan.off_Gpart);
+  float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
+  float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
+  float* pba = reinterpret_cast<float*>(ws + plan.off_pba);
+
+  DORA_TRY(cudaMemsetAsync(status, 0, 256, stream));
+
+  int n_base = 0, n_cross = 0, n_ba = 0;
+  if (d_in == 0) {
+    // W has no columns: every term is zero.
+  } else if (!adapter) {
+    // s = 0 or r = 0: only the base term (Algorithm 1 notes: no U, no G).
+    if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
+    DORA_TRY(launch_row_sumsq(W, bf16, d_out, d_in, pbase, stream));
+    if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
+    n_base = 1;
+  } else if (bf16) {
+    const int rp = plan.rp;
+    int y_box = 128;
+    while (rp % y_box) y_box >>= 1;
+    const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
+    const int stages = tc_pick_stages(rp);
+    const uint32_t tmem_cols = [&] {
+      uint32_t c = 32;
+      while (c < static_cast<uint32_t>(rp)) c <<= 1;
+      return c;
+    }();
+    CUtensorMap mW, mA_x, mA_y, mB_x, mGhi, mGlo;
+    if (!make_map_bf16(&mW, W, d_in, d_out, kTcBlockM) ||
+        !make_map_bf16(&mA_x, A, d_in, r, kTcBlockM) ||
+        !make_map_bf16(&mA_y, A, d_in, r, y_box) || !make_map_bf16(&mB_x, B, r, d_out, kTcBlockM) ||
+        !make_map_bf16(&mGhi, Ghi, rp, rp, y_box) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box))
+      return DORA_ERR_CUDA;
+
+    TcParams base{};
+    base.n_pad = rp;
+    base.y_box_rows = y_box;
+    base.stages = stages;
+    base.r = static_cast<int>(r);
+    base.tmem_cols = tmem_cols;
+    base.status = status;
+    base.timeout_ns = kDefaultTimeoutNs;
+    base.inject_fault = 0;
+
+    // G partials: X = A, Y = A
+    const int gram_tiles = static_cast<int>(ceil_div(rp, kTcBlockM));
+    const int gram_splits = pick_splits(gram_tiles, k_tiles, dev.sms, kMaxGramSplits);
+    TcParams pg = base;
+    pg.rows = static_cast<int>(r);
+    pg.k_tiles = k_tiles;
+    pg.k_tiles_pass = k_tiles;
+    pg.mode = kTcStore;
+    pg.out_store = Gpart;
+    DORA_TRY(launch_gemm_tc(mA_x, mA_y, mA_y, pg, gram_tiles, gram_splits, stream));
+    DORA_TRY(launch_gram_reduce(Gpart, gram_splits, rp, G, Ghi, Glo, stream));
+
+    // BA-norm term: X = B (K = r), Y = G_hi then G_lo; one split per pass
+    const int row_tiles = static_cast<int>(ceil_div(d_out, kTcBlockM));
+    const int kb = static_cast<int>(ceil_div(r, kTcBlockK));
+    TcParams pb = base;
+    pb.rows = static_cast<int>(d_out);
+    pb.k_tiles = 2 * kb;
+    pb.k_tiles_pass = kb;
+    pb.mode = kTcDotB;
+    pb.B = static_cast<const uint16_t*>(B);
+    pb.out_dot = pba;
+    DORA_TRY(launch_gemm_tc(mB_x, mGhi, mGlo, pb, row_tiles, 2, stream));
+    n_ba = 2;
+
+    // main pass: X = W, Y = A; base sum of squares and rowsum(B o U)
+    const int main_splits = pick_splits(row_tiles, k_tiles, dev.sms, kMaxMainSplits);
+    TcParams pm = base;
+    pm.rows = static_cast<int>(d_out);
+    pm.k_tiles = k_tiles;
+    pm.k_tiles_pass = k_tiles;
+    pm.mode = kTcSumSq | kTcDotB;
+    pm.B = static_cast<const uint16_t*>(B);
+    pm.out_sumsq = pbase;
+    pm.out_dot = pcross;
+    if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
+    DORA_TRY(launch_gemm_tc(mW, mA_y, mA_y, pm, row_tiles, main_splits, stream));
+    if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
+    n_base = n_cross = main_splits;
+  } else {
+    // fp32 inputs: CUDA-core path
+    const float* Wf = static_cast<const float*>(W);
+    const float* Af = static_cast<const float*>(A);
+    const float* Bf = static_cast<const float*>(B);
+    const int ri = static_cast<int>(r);
+    DORA_TRY(launch_gemm_simt(Af, Af, ri, ri, static_cast<int>(d_in), nullptr, 0, nullptr, nullptr,
+                              G, kSimtStore, stream));
+    DORA_TRY(launch_gemm_simt(Bf, G, static_cast<int>(d_out), ri, ri, Bf, ri, nullptr, pba,
+                              nullptr, kSimtDotB, stream));
+    n_ba = static_cast<int>(ceil_div(r, kSimtTile));
+    if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
+    DORA_TRY(launch_gemm_simt(Wf, Af, static_cast<int>(d_out), ri, static_cast<int>(d_in), Bf, ri,
+                              pbase, pcross, nullptr, kSimtSumSq | kSimtDotB, stream));
+    if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
+    n_base = 1;
+    n_cross = n_ba;
+  }
+  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, pba, n_ba,
+                           static_cast<double>(s), m, bf16, static_cast<double>(eps), wnorm, g,
+                           stream));
+  return DORA_OK;
+}
+
+}  // namespace
+}  // namespace dora
+
+using namespace dora;
+
+extern "C" {
+
+size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
+  if (!shape_ok(d_out, d_in, r, dtype)) return 0;
+  return make_plan(d_out, d_in, r, dtype).total;
+}
+
+int dora_factored_norm(const void* W, const void* A, const void* B, int dtype, int64_t d_out,
+                       int64_t d_in, int64_t r, float s, const void* m, float eps, float* wnorm,
+                       float* g, void* workspace, size_t workspace_bytes, void* stream) {
+  return factored_norm_impl(W, A, B, dtype, d_out, d_in, r, s, m, eps, wnorm, g, workspace,
+                            workspace_bytes, stream, nullptr, nullptr);
+}
+
+int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dtype,
+                             int64_t d_out, int64_t d_in, int64_t r, float s, const void* m,
+                             float eps, float* wnorm, float* g, void* workspace,
+                             size_t workspace_bytes, void* stream, void* ev_main_begin,
+                             void* ev_main_end) {
+  return factored_norm_impl(W, A, B, dtype, d_out, d_in, r, s, m, eps, wnorm, g, workspace,
+                            workspace_bytes, stream, ev_main_begin, ev_main_end);
+}
+
+int dora_compose(const void* base, const void* lora, const float* g, float s, int dtype,
+                 int64_t T, int64_t d_out, void* out, void* stream) {
+  if (T < 0 || d_out < 0 || (dtype != DORA_BF16 && dtype != DORA_F32) || !std::isfinite(s))
+    return DORA_ERR_INVALID_ARG;
+  if (T == 0 || d_out == 0) return DORA_OK;
+  if (!base || !lora || !g || !out) return DORA_ERR_INVALID_ARG;
+  const size_t eb = dtype == DORA_BF16 ? 2 : 4;
+  const size_t nbytes = static_cast<size_t>(T) * d_out * eb;
+  // in place is fine (each element is read before it is written by the same
+  // thread); a partial overlap is not
+  if ((out != base && overlap(out, nbytes, base, nbytes)) ||
+      (out != lora && overlap(out, nbytes, lora, nbytes)))
+    return DORA_ERR_INVALID_ARG;
+  if (overlap(g, static_cast<size_t>(d_out) * 4, out, nbytes)) return DORA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  return cuda_status(launch_compose(base, lora, g, s, dtype == DORA_BF16, T, d_out, out, dev.sms,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+int dora_check_status(const void* workspace, void* stream) {
+  if (!workspace) return DORA_ERR_INVALID_ARG;
+  int h = -1;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return DORA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DORA_ERR_CUDA;
+  return h;
+}
+
+const char* dora_status_string(int status) {
+  switch (status) {
+    case DORA_OK: return "DORA_OK";
+    case DORA_ERR_INVALID_ARG: return "DORA_ERR_INVALID_ARG: invalid argument";
+    case DORA_ERR_UNSUPPORTED: return "DORA_ERR_UNSUPPORTED: shape, stride or alignment not supported";
+    case DORA_ERR_WORKSPACE: return "DORA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case DORA_ERR_CUDA: return "DORA_ERR_CUDA: a CUDA call failed";
+    case DORA_ERR_TIMEOUT: return "DORA_ERR_TIMEOUT: a device pipeline wait ran out of time";
+    case DORA_ERR_NO_DEVICE: return "DORA_ERR_NO_DEVICE: no sm_100-family GPU is current";
+    default: return "unknown dora_status";
+  }
+}
+
+int dora_version(void) { return (1 << 16) | 0; }
+
+uint64_t dora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+/*
+ * dora.h -- C ABI of the DoRA per-module hot path on one GB300 (sm_103a).
+ *
+ * Two operations, both defined in "Scaling DoRA: High-Rank Adaptation via
+ * Factored Norms and Fused Kernels" (Zelenin, Zhuravlyova):
+ *
+ *   dora_factored_norm  wnorm_j = || W_j + s (B A)_j ||_2,  g_j = m_j / max(wnorm_j, eps)
+ *       The DoRA weight is W' = m * (W + sBA) / ||W + sBA||_row (English summary,
+ *       "The Problem").  The row norm is evaluated through the factored identity
+ *       ||W+sBA||^2_row = ||W||^2_row + 2s rowsum(B o U) + s^2 rowsum((BG) o B),
+ *       U = W A^T, G = A A^T (English summary, "Factored Norm"; Chinese write-up
+ *       sections 1.2 and 1.2.1), clamped at zero under the root and divided
+ *       with eps as a floor (Chinese write-up section 1.2.2; Algorithm 1 of
+ *       section 5.1).  The dense product BA is never formed.
+ *
+ *   dora_compose        out = (g - 1) * base + g * (s * lora)
+ *       The numerically stable compose (Chinese write-up sections 2.1 and
+ *       2.1.1; English summary, "Fused Kernels"), one pass, fp32 registers,
+ *       stored once.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, row-major, contiguous, in device memory (any
+ *     pointer the CUDA runtime can address from the device: cudaMalloc'd,
+ *     managed, or torch-allocated).  The caller owns every buffer; the
+ *     library allocates nothing and keeps no per-call state.
+ *   - Element type `dtype` is DORA_BF16 (bfloat16 bit patterns) or DORA_F32.
+ *     It applies to W, A, B, m, base, lora and out.  wnorm and g are always
+ *     float32.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Argument checks run on the host before anything is
+ *     enqueued; on an argument error nothing is launched.
+ *   - Return value: a dora_status.  DORA_ERR_CUDA means a CUDA runtime call
+ *     failed while enqueueing (the stream may hold part of the work).
+ *     Failures detected on the device (a pipeline wait that ran out of its
+ *     time limit) are recorded in the workspace and reported by
+ *     dora_check_status.
+ */
+#ifndef DORA_H_
+#define DORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dora_status {
+    DORA_OK = 0,
+    DORA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, aliasing, bad dtype */
+    DORA_ERR_UNSUPPORTED = 2,  /* legal but outside what the kernels handle: r > 512,
+                                  a row stride that is not a multiple of 16 bytes,
+                                  a pointer not 16-byte aligned (norm only) */
+    DORA_ERR_WORKSPACE = 3,    /* workspace null, misaligned or too small */
+    DORA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    DORA_ERR_TIMEOUT = 5,      /* device side: a bounded pipeline wait expired */
+    DORA_ERR_NO_DEVICE = 6     /* no usable sm_100-family device for this library */
+} dora_status;
+
+typedef enum dora_dtype {
+    DORA_BF16 = 0,
+    DORA_F32 = 1
+} dora_dtype;
+
+/* Largest adapter rank the norm supports: U = W A^T for a 128-row tile lives
+ * in tensor memory, 512 fp32 columns per SM. */
+#define DORA_MAX_RANK 512
+
+/*
+ * Bytes of device workspace dora_factored_norm needs for this shape.
+ * The workspace holds the Gram matrix G = A A^T (fp32 and a bf16 hi/lo split),
+ * per-split partial sums of the three norm terms, and a device status word;
+ * at d_out = d_in = 8192, r = 512 (fp32) it is about 17 MB, independent of d_in.
+ * Returns 0 for an invalid shape (negative sizes, bad dtype, r > DORA_MAX_RANK).
+ */
+size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtype);
+
+/*
+ * Factored row norm and magnitude scale of one DoRA module.
+ *
+ *   W      [d_out x d_in]  frozen base weight, dtype
+ *   A      [r x d_in]      LoRA down projection, dtype
+ *   B      [d_out x r]     LoRA up projection, dtype
+ *   s      LoRA scale (alpha / r or any real); s == 0 or r == 0 skips the
+ *          cross and BA-norm terms (Algorithm 1 notes, section 5.1)
+ *   m      [d_out]         DoRA magnitude, dtype
+ *   eps    floor of the divisor in g = m / max(wnorm, eps) (eps > 0)
+ *   wnorm  [d_out] float32 output, the row norm ||W + sBA||_row
+ *   g      [d_out] float32 output, m / max(wnorm, eps)
+ *   workspace / workspace_bytes  device scratch of at least
+ *          dora_norm_workspace_size(d_out, d_in, r, dtype) bytes, 256-byte
+ *          aligned; its contents need no initialisation and are overwritten.
+ *          One workspace must not be used by two calls in flight at once.
+ *   stream cudaStream_t
+ *
+ * Requirements (else DORA_ERR_UNSUPPORTED): d_in * elem_size and r * elem_size
+ * multiples of 16 bytes; W, A, B 16-byte aligned; r <= DORA_MAX_RANK.
+ * wnorm and g must not overlap each other or any input.
+ * Precision: products of the stored inputs are exact in fp32, every sum is
+ * accumulated in fp32, the three terms are assembled, square-rooted and
+ * divided in fp64 and rounded once to fp32.
+ */
+int dora_factored_norm(const void* W, const void* A, const void* B, int dtype,
+                       int64_t d_out, int64_t d_in, int64_t r, float s,
+                       const void* m, float eps, float* wnorm, float* g,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Same as dora_factored_norm, and records `ev_main_begin` / `ev_main_end`
+ * (cudaEvent_t, either may be NULL) on `stream` immediately before and after
+ * the launch of the U = W A^T main-pass kernel, so a caller can time that
+ * kernel alone with cudaEventElapsedTime.
+ */
+int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dtype,
+                             int64_t d_out, int64_t d_in, int64_t r, float s,
+                             const void* m, float eps, float* wnorm, float* g,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* ev_main_begin, void* ev_main_end);
+
+/*
+ * Stable fused compose.
+ *
+ *   base, lora  [T x d_out]  dtype (base = the frozen layer's output, lora =
+ *               the adapter branch's output, one row per token)
+ *   g           [d_out] float32, one scale per output feature, broadcast over T
+ *   s           LoRA scale
+ *   out         [T x d_out]  dtype; may equal base or lora (in place), must not
+ *               partially overlap them
+ *
+ * Evaluation order: s * lora first, then g * (.), plus (g - 1) * base with the
+ * exact rounding error of that product carried (an error-free product), all in
+ * fp32 registers, rounded once to dtype.  T == 0 or d_out == 0 is a no-op.
+ * Any alignment and any d_out are accepted (the 16-byte vector path covers
+ * aligned rows, the same kernel handles the rest element by element).
+ */
+int dora_compose(const void* base, const void* lora, const float* g, float s,
+                 int dtype, int64_t T, int64_t d_out, void* out, void* stream);
+
+/*
+ * Waits for `stream`, then reads the device status word of `workspace` (as
+ * last written by dora_factored_norm on it): DORA_OK, or DORA_ERR_TIMEOUT if
+ * a kernel gave up on a pipeline wait (its outputs are then undefined, the
+ * CUDA context stays usable).  Returns DORA_ERR_CUDA if the copy fails.
+ */
+int dora_check_status(const void* workspace, void* stream);
+
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all devices, all entry points); a diagnostic counter. */
+uint64_t dora_launch_count(void);
+
+/* Static, human-readable name of a dora_status value. */
+const char* dora_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+int dora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DORA_H_ */
