@@ -34,6 +34,9 @@ SIGNATURES = {
     "dora_factored_norm_timed": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
                                                 ctypes.c_float, _P, ctypes.c_float, _P, _P, _P,
                                                 ctypes.c_size_t, _P, _P, _P]),
+    "dora_factored_norm_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
+                                                  ctypes.c_float, _P, ctypes.c_float, _P, _P,
+                                                  _P]),
     "dora_compose": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64, _P, _P]),
     "dora_check_status": (ctypes.c_int, [_P, _P]),
     "dora_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -120,5 +120,23 @@ def dora_check_status(workspace: torch.Tensor,
                                              _stream_handle(stream)))
 
 
-__all__ = ["dora_factored_norm", "dora_compose", "dora_check_status", "workspace_size",
-           "alloc_workspace", "DoraError"]
+def dora_factored_norm_noalloc(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
+                               m: torch.Tensor, eps: float, wnorm: torch.Tensor,
+                               g: torch.Tensor,
+                               stream: Optional[torch.cuda.Stream] = None) -> None:
+    """dora_factored_norm for callers that cannot allocate device memory.
+
+    The caller passes every input and both fp32 [d_out] outputs; the library
+    uses its own fixed 32 MiB device scratch (shared by all calls on a device,
+    so calls must not overlap on the GPU) and allocates nothing."""
+    code = _dtype_code(W)
+    d_out, d_in = W.shape
+    r = A.shape[0]
+    st = _lib.load().dora_factored_norm_noalloc(
+        _dev(W, "W"), _dev(A, "A"), _dev(B, "B"), code, d_out, d_in, r, float(s), _dev(m, "m"),
+        float(eps), _dev(wnorm, "wnorm"), _dev(g, "g"), _stream_handle(stream))
+    check(st, "dora_factored_norm_noalloc")
+
+
+__all__ = ["dora_factored_norm", "dora_factored_norm_noalloc", "dora_compose",
+           "dora_check_status", "workspace_size", "alloc_workspace", "DoraError"]

@@ -318,6 +318,30 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   return DORA_OK;
 }
 
+// ---------------------------------------------------------------- allocation-free variant
+// Scratch of dora_factored_norm_noalloc: a file-scope device array, so callers
+// that cannot allocate device memory still get a workspace.  Every device
+// that loads this library holds it until the process exits.  In host code the
+// name is only a stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DORA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DORA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DORA_OK;
+}
+
 }  // namespace
 }  // namespace dora
 
@@ -344,6 +368,22 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
                              void* ev_main_end) {
   return factored_norm_impl(W, A, B, dtype, d_out, d_in, r, s, m, eps, wnorm, g, workspace,
                             workspace_bytes, stream, ev_main_begin, ev_main_end);
+}
+
+int dora_factored_norm_noalloc(const void* W, const void* A, const void* B, int dtype,
+                               int64_t d_out, int64_t d_in, int64_t r, float s, const void* m,
+                               float eps, float* wnorm, float* g, void* stream) {
+  // Refuse shapes whose workspace does not fit the built-in scratch before
+  // touching the device.
+  if (!shape_ok(d_out, d_in, r, dtype))
+    return (r > DORA_MAX_RANK && d_out >= 0 && d_in >= 0) ? DORA_ERR_UNSUPPORTED
+                                                          : DORA_ERR_INVALID_ARG;
+  if (make_plan(d_out, d_in, r, dtype).total > kNoAllocScratchBytes) return DORA_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const int st = noalloc_scratch(&scratch);
+  if (st != DORA_OK) return st;
+  return factored_norm_impl(W, A, B, dtype, d_out, d_in, r, s, m, eps, wnorm, g, scratch,
+                            kNoAllocScratchBytes, stream, nullptr, nullptr);
 }
 
 int dora_compose(const void* base, const void* lora, const float* g, float s, int dtype,

@@ -69,8 +69,9 @@ typedef enum dora_dtype {
 /*
  * Bytes of device workspace dora_factored_norm needs for this shape.
  * The workspace holds the Gram matrix G = A A^T (fp32 and a bf16 hi/lo split),
- * per-split partial sums of the three norm terms, and a device status word;
- * at d_out = d_in = 8192, r = 512 (fp32) it is about 17 MB, independent of d_in.
+ * per-split partial sums of the three norm terms, and a device status word.
+ * It does not depend on d_in: about 11.7 MB at d_out = 8192, r = 384 (bf16)
+ * and 2.3 MB at d_out = 8192, r = 512 (fp32).
  * Returns 0 for an invalid shape (negative sizes, bad dtype, r > DORA_MAX_RANK).
  */
 size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtype);
@@ -116,6 +117,39 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
                              const void* m, float eps, float* wnorm, float* g,
                              void* workspace, size_t workspace_bytes, void* stream,
                              void* ev_main_begin, void* ev_main_end);
+
+/*
+ * dora_factored_norm without a caller-supplied workspace: it allocates no
+ * device memory at any point.  The paper has no counterpart; this entry point
+ * exists for callers that cannot allocate device memory -- for example a
+ * plug-in running inside a host program whose allocator owns all of the
+ * device's free memory and offers it no hook, or code on a path where
+ * cudaMalloc/cudaFree are off limits because they synchronize the device and
+ * can fail under memory pressure.
+ *
+ * Arguments, results and requirements are those of dora_factored_norm.  The
+ * workspace is instead a 32 MiB array in the library's own device memory
+ * (a file-scope __device__ array): every GPU that loads the library holds it
+ * until the process exits.  With bf16 inputs 32 MiB covers d_out up to
+ * 91 748 rows at r = 512 (150 901 at r = 384, 238 048 at r = 128; fp32 inputs
+ * need less); a shape whose
+ * dora_norm_workspace_size exceeds 32 MiB is refused with DORA_ERR_WORKSPACE
+ * before anything is enqueued.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (every value a call reads from it, the call itself writes
+ *     first).  Calls that overlap on the GPU race: issue them on one stream,
+ *     or otherwise order them.
+ *   - A device-side pipeline timeout is recorded in the shared array and is
+ *     not reported by this entry point; use dora_factored_norm with your own
+ *     workspace and dora_check_status where that matters.
+ */
+int dora_factored_norm_noalloc(const void* W, const void* A, const void* B, int dtype,
+                               int64_t d_out, int64_t d_in, int64_t r, float s,
+                               const void* m, float eps, float* wnorm, float* g,
+                               void* stream);
 
 /*
  * Stable fused compose.
