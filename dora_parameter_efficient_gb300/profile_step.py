@@ -1,0 +1,62 @@
+"""Run the hot path (factored norm + compose) of one synthetic workload for a few
+steps and print per-step CUDA-event times; meant as the target of profilers
+(ncu), which want a short program with few launches.
+
+    python -m dora_parameter_efficient_gb300.profile_step --config 1 --steps 3
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dora_parameter_efficient_gb300 import api  # noqa: E402
+from synthetic import configs, gen  # noqa: E402
+
+
+def to_dev(a: np.ndarray, dtype: str) -> torch.Tensor:
+    if dtype == configs.BF16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--module", type=int, default=0)
+    ap.add_argument("--steps", type=int, default=3)
+    args = ap.parse_args()
+    cfg = configs.get(args.config)
+    x = gen.norm_inputs(cfg, module=args.module)
+    c = gen.compose_inputs(cfg, module=args.module)
+    W, A, B, m = (to_dev(x[k], cfg.dtype) for k in ("W", "A", "B", "m"))
+    base, lora = to_dev(c["base"], cfg.dtype), to_dev(c["lora"], cfg.dtype)
+    d_out, d_in = W.shape
+    ws = api.alloc_workspace(d_out, d_in, A.shape[0], W.dtype)
+    wn = torch.empty(d_out, dtype=torch.float32, device="cuda")
+    g = torch.empty(d_out, dtype=torch.float32, device="cuda")
+    out = torch.empty_like(base)
+    for i in range(args.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        api.dora_factored_norm(W, A, B, cfg.s, m, cfg.eps, wnorm=wn, g=g, workspace=ws)
+        e[1].record()
+        api.dora_compose(base, lora, g, cfg.s, out=out)
+        e[2].record()
+        torch.cuda.synchronize()
+        print(f"step {i}: norm {e[0].elapsed_time(e[1]) * 1e3:.1f} us, "
+              f"compose {e[1].elapsed_time(e[2]) * 1e3:.1f} us")
+    status = api.dora_check_status(ws)
+    print("status", status)
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
