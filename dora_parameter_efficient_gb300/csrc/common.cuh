@@ -75,6 +75,37 @@ int tc_pick_stages(int n_pad);
 cudaError_t launch_gemm_tc(const CUtensorMap& tx, const CUtensorMap& ty0, const CUtensorMap& ty1,
                            const TcParams& p, int row_tiles, int splits, cudaStream_t stream);
 
+// ------------------------------------------------------------------ CTA-pair main pass
+// D [256-row pair tile x n0+n1] = X * Y^T over the K tiles of one work item,
+// M = 256 per CTA pair (tcgen05 cta_group::2), persistent over items.
+struct PairParams {
+  int rows;              // d_out
+  int n0, n1;            // N of the first / second MMA (n1 = 0 when r <= 256)
+  int y_box_rows;        // rows per Y TMA box (divides n0/2 and n1/2)
+  int kt_w;              // K tiles of (W, A)
+  int kt_b;              // K tiles of (B, G'_hi), and again of (B, G'_lo)
+  int splits;            // K splits per pair tile
+  int pair_tiles;        // ceil(d_out / 256)
+  int stages;
+  int r;
+  int prefetch;          // W tiles pulled into L2 this many tiles ahead
+  uint32_t tmem_cols;
+  const uint16_t* B;     // [rows x r] bf16
+  const uint16_t* W;     // [rows x d_in] bf16 (read directly for the sum of squares)
+  int d_in;
+  float* out_sumsq;      // [splits][rows]
+  float* out_dot;        // [splits][rows]
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+size_t pair_smem_bytes(int n_pad, int stages);
+int pair_pick_stages(int n_pad);
+int pair_max_clusters(size_t smem_bytes);
+cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const CUtensorMap& tB,
+                             const CUtensorMap& tGhi, const CUtensorMap& tGlo, const PairParams& p,
+                             int clusters, cudaStream_t stream);
+
 // ------------------------------------------------------------------ SIMT (fp32 inputs)
 enum SimtMode : int { kSimtSumSq = 1, kSimtDotB = 2, kSimtStore = 4 };
 constexpr int kSimtTile = 64;
@@ -87,7 +118,7 @@ cudaError_t launch_gemm_simt(const float* X, const float* Y, int rows, int ncols
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,
                              float* out, cudaStream_t stream);
 cudaError_t launch_gram_reduce(const float* parts, int splits, int n_pad, float* G,
-                               uint16_t* G_hi, uint16_t* G_lo, cudaStream_t stream);
+                               uint16_t* G_hi, uint16_t* G_lo, float scale, cudaStream_t stream);
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
                             int n_cross, const float* pba, int n_ba, double s, const void* m,
                             int is_bf16, double eps, float* wnorm, float* g,

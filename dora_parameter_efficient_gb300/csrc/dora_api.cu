@@ -8,7 +8,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/dora.h"
+#include "dora.h"
 #include "common.cuh"
 
 namespace dora {
@@ -155,6 +155,32 @@ bool shape_ok(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
          d_in < (int64_t(1) << 31);
 }
 
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// K splits of the pair main pass: minimise (items per cluster) x (K tiles per
+// item + about three tiles of epilogue), items = pair_tiles x splits.
+int pick_pair_splits(int64_t pair_tiles, int64_t k_tiles, int clusters, int max_splits) {
+  int best = 1;
+  double best_cost = 1e300;
+  const int lim = static_cast<int>(k_tiles < max_splits ? k_tiles : max_splits);
+  for (int s = 1; s <= (lim > 0 ? lim : 1); ++s) {
+    const int64_t rounds = ceil_div(pair_tiles * s, clusters);
+    const double cost = static_cast<double>(rounds) * (ceil_div(k_tiles, s) + 3.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -228,72 +254,82 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
     n_base = 1;
   } else if (bf16) {
+    // G = A A^T (split-K partials on the single-CTA tensor-core kernel), then
+    // G' = (s/2) G split into two bf16 terms, then the CTA-pair main pass with
+    // the BA-norm tiles folded into its K loop.
     const int rp = plan.rp;
-    int y_box = 128;
-    while (rp % y_box) y_box >>= 1;
+    int y_box1 = 128;                       // single-CTA kernel: Y box rows dividing rp
+    while (rp % y_box1) y_box1 >>= 1;
     const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
-    const int stages = tc_pick_stages(rp);
     const uint32_t tmem_cols = [&] {
       uint32_t c = 32;
       while (c < static_cast<uint32_t>(rp)) c <<= 1;
       return c;
     }();
-    CUtensorMap mW, mA_x, mA_y, mB_x, mGhi, mGlo;
+    // N split of the pair MMAs: each CTA of the pair holds half of every chunk
+    const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
+    const int n1 = rp - n0;
+    const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
+    CUtensorMap mW, mA_x, mA_y1, mA_y2, mB_x, mGhi, mGlo;
     if (!make_map_bf16(&mW, W, d_in, d_out, kTcBlockM) ||
         !make_map_bf16(&mA_x, A, d_in, r, kTcBlockM) ||
-        !make_map_bf16(&mA_y, A, d_in, r, y_box) || !make_map_bf16(&mB_x, B, r, d_out, kTcBlockM) ||
-        !make_map_bf16(&mGhi, Ghi, rp, rp, y_box) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box))
+        !make_map_bf16(&mA_y1, A, d_in, r, y_box1) ||
+        !make_map_bf16(&mA_y2, A, d_in, r, y_box2) ||
+        !make_map_bf16(&mB_x, B, r, d_out, kTcBlockM) ||
+        !make_map_bf16(&mGhi, Ghi, rp, rp, y_box2) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box2))
       return DORA_ERR_CUDA;
 
-    TcParams base{};
-    base.n_pad = rp;
-    base.y_box_rows = y_box;
-    base.stages = stages;
-    base.r = static_cast<int>(r);
-    base.tmem_cols = tmem_cols;
-    base.status = status;
-    base.timeout_ns = kDefaultTimeoutNs;
-    base.inject_fault = 0;
-
-    // G partials: X = A, Y = A
-    const int gram_tiles = static_cast<int>(ceil_div(rp, kTcBlockM));
-    const int gram_splits = pick_splits(gram_tiles, k_tiles, dev.sms, kMaxGramSplits);
-    TcParams pg = base;
+    TcParams pg{};
     pg.rows = static_cast<int>(r);
+    pg.n_pad = rp;
+    pg.y_box_rows = y_box1;
     pg.k_tiles = k_tiles;
     pg.k_tiles_pass = k_tiles;
+    pg.stages = tc_pick_stages(rp);
     pg.mode = kTcStore;
+    pg.r = static_cast<int>(r);
+    pg.tmem_cols = tmem_cols;
     pg.out_store = Gpart;
-    DORA_TRY(launch_gemm_tc(mA_x, mA_y, mA_y, pg, gram_tiles, gram_splits, stream));
-    DORA_TRY(launch_gram_reduce(Gpart, gram_splits, rp, G, Ghi, Glo, stream));
+    pg.status = status;
+    pg.timeout_ns = kDefaultTimeoutNs;
+    const int gram_tiles = static_cast<int>(ceil_div(rp, kTcBlockM));
+    const int gram_splits = pick_splits(gram_tiles, k_tiles, dev.sms, kMaxGramSplits);
+    DORA_TRY(launch_gemm_tc(mA_x, mA_y1, mA_y1, pg, gram_tiles, gram_splits, stream));
+    DORA_TRY(launch_gram_reduce(Gpart, gram_splits, rp, G, Ghi, Glo, 0.5f * s, stream));
 
-    // BA-norm term: X = B (K = r), Y = G_hi then G_lo; one split per pass
-    const int row_tiles = static_cast<int>(ceil_div(d_out, kTcBlockM));
-    const int kb = static_cast<int>(ceil_div(r, kTcBlockK));
-    TcParams pb = base;
-    pb.rows = static_cast<int>(d_out);
-    pb.k_tiles = 2 * kb;
-    pb.k_tiles_pass = kb;
-    pb.mode = kTcDotB;
-    pb.B = static_cast<const uint16_t*>(B);
-    pb.out_dot = pba;
-    DORA_TRY(launch_gemm_tc(mB_x, mGhi, mGlo, pb, row_tiles, 2, stream));
-    n_ba = 2;
 
-    // main pass: X = W, Y = A; base sum of squares and rowsum(B o U)
-    const int main_splits = pick_splits(row_tiles, k_tiles, dev.sms, kMaxMainSplits);
-    TcParams pm = base;
-    pm.rows = static_cast<int>(d_out);
-    pm.k_tiles = k_tiles;
-    pm.k_tiles_pass = k_tiles;
-    pm.mode = kTcSumSq | kTcDotB;
-    pm.B = static_cast<const uint16_t*>(B);
-    pm.out_sumsq = pbase;
-    pm.out_dot = pcross;
+    PairParams pp{};
+    pp.rows = static_cast<int>(d_out);
+    pp.n0 = n0;
+    pp.n1 = n1;
+    pp.y_box_rows = y_box2;
+    pp.kt_w = k_tiles;
+    pp.kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+    pp.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
+    pp.stages = pair_pick_stages(rp);
+    const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages));
+    if (clusters_max <= 0) return DORA_ERR_CUDA;
+    pp.splits = pick_pair_splits(pp.pair_tiles, pp.kt_w + 2 * pp.kt_b, clusters_max,
+                                 kMaxMainSplits);
+    pp.r = static_cast<int>(r);
+    pp.prefetch = 4;
+    pp.tmem_cols = tmem_cols;
+    pp.B = static_cast<const uint16_t*>(B);
+    pp.W = static_cast<const uint16_t*>(W);
+    pp.d_in = static_cast<int>(d_in);
+    pp.out_sumsq = pbase;
+    pp.out_dot = pcross;
+    pp.status = status;
+    pp.timeout_ns = kDefaultTimeoutNs;
+    const int items = pp.pair_tiles * pp.splits;
+    const int clusters = items < clusters_max ? items : clusters_max;
     if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
-    DORA_TRY(launch_gemm_tc(mW, mA_y, mA_y, pm, row_tiles, main_splits, stream));
+    DORA_TRY(launch_gemm_pair(mW, mA_y2, mB_x, mGhi, mGlo, pp, clusters, stream));
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
-    n_base = n_cross = main_splits;
+    // sum over splits of rowsum(B o D) = cross + (s/2) ba: the finalize's
+    // 2s * cross term then carries the BA-norm term too
+    n_base = n_cross = pp.splits;
+    n_ba = 0;
   } else {
     // fp32 inputs: CUDA-core path
     const float* Wf = static_cast<const float*>(W);

@@ -1,0 +1,437 @@
+// gemm_pair.cu -- the main pass of the factored norm on CTA pairs (bf16 inputs).
+//
+// What it computes ("Scaling DoRA", Chinese write-up section 1.2.1 and
+// Algorithm 1 of section 5.1; English summary "Factored Norm"), for every
+// output row j and every split of the K range:
+//
+//   sumsq_j  = sum_k W_jk^2                       over the split's W columns
+//   dot_j    = rowsum(B_j o D_j),  D = W A^T + (s/2) B G
+//
+// The BA-norm GEMM B G is folded into the same K loop: after the d_in/64 tiles
+// of (W, A) come the r/64 tiles of (B, G'_hi) and of (B, G'_lo), where
+// G'_hi + G'_lo = (s/2) G (two bf16 terms, computed beforehand).  Because the
+// epilogue is linear in D, summing dot over the splits gives
+// cross + (s/2) ba, and 2s (cross + (s/2) ba) = 2s cross + s^2 ba is exactly
+// what the norm needs; the finalize kernel adds the base term.
+//
+// Tiling for sm_103a:
+//   * a cluster of 2 CTAs on 2 SMs forms one tcgen05 "CTA pair": the even CTA
+//     issues tcgen05.mma.cta_group::2 with M = 256 (128 rows of W in each
+//     CTA's shared memory), N = r padded to 16 (each CTA holds half of the
+//     N rows of the A / G' tile), so each SM stages 16 KB of W and only half
+//     of the [r x 64] A tile per K step;
+//   * the accumulator D [128 x r] of each CTA lives in its own tensor memory;
+//   * warp 0 of each CTA issues the TMA loads of its half; all loads of a
+//     stage complete on the even CTA's `full` barrier; the even CTA's MMA
+//     thread waits on it and commits `empty` to both CTAs -- the only
+//     hand-off on the shared-memory pipeline;
+//   * warps 2-5 of each CTA stay off that pipeline: while the MMAs run they
+//     stream their 128 rows of W straight from global memory (coalesced,
+//     4 rows x 128 bytes per warp instruction) for the sum of squares, then
+//     read D rows from tensor memory (tcgen05.ld) and dot them with B;
+//   * the grid is persistent: cluster c processes work items c, c + C, ...,
+//     an item being (256-row tile, K split); the TMA producer runs ahead into
+//     the next item while the epilogue drains the accumulator.
+// Every wait is bounded by %globaltimer; on expiry the kernel records a
+// timeout in the status word, stops issuing, drains what it issued and exits.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dora {
+
+namespace {
+
+// Sum of squares of 8 bf16 values.
+__device__ __forceinline__ float sumsq8(const uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = bf16_lo(w[i]), b = bf16_hi(w[i]);
+    acc = fmaf(a, a, acc);
+    acc = fmaf(b, b, acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Columns [32c, 32c + 32) of one row of B (bf16); columns past r read as 0.
+constexpr int kMaxChunks = 512 / 32;
+constexpr int kBLookahead = 4;
+
+__device__ __forceinline__ void load_b_chunk(const uint16_t* brow, int c, int r, bool valid,
+                                             uint4 (&dst)[4]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    if (valid && c * 32 + v * 8 < r)
+      dst[v] = __ldg(reinterpret_cast<const uint4*>(brow + c * 32) + v);
+    else
+      dst[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void item_range(const PairParams& p, int item, int& tile, int& split,
+                                           int& kb, int& ke) {
+  tile = item / p.splits;
+  split = item - tile * p.splits;
+  const int ktot = p.kt_w + 2 * p.kt_b;
+  kb = static_cast<int>((static_cast<long long>(ktot) * split) / p.splits);
+  ke = static_cast<int>((static_cast<long long>(ktot) * (split + 1)) / p.splits);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tA,
+                const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tGhi,
+                const __grid_constant__ CUtensorMap tGlo, const PairParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t half_rows = static_cast<uint32_t>(p.n0 + p.n1) / 2u;
+  const uint32_t stage_bytes = kTcXTileBytes + half_rows * 128u;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
+  uint64_t* empty = full + p.stages;
+  uint64_t* accum_full = empty + p.stages;
+  uint64_t* accum_empty = accum_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs, 1: its peer
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(num_clusters_x());
+  const int n_items = p.pair_tiles * p.splits;
+  const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum_full, 1);
+    mbar_init(accum_empty, 8);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tW);
+    tma_prefetch_desc(&tA);
+    tma_prefetch_desc(&tB);
+    tma_prefetch_desc(&tGhi);
+    tma_prefetch_desc(&tGlo);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, p.tmem_cols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync();          // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_stream = l2_policy_evict_first();
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint32_t full0 = map_to_rank(smem_u32(full), 0);
+      const int h0 = p.n0 / 2, h1 = p.n1 / 2;
+      uint32_t it = 0;
+      bool stop = false;
+      for (int item = cid; item < n_items && !stop; item += ncl) {
+        int tile, split, kb, ke;
+        item_range(p, item, tile, split, kb, ke);
+        const int row0 = tile * 256 + static_cast<int>(rank) * 128;
+        for (int kt = kb; kt < ke; ++kt, ++it) {
+          const uint32_t s = it % p.stages;
+          const uint32_t use = it / p.stages;
+          if (it >= static_cast<uint32_t>(p.stages) &&
+              !mbar_wait(&empty[s], (use - 1) & 1u, deadline)) {
+            atomicExch(p.status, kStatusTimeout);
+            *abort_flag = 1;
+          }
+          if (*abort_flag) {
+            stop = true;
+            break;
+          }
+          const CUtensorMap* xm;
+          const CUtensorMap* ym;
+          int kx;
+          if (kt < p.kt_w) {
+            xm = &tW; ym = &tA; kx = kt * kTcBlockK;
+            // pull a later W tile of this item into L2 while this one loads
+            const int kpf = kt + p.prefetch;
+            if (kpf < ke && kpf < p.kt_w) tma_prefetch_l2_2d(&tW, kpf * kTcBlockK, row0);
+          } else if (kt < p.kt_w + p.kt_b) {
+            xm = &tB; ym = &tGhi; kx = (kt - p.kt_w) * kTcBlockK;
+          } else {
+            xm = &tB; ym = &tGlo; kx = (kt - p.kt_w - p.kt_b) * kTcBlockK;
+          }
+          uint8_t* xs = smem + s * stage_bytes;
+          uint8_t* ys = xs + kTcXTileBytes;
+          const uint32_t bar0 = full0 + s * 8u;
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * stage_bytes);
+          tma_load_2d_pair(xs, xm, bar0, kx, row0, kt < p.kt_w ? pol_stream : pol_keep);
+          // this CTA's half of each N chunk of the Y tile
+          for (int c = 0; c < h0; c += p.y_box_rows)
+            tma_load_2d_pair(ys + c * 128, ym, bar0, kx, static_cast<int>(rank) * h0 + c, pol_keep);
+          for (int c = 0; c < h1; c += p.y_box_rows)
+            tma_load_2d_pair(ys + (h0 + c) * 128, ym, bar0, kx,
+                             p.n0 + static_cast<int>(rank) * h1 + c, pol_keep);
+        }
+      }
+      // The even CTA's `full` barriers count the loads of both CTAs: once the
+      // last use of every stage has completed, no copy is still in flight.
+      if (rank == 0) {
+        const uint64_t drain_deadline = global_timer_ns() + p.timeout_ns;
+        const uint32_t first = it > static_cast<uint32_t>(p.stages) ? it - p.stages : 0;
+        for (uint32_t i = first; i < it; ++i)
+          if (!mbar_wait(&full[i % p.stages], (i / p.stages) & 1u, drain_deadline))
+            atomicExch(p.status, kStatusTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      // Everything the issue loop needs is in registers: descriptors of stage 0
+      // plus per-stage and per-K-step offsets (in the descriptors' 16-byte units).
+      const uint32_t idesc0 = idesc_bf16_f32(256, p.n0);
+      const uint32_t idesc1 = idesc_bf16_f32(256, p.n1 > 0 ? p.n1 : 16);
+      const bool two = p.n1 > 0;
+      const uint32_t tmem1 = tmem_base + static_cast<uint32_t>(p.n0);
+      const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
+      const uint64_t dy0 = smem_desc_sw128(smem_u32(smem) + kTcXTileBytes);
+      const uint64_t dy1_off = static_cast<uint64_t>(p.n0 / 2) * 128u >> 4;
+      const uint64_t stage_step = stage_bytes >> 4;
+      const int stages = p.stages;
+      uint32_t it = 0;
+      int icount = 0;
+      bool stop = false;
+      for (int item = cid; item < n_items && !stop; item += ncl, ++icount) {
+        int tile, split, kb, ke;
+        item_range(p, item, tile, split, kb, ke);
+        if (icount > 0 && !mbar_wait(accum_empty, (icount - 1) & 1, deadline)) {
+          atomicExch(p.status, kStatusTimeout);
+          *abort_flag = 1;
+        }
+        tc_fence_after_sync();
+        for (int kt = kb; kt < ke; ++kt, ++it) {
+          const uint32_t s = it % stages;
+          const uint32_t use = it / stages;
+          if (!*abort_flag && !mbar_wait(&full[s], use & 1u, deadline)) {
+            atomicExch(p.status, kStatusTimeout);
+            *abort_flag = 1;
+          }
+          if (*abort_flag) {
+            stop = true;
+            break;
+          }
+          const uint64_t dx = dx0 + s * stage_step;
+          const uint64_t dy = dy0 + s * stage_step;
+          const uint32_t first = kt == kb ? 0u : 1u;
+#pragma unroll
+          for (int ks = 0; ks < kTcBlockK / 16; ++ks) {
+            const uint32_t acc = ks > 0 ? 1u : first;
+            umma_bf16_pair(tmem_base, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
+            if (two) umma_bf16_pair(tmem1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
+          }
+          umma_commit_pair(&empty[s], 0x3);
+        }
+        // both CTAs learn that this item's accumulator is complete
+        umma_commit_pair(accum_full, 0x3);
+      }
+      // do not leave tensor-core work in flight behind the final barrier
+      if (icount > 0 && !mbar_wait(accum_full, (icount - 1) & 1, global_timer_ns() + p.timeout_ns))
+        atomicExch(p.status, kStatusTimeout);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    const int q = warp & 3;                 // TMEM lane quadrant = 32-row group of this warp
+    const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t accum_empty0 = map_to_rank(smem_u32(accum_empty), 0);
+    // sum-of-squares mapping: one warp instruction reads 4 rows x 128 bytes;
+    // lane = 8 * sub + chunk reads row (4 * r4 + sub), 16-byte chunk `chunk`
+    const int sub = lane >> 3;
+    const int chunk = lane & 7;
+    int icount = 0;
+    for (int item = cid; item < n_items; item += ncl, ++icount) {
+      int tile, split, kb, ke;
+      item_range(p, item, tile, split, kb, ke);
+      const int rowbase = tile * 256 + static_cast<int>(rank) * 128 + q * 32;
+      const int grow = rowbase + lane;      // the row whose dot this lane computes
+      const bool valid = grow < p.rows;
+      const uint16_t* brow = p.B + static_cast<size_t>(valid ? grow : 0) * p.r;
+      // warm L2 with this row of B for the end of the item
+      for (int c = 0; c < p.r * 2; c += 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(brow) + c));
+
+      // ---- sum of squares of this warp's 32 rows over the item's W columns
+      float sacc[8], scmp[8];
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) sacc[r4] = scmp[r4] = 0.f;
+      const uint16_t* wrow[8];
+      bool wvalid[8];
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) {
+        const int row = rowbase + 4 * r4 + sub;
+        wvalid[r4] = row < p.rows;
+        wrow[r4] = p.W + static_cast<size_t>(wvalid[r4] ? row : 0) * p.d_in + chunk * 8;
+      }
+      const int kw_end = ke < p.kt_w ? ke : p.kt_w;
+      for (int kt = kb; kt < kw_end; kt += 2) {
+        uint4 v[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col = (kt + u) * kTcBlockK + chunk * 8;
+          const bool cok = kt + u < kw_end && col < p.d_in;
+#pragma unroll
+          for (int r4 = 0; r4 < 8; ++r4)
+            v[u][r4] = (cok && wvalid[r4]) ? ldg_stream(wrow[r4] + (kt + u) * kTcBlockK)
+                                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int r4 = 0; r4 < 8; ++r4) kahan_add(sacc[r4], scmp[r4], sumsq8(v[u][r4]));
+      }
+      // fold the 8 chunk lanes of each row, then hand row (rowbase + lane) to its lane
+      float ss = 0.f;
+#pragma unroll
+      for (int r4 = 0; r4 < 8; ++r4) {
+        float t = __fsub_rn(sacc[r4], scmp[r4]);
+        t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
+        t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
+        t += __shfl_xor_sync(0xFFFFFFFFu, t, 4);
+        const float mine = __shfl_sync(0xFFFFFFFFu, t, (lane & 3) * 8);
+        if ((lane >> 2) == r4) ss = mine;
+      }
+
+      // ---- rowsum(B o D): B is streamed kBLookahead chunks ahead of the TMEM reads
+      uint4 bq[kBLookahead][4];
+#pragma unroll
+      for (int c = 0; c < kBLookahead; ++c)
+        if (c * 32 < p.r) load_b_chunk(brow, c, p.r, valid, bq[c]);
+      bool ok = mbar_wait(accum_full, icount & 1, deadline);
+      if (!ok) {
+        atomicExch(p.status, kStatusTimeout);
+        *abort_flag = 1;
+      }
+      tc_fence_after_sync();
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < kMaxChunks; ++c) {
+        if (c * 32 < p.r) {
+          float v[32];
+          tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
+          uint4 cur[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) cur[e] = bq[c % kBLookahead][e];
+          if (c + kBLookahead < kMaxChunks && (c + kBLookahead) * 32 < p.r)
+            load_b_chunk(brow, c + kBLookahead, p.r, valid, bq[c % kBLookahead]);
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            const uint32_t w[4] = {cur[qq].x, cur[qq].y, cur[qq].z, cur[qq].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc = fmaf(bf16_lo(w[e]), v[qq * 8 + 2 * e], acc);
+              acc = fmaf(bf16_hi(w[e]), v[qq * 8 + 2 * e + 1], acc);
+            }
+          }
+        }
+      }
+      if (valid) {
+        p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc;
+        p.out_sumsq[static_cast<size_t>(split) * p.rows + grow] = ss;
+      }
+      // accumulator drained: let the even CTA start the next item's MMAs
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(accum_empty0);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();            // the peer may still read this CTA's shared memory until here
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, p.tmem_cols);
+  }
+}
+
+}  // namespace
+
+size_t pair_smem_bytes(int n_pad, int stages) {
+  const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
+  return 1024 + stage * stages + (2 * stages + 2) * 8 + 16;
+}
+
+int pair_pick_stages(int n_pad) {
+  const size_t budget = 227 * 1024;
+  int st = kTcMaxStages;
+  while (st > 2 && pair_smem_bytes(n_pad, st) > budget) --st;
+  return st;
+}
+
+// Co-resident CTA pairs.  Every shape of this kernel needs more than half of
+// an SM's shared memory, so one CTA per SM and the count does not depend on
+// the shape; the attribute is raised to the largest size once per device.
+int pair_max_clusters(size_t smem_bytes) {
+  (void)smem_bytes;
+  constexpr int kMaxSmem = 227 * 1024;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cached[64] = {0};
+  if (dev < 64 && cached[dev]) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMaxSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaFuncSetAttribute(k_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_gemm_pair, &cfg) != cudaSuccess)
+    return 0;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const CUtensorMap& tB,
+                             const CUtensorMap& tGhi, const CUtensorMap& tGlo, const PairParams& p,
+                             int clusters, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair, tW, tA, tB, tGhi, tGlo, p);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace dora

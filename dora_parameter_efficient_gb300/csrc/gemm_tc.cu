@@ -134,31 +134,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // descriptors of stage 0 and register offsets; no parameter reloads in the loop
       const int n0 = p.n_pad < 256 ? p.n_pad : 256;
       const int n1 = p.n_pad - n0;
+      const bool two = n1 > 0;
       const uint32_t idesc0 = idesc_bf16_f32(kTcBlockM, n0);
-      const uint32_t idesc1 = idesc_bf16_f32(kTcBlockM, n1 > 0 ? n1 : 16);
+      const uint32_t idesc1 = idesc_bf16_f32(kTcBlockM, two ? n1 : 16);
+      const uint32_t tmem1 = tmem_base + static_cast<uint32_t>(n0);
+      const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
+      const uint64_t dy0 = smem_desc_sw128(smem_u32(smem) + kTcXTileBytes);
+      const uint64_t dy1_off = static_cast<uint64_t>(n0) * 128u >> 4;
+      const uint64_t stage_step = stage_bytes >> 4;
+      const int stages = p.stages;
       for (int i = 0; i < n_iter; ++i) {
-        const int s = i % p.stages;
-        const uint32_t use = static_cast<uint32_t>(i / p.stages);
+        const int s = i % stages;
+        const uint32_t use = static_cast<uint32_t>(i / stages);
         if (!mbar_wait(&full[s], use & 1u, deadline)) {
           record_timeout(p.status);
           *abort_flag = 1;
           break;
         }
         if (*abort_flag) break;
-        tc_fence_after_sync();
-        const uint32_t xa = smem_u32(smem + s * stage_bytes);
-        const uint32_t ya = xa + kTcXTileBytes;
+        const uint64_t dx = dx0 + s * stage_step;
+        const uint64_t dy = dy0 + s * stage_step;
+        const uint32_t first = i > 0 ? 1u : 0u;
 #pragma unroll
         for (int ks = 0; ks < kTcBlockK / 16; ++ks) {
-          const uint64_t ad = smem_desc_sw128(xa + ks * 32);
-          const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-          umma_bf16(tmem_base, ad, smem_desc_sw128(ya + ks * 32), idesc0, acc);
-          if (n1 > 0)
-            umma_bf16(tmem_base + static_cast<uint32_t>(n0), ad,
-                      smem_desc_sw128(ya + static_cast<uint32_t>(n0) * 128u + ks * 32), idesc1,
-                      acc);
+          const uint32_t acc = ks > 0 ? 1u : first;
+          umma_bf16(tmem_base, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
+          if (two) umma_bf16(tmem1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
         }
         umma_commit(&empty[s]);
       }

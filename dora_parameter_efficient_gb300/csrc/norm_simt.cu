@@ -166,21 +166,29 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) out[row] = acc;
 }
 
-// G = sum over splits of the partial Gram tiles (fixed order), and its split
-// into two bf16 terms G_hi + G_lo for the tensor-core BA-norm pass.
+// G = sum over splits of the partial Gram tiles (fixed order), and the split
+// of scale * G into two bf16 terms G_hi + G_lo for the tensor-core BA-norm
+// tiles (about 16 significant bits of G survive the two bf16 terms).
+constexpr int kMaxGramParts = 16;
+
 __global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int n_pad,
                               float* __restrict__ G, uint16_t* __restrict__ G_hi,
-                              uint16_t* __restrict__ G_lo) {
+                              uint16_t* __restrict__ G_lo, float scale) {
   const int64_t n = static_cast<int64_t>(n_pad) * n_pad;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v[kMaxGramParts];
+#pragma unroll
+    for (int s = 0; s < kMaxGramParts; ++s) v[s] = s < splits ? __ldg(parts + s * n + i) : 0.f;
     float acc = 0.f;
-    for (int s = 0; s < splits; ++s) acc = __fadd_rn(acc, parts[s * n + i]);
+#pragma unroll
+    for (int s = 0; s < kMaxGramParts; ++s) acc = __fadd_rn(acc, v[s]);
     G[i] = acc;
     if (G_hi) {
-      const uint16_t hi = f32_to_bf16_rn(acc);
+      const float sc = __fmul_rn(scale, acc);
+      const uint16_t hi = f32_to_bf16_rn(sc);
       G_hi[i] = hi;
-      G_lo[i] = f32_to_bf16_rn(__fsub_rn(acc, bf16_to_f32(hi)));
+      G_lo[i] = f32_to_bf16_rn(__fsub_rn(sc, bf16_to_f32(hi)));
     }
   }
 }
@@ -188,6 +196,8 @@ __global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int n
 // wnorm = sqrt(max(base + 2 s cross + s^2 ba, 0)), g = m / max(wnorm, eps)
 // (Chinese write-up section 1.2.2, Algorithm 1 step 6).  Partials are summed
 // in split order; the assembly, root and divide run in fp64 and round once.
+constexpr int kMaxFinalParts = 16;
+
 __global__ void k_finalize(int64_t d_out, const float* __restrict__ pbase, int n_base,
                            const float* __restrict__ pcross, int n_cross,
                            const float* __restrict__ pba, int n_ba, double s,
@@ -195,10 +205,21 @@ __global__ void k_finalize(int64_t d_out, const float* __restrict__ pbase, int n
                            float* __restrict__ wnorm, float* __restrict__ g) {
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= d_out) return;
+  // all partial loads are issued before the (fixed-order) sums
+  float vb[kMaxFinalParts], vc[kMaxFinalParts], va[kMaxFinalParts];
+#pragma unroll
+  for (int i = 0; i < kMaxFinalParts; ++i) {
+    vb[i] = i < n_base ? __ldg(pbase + i * d_out + j) : 0.f;
+    vc[i] = i < n_cross ? __ldg(pcross + i * d_out + j) : 0.f;
+    va[i] = i < n_ba ? __ldg(pba + i * d_out + j) : 0.f;
+  }
   double base = 0.0, cross = 0.0, ba = 0.0;
-  for (int i = 0; i < n_base; ++i) base += static_cast<double>(pbase[i * d_out + j]);
-  for (int i = 0; i < n_cross; ++i) cross += static_cast<double>(pcross[i * d_out + j]);
-  for (int i = 0; i < n_ba; ++i) ba += static_cast<double>(pba[i * d_out + j]);
+#pragma unroll
+  for (int i = 0; i < kMaxFinalParts; ++i) {
+    base += static_cast<double>(vb[i]);
+    cross += static_cast<double>(vc[i]);
+    ba += static_cast<double>(va[i]);
+  }
   const double w2 = __dadd_rn(__dadd_rn(base, __dmul_rn(__dmul_rn(2.0, s), cross)),
                               __dmul_rn(__dmul_rn(s, s), ba));
   const double wn = sqrt(fmax(w2, 0.0));
@@ -231,10 +252,11 @@ cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t c
 }
 
 cudaError_t launch_gram_reduce(const float* parts, int splits, int n_pad, float* G,
-                               uint16_t* G_hi, uint16_t* G_lo, cudaStream_t stream) {
+                               uint16_t* G_hi, uint16_t* G_lo, float scale, cudaStream_t stream) {
+  if (splits > kMaxGramParts) return cudaErrorInvalidValue;
   const int64_t n = static_cast<int64_t>(n_pad) * n_pad;
   const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-  k_gram_reduce<<<blocks, 256, 0, stream>>>(parts, splits, n_pad, G, G_hi, G_lo);
+  k_gram_reduce<<<blocks, 256, 0, stream>>>(parts, splits, n_pad, G, G_hi, G_lo, scale);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -243,8 +265,10 @@ cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const
                             int n_cross, const float* pba, int n_ba, double s, const void* m,
                             int is_bf16, double eps, float* wnorm, float* g,
                             cudaStream_t stream) {
-  const unsigned blocks = static_cast<unsigned>((d_out + 255) / 256);
-  k_finalize<<<blocks, 256, 0, stream>>>(d_out, pbase, n_base, pcross, n_cross, pba, n_ba, s, m,
+  if (n_base > kMaxFinalParts || n_cross > kMaxFinalParts || n_ba > kMaxFinalParts)
+    return cudaErrorInvalidValue;
+  const unsigned blocks = static_cast<unsigned>((d_out + 127) / 128);
+  k_finalize<<<blocks, 128, 0, stream>>>(d_out, pbase, n_base, pcross, n_cross, pba, n_ba, s, m,
                                          is_bf16, eps, wnorm, g);
   note_launches(1);
   return cudaGetLastError();

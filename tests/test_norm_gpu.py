@@ -163,7 +163,8 @@ def _int_case(dtype, d_out, d_in, r, seed, ab_max=3):
     aU = aW @ aA.T                     # |U| partial sums
     aG = aA @ aA.T                     # |G| partial sums
     aT = aB @ aG                       # |B G| partial sums
-    bounds = [(aW * aW).sum(1), aU, (aB * aU).sum(1), aG, aT, (aB * aT).sum(1)]
+    # the bf16 path accumulates U + (s/2) B G in one accumulator (s = 2 here)
+    bounds = [(aW * aW).sum(1), aU + aT, (aB * (aU + aT)).sum(1), aG, aT, (aB * aT).sum(1)]
     assert max(int(np.max(b)) for b in bounds) < 2 ** 24
     if dtype == configs.BF16:
         conv = gen.f32_to_bf16_bits
