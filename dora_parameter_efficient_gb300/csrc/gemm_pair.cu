@@ -25,10 +25,12 @@
 //     stage complete on the even CTA's `full` barrier; the even CTA's MMA
 //     thread waits on it and commits `empty` to both CTAs -- the only
 //     hand-off on the shared-memory pipeline;
-//   * warps 2-5 of each CTA stay off that pipeline: while the MMAs run they
+//   * warps 2-9 of each CTA stay off that pipeline: while the MMAs run they
 //     stream their 128 rows of W straight from global memory (coalesced,
-//     4 rows x 128 bytes per warp instruction) for the sum of squares, then
-//     read D rows from tensor memory (tcgen05.ld) and dot them with B;
+//     4 rows x 128 bytes per warp instruction) for the sum of squares and
+//     fetch their half of each B row into registers; then two warps per TMEM
+//     lane quadrant read the halves of the D rows (tcgen05.ld), dot them with
+//     B and add the halves in a fixed order;
 //   * the grid is persistent: cluster c processes work items c, c + C, ...,
 //     an item being (256-row tile, K split); the TMA producer runs ahead into
 //     the next item while the epilogue drains the accumulator.
@@ -62,19 +64,32 @@ __device__ __forceinline__ uint4 ldg_stream(const uint16_t* p) {
   return v;
 }
 
-// Columns [32c, 32c + 32) of one row of B (bf16); columns past r read as 0.
-constexpr int kMaxChunks = 512 / 32;
-constexpr int kBLookahead = 4;
-
-__device__ __forceinline__ void load_b_chunk(const uint16_t* brow, int c, int r, bool valid,
-                                             uint4 (&dst)[4]) {
+// Columns [c0, c0 + 8 * N) of one row of B (bf16); columns past r read as 0.
+template <int N>
+__device__ __forceinline__ void load_b_cols(const uint16_t* brow, int c0, int r, bool valid,
+                                            uint4 (&dst)[N]) {
 #pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    if (valid && c * 32 + v * 8 < r)
-      dst[v] = __ldg(reinterpret_cast<const uint4*>(brow + c * 32) + v);
+  for (int v = 0; v < N; ++v) {
+    if (valid && c0 + v * 8 < r)
+      dst[v] = __ldg(reinterpret_cast<const uint4*>(brow + c0) + v);
     else
       dst[v] = make_uint4(0u, 0u, 0u, 0u);
   }
+}
+
+// acc += sum over 8 * N columns of B (bf16 pairs in `b`) times D (`v`)
+template <int N>
+__device__ __forceinline__ float dot_b(const uint4 (&b)[N], const float* v, float acc) {
+#pragma unroll
+  for (int q = 0; q < N; ++q) {
+    const uint32_t w[4] = {b[q].x, b[q].y, b[q].z, b[q].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(bf16_lo(w[e]), v[q * 8 + 2 * e], acc);
+      acc = fmaf(bf16_hi(w[e]), v[q * 8 + 2 * e + 1], acc);
+    }
+  }
+  return acc;
 }
 
 __device__ __forceinline__ void item_range(const PairParams& p, int item, int& tile, int& split,
@@ -86,7 +101,11 @@ __device__ __forceinline__ void item_range(const PairParams& p, int item, int& t
   ke = static_cast<int>((static_cast<long long>(ktot) * (split + 1)) / p.splits);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+// warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per tensor-memory lane quadrant)
+constexpr int kPairThreads = 320;
+constexpr int kPairEpiThreads = 256;
+
+__global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tA,
                 const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tGhi,
                 const __grid_constant__ CUtensorMap tGlo, const PairParams p) {
@@ -101,6 +120,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* accum_empty = accum_full + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  float* dot_half = reinterpret_cast<float*>(tmem_holder + 4);   // [128] second-half dots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,7 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(accum_full, 1);
-    mbar_init(accum_empty, 8);
+    mbar_init(accum_empty, 16);     // 8 epilogue warps in each CTA of the pair
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -143,21 +163,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol_keep = l2_policy_evict_last();
       const uint32_t full0 = map_to_rank(smem_u32(full), 0);
       const int h0 = p.n0 / 2, h1 = p.n1 / 2;
-      uint32_t it = 0;
+      const uint32_t stages = static_cast<uint32_t>(p.stages);
+      // stage index and the parity of its current use, kept incrementally (a
+      // runtime division per tile sits on the issuing thread's critical path)
+      uint32_t s = 0, phase = 0, it = 0;
       bool stop = false;
       for (int item = cid; item < n_items && !stop; item += ncl) {
         int tile, split, kb, ke;
         item_range(p, item, tile, split, kb, ke);
         const int row0 = tile * 256 + static_cast<int>(rank) * 128;
         for (int kt = kb; kt < ke; ++kt, ++it) {
-          const uint32_t s = it % p.stages;
-          const uint32_t use = it / p.stages;
-          if (it >= static_cast<uint32_t>(p.stages) &&
-              !mbar_wait(&empty[s], (use - 1) & 1u, deadline)) {
+          // the slot's previous use (parity phase ^ 1) must have been consumed
+          if (it >= stages && !mbar_wait(&empty[s], phase ^ 1u, deadline)) {
             atomicExch(p.status, kStatusTimeout);
             *abort_flag = 1;
-          }
-          if (*abort_flag) {
             stop = true;
             break;
           }
@@ -185,15 +204,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int c = 0; c < h1; c += p.y_box_rows)
             tma_load_2d_pair(ys + (h0 + c) * 128, ym, bar0, kx,
                              p.n0 + static_cast<int>(rank) * h1 + c, pol_keep);
+          if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+          }
         }
       }
       // The even CTA's `full` barriers count the loads of both CTAs: once the
       // last use of every stage has completed, no copy is still in flight.
       if (rank == 0) {
         const uint64_t drain_deadline = global_timer_ns() + p.timeout_ns;
-        const uint32_t first = it > static_cast<uint32_t>(p.stages) ? it - p.stages : 0;
+        const uint32_t first = it > stages ? it - stages : 0;
         for (uint32_t i = first; i < it; ++i)
-          if (!mbar_wait(&full[i % p.stages], (i / p.stages) & 1u, drain_deadline))
+          if (!mbar_wait(&full[i % stages], (i / stages) & 1u, drain_deadline))
             atomicExch(p.status, kStatusTimeout);
       }
     }
@@ -210,26 +233,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t dy0 = smem_desc_sw128(smem_u32(smem) + kTcXTileBytes);
       const uint64_t dy1_off = static_cast<uint64_t>(p.n0 / 2) * 128u >> 4;
       const uint64_t stage_step = stage_bytes >> 4;
-      const int stages = p.stages;
-      uint32_t it = 0;
+      const uint32_t stages = static_cast<uint32_t>(p.stages);
+      uint32_t s = 0, phase = 0;
       int icount = 0;
       bool stop = false;
       for (int item = cid; item < n_items && !stop; item += ncl, ++icount) {
         int tile, split, kb, ke;
         item_range(p, item, tile, split, kb, ke);
         if (icount > 0 && !mbar_wait(accum_empty, (icount - 1) & 1, deadline)) {
+          // the accumulator was never drained: issue nothing more
           atomicExch(p.status, kStatusTimeout);
           *abort_flag = 1;
+          break;
         }
         tc_fence_after_sync();
-        for (int kt = kb; kt < ke; ++kt, ++it) {
-          const uint32_t s = it % stages;
-          const uint32_t use = it / stages;
-          if (!*abort_flag && !mbar_wait(&full[s], use & 1u, deadline)) {
+        for (int kt = kb; kt < ke; ++kt) {
+          if (!mbar_wait(&full[s], phase, deadline)) {
             atomicExch(p.status, kStatusTimeout);
             *abort_flag = 1;
-          }
-          if (*abort_flag) {
             stop = true;
             break;
           }
@@ -243,6 +264,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (two) umma_bf16_pair(tmem1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
           }
           umma_commit_pair(&empty[s], 0x3);
+          if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+          }
         }
         // both CTAs learn that this item's accumulator is complete
         umma_commit_pair(accum_full, 0x3);
@@ -253,11 +278,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue (both CTAs)
-    const int q = warp & 3;                 // TMEM lane quadrant = 32-row group of this warp
+    // Warps 2-9: quadrant q = warp % 4 (the TMEM lanes = tile rows this warp
+    // may read), half h = (warp - 2) / 4.  Half h owns accumulator columns
+    // [h * cols0, ...) of all 32 rows of its quadrant, and the sums of
+    // squares of rows 16h .. 16h + 15 of the quadrant.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int trow = q * 32 + lane;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t accum_empty0 = map_to_rank(smem_u32(accum_empty), 0);
+    const int nchunk = (p.r + 31) / 32;              // 32-column chunks of the accumulator
+    const int c_lo = h == 0 ? 0 : (nchunk + 1) / 2;
+    const int c_hi = h == 0 ? (nchunk + 1) / 2 : nchunk;
     // sum-of-squares mapping: one warp instruction reads 4 rows x 128 bytes;
-    // lane = 8 * sub + chunk reads row (4 * r4 + sub), 16-byte chunk `chunk`
+    // lane = 8 * sub + chunk reads row (16h + 4 * r4 + sub), 16-byte chunk `chunk`
     const int sub = lane >> 3;
     const int chunk = lane & 7;
     int icount = 0;
@@ -268,43 +302,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int grow = rowbase + lane;      // the row whose dot this lane computes
       const bool valid = grow < p.rows;
       const uint16_t* brow = p.B + static_cast<size_t>(valid ? grow : 0) * p.r;
-      // warm L2 with this row of B for the end of the item
-      for (int c = 0; c < p.r * 2; c += 128)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const uint8_t*>(brow) + c));
 
-      // ---- sum of squares of this warp's 32 rows over the item's W columns
-      float sacc[8], scmp[8];
+      // ---- sum of squares of 16 rows over the item's W columns
+      float sacc[4], scmp[4];
 #pragma unroll
-      for (int r4 = 0; r4 < 8; ++r4) sacc[r4] = scmp[r4] = 0.f;
-      const uint16_t* wrow[8];
-      bool wvalid[8];
+      for (int r4 = 0; r4 < 4; ++r4) sacc[r4] = scmp[r4] = 0.f;
+      const uint16_t* wrow[4];
+      bool wvalid[4];
 #pragma unroll
-      for (int r4 = 0; r4 < 8; ++r4) {
-        const int row = rowbase + 4 * r4 + sub;
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int row = rowbase + 16 * h + 4 * r4 + sub;
         wvalid[r4] = row < p.rows;
         wrow[r4] = p.W + static_cast<size_t>(wvalid[r4] ? row : 0) * p.d_in + chunk * 8;
       }
       const int kw_end = ke < p.kt_w ? ke : p.kt_w;
-      for (int kt = kb; kt < kw_end; kt += 2) {
-        uint4 v[2][8];
+      for (int kt = kb; kt < kw_end; kt += 4) {
+        uint4 v[4][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const int col = (kt + u) * kTcBlockK + chunk * 8;
           const bool cok = kt + u < kw_end && col < p.d_in;
 #pragma unroll
-          for (int r4 = 0; r4 < 8; ++r4)
+          for (int r4 = 0; r4 < 4; ++r4)
             v[u][r4] = (cok && wvalid[r4]) ? ldg_stream(wrow[r4] + (kt + u) * kTcBlockK)
                                            : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
-          for (int r4 = 0; r4 < 8; ++r4) kahan_add(sacc[r4], scmp[r4], sumsq8(v[u][r4]));
+          for (int r4 = 0; r4 < 4; ++r4) kahan_add(sacc[r4], scmp[r4], sumsq8(v[u][r4]));
       }
-      // fold the 8 chunk lanes of each row, then hand row (rowbase + lane) to its lane
+      // fold the 8 chunk lanes of each row; lane L < 16 then takes row 16h + L
       float ss = 0.f;
 #pragma unroll
-      for (int r4 = 0; r4 < 8; ++r4) {
+      for (int r4 = 0; r4 < 4; ++r4) {
         float t = __fsub_rn(sacc[r4], scmp[r4]);
         t += __shfl_xor_sync(0xFFFFFFFFu, t, 1);
         t += __shfl_xor_sync(0xFFFFFFFFu, t, 2);
@@ -312,50 +343,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float mine = __shfl_sync(0xFFFFFFFFu, t, (lane & 3) * 8);
         if ((lane >> 2) == r4) ss = mine;
       }
+      {
+        const int srow = rowbase + 16 * h + lane;
+        if (lane < 16 && srow < p.rows) p.out_sumsq[static_cast<size_t>(split) * p.rows + srow] = ss;
+      }
 
-      // ---- rowsum(B o D): B is streamed kBLookahead chunks ahead of the TMEM reads
-      uint4 bq[kBLookahead][4];
+      // ---- this half's part of rowsum(B o D).  Up to 192 columns of the B
+      // row are fetched into registers before the accumulator is complete.
+      uint4 bb[24];
 #pragma unroll
-      for (int c = 0; c < kBLookahead; ++c)
-        if (c * 32 < p.r) load_b_chunk(brow, c, p.r, valid, bq[c]);
+      for (int v = 0; v < 24; ++v) {
+        const int col = c_lo * 32 + v * 8;
+        bb[v] = (valid && col < c_hi * 32 && col < p.r)
+                    ? __ldg(reinterpret_cast<const uint4*>(brow + col))
+                    : make_uint4(0u, 0u, 0u, 0u);
+      }
       bool ok = mbar_wait(accum_full, icount & 1, deadline);
       if (!ok) {
         atomicExch(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
       tc_fence_after_sync();
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
+      {
+        // one decision for all 8 epilogue warps (they meet at named barriers below)
+        uint32_t all_ok;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 1, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(all_ok)
+            : "r"(ok ? 1u : 0u), "n"(kPairEpiThreads)
+            : "memory");
+        ok = all_ok != 0;
+      }
       float acc = 0.f;
+      if (ok) {
 #pragma unroll
-      for (int c = 0; c < kMaxChunks; ++c) {
-        if (c * 32 < p.r) {
-          float v[32];
-          tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
-          uint4 cur[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) cur[e] = bq[c % kBLookahead][e];
-          if (c + kBLookahead < kMaxChunks && (c + kBLookahead) * 32 < p.r)
-            load_b_chunk(brow, c + kBLookahead, p.r, valid, bq[c % kBLookahead]);
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const uint32_t w[4] = {cur[qq].x, cur[qq].y, cur[qq].z, cur[qq].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc = fmaf(bf16_lo(w[e]), v[qq * 8 + 2 * e], acc);
-              acc = fmaf(bf16_hi(w[e]), v[qq * 8 + 2 * e + 1], acc);
-            }
+        for (int j = 0; j < 6; ++j) {            // chunks c_lo + j held in bb
+          const int c = c_lo + j;
+          if (c < c_hi) {
+            float v[32];
+            tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
+            const uint4 part[4] = {bb[4 * j], bb[4 * j + 1], bb[4 * j + 2], bb[4 * j + 3]};
+            acc = dot_b<4>(part, v, acc);
           }
         }
-      }
-      if (valid) {
-        p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc;
-        p.out_sumsq[static_cast<size_t>(split) * p.rows + grow] = ss;
+        for (int c = c_lo + 6; c < c_hi; ++c) {   // ranks above 384: the rest, loaded now
+          uint4 part[4];
+          load_b_cols<4>(brow, c * 32, p.r, valid, part);
+          float v[32];
+          tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
+          acc = dot_b<4>(part, v, acc);
+        }
       }
       // accumulator drained: let the even CTA start the next item's MMAs
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(accum_empty0);
+      if (!ok) break;
+      // first half + second half, in that order, for each row
+      if (h == 1) dot_half[trow] = acc;
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
+      if (h == 0 && valid)
+        p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc + dot_half[trow];
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
     }
   }
 
@@ -373,7 +425,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 size_t pair_smem_bytes(int n_pad, int stages) {
   const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
-  return 1024 + stage * stages + (2 * stages + 2) * 8 + 16;
+  return 1024 + stage * stages + (2 * stages + 2) * 8 + 16 + 128 * 4;
 }
 
 int pair_pick_stages(int n_pad) {
@@ -395,7 +447,7 @@ int pair_max_clusters(size_t smem_bytes) {
   if (dev < 64 && cached[dev]) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = kMaxSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -418,7 +470,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
                              int clusters, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
