@@ -64,10 +64,11 @@ struct TcParams {
   const uint16_t* B;     // DotB: [rows x r] bf16
   float* out_sumsq;      // [splits][rows]
   float* out_dot;        // [splits][rows]
-  float* out_store;      // [splits][n_pad][n_pad]
+  float* out_store;      // [splits][gridDim.x][128][n_pad] partial tiles
   int* status;
   unsigned long long timeout_ns;
   int inject_fault;      // test hook: the producer issues no loads
+  int gram_nb;           // > 0: Gram mode over the nb x nb grid of 128-blocks (upper triangle)
 };
 
 size_t tc_smem_bytes(int n_pad, int stages);
@@ -117,11 +118,12 @@ cudaError_t launch_gemm_simt(const float* X, const float* Y, int rows, int ncols
 // ------------------------------------------------------------------ small kernels
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,
                              float* out, cudaStream_t stream);
-cudaError_t launch_gram_reduce(const float* parts, int splits, int n_pad, float* G,
-                               uint16_t* G_hi, uint16_t* G_lo, float scale, cudaStream_t stream);
+cudaError_t launch_gram_reduce(const float* parts, int splits, int nb, int bw, int n_pad,
+                               float* G, uint16_t* G_hi, uint16_t* G_lo, float scale,
+                               cudaStream_t stream);
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
-                            int n_cross, const float* pba, int n_ba, double s, const void* m,
-                            int is_bf16, double eps, float* wnorm, float* g,
+                            int n_cross, const float* pba, int n_ba, float s, const void* m,
+                            int is_bf16, float eps, float* wnorm, float* g,
                             cudaStream_t stream);
 cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
                            int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,

@@ -19,7 +19,7 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::
 namespace {
 
 constexpr int kMaxMainSplits = 16;
-constexpr int kMaxGramSplits = 16;
+constexpr int kMaxGramSplits = 24;   // K splits of the Gram blocks (workspace sized for this)
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -87,6 +87,15 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Gram blocks: the upper triangle of the nb x nb grid of 128-row blocks of
+// G [rp x rp]; each block partial is [128 x bw] floats.
+int gram_nb(int rp) { return static_cast<int>((rp + 127) / 128); }
+int gram_bw(int rp) { return rp > 128 ? 128 : rp; }
+size_t gram_block_floats(int rp) {
+  const size_t nb = gram_nb(rp);
+  return nb * (nb + 1) / 2 * 128 * static_cast<size_t>(gram_bw(rp));
+}
+
 // ---------------------------------------------------------------- workspace plan
 struct Plan {
   bool bf16 = true;
@@ -136,7 +145,7 @@ Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
     p.off_Glo = off;
     off = align_up(off + rp2 * 2, 256);
     p.off_Gpart = off;
-    off = align_up(off + kMaxGramSplits * rp2 * 4, 256);
+    off = align_up(off + static_cast<size_t>(kMaxGramSplits) * gram_block_floats(p.rp) * 4, 256);
   }
   p.off_pbase = off;
   off = align_up(off + static_cast<size_t>(p.cap_base) * d_out * 4, 256);
@@ -258,8 +267,9 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     // G' = (s/2) G split into two bf16 terms, then the CTA-pair main pass with
     // the BA-norm tiles folded into its K loop.
     const int rp = plan.rp;
-    int y_box1 = 128;                       // single-CTA kernel: Y box rows dividing rp
-    while (rp % y_box1) y_box1 >>= 1;
+    const int gnb = gram_nb(rp), gbw = gram_bw(rp);
+    int y_box1 = 128;                       // Gram kernel: Y box rows dividing the block width
+    while (gbw % y_box1) y_box1 >>= 1;
     const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
     const uint32_t tmem_cols = [&] {
       uint32_t c = 32;
@@ -279,23 +289,30 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
         !make_map_bf16(&mGhi, Ghi, rp, rp, y_box2) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box2))
       return DORA_ERR_CUDA;
 
+    // G = A A^T: upper-triangular 128x128 blocks, K split so about one CTA
+    // per SM is busy; partial blocks are summed in split order afterwards.
     TcParams pg{};
     pg.rows = static_cast<int>(r);
-    pg.n_pad = rp;
+    pg.n_pad = gbw;
     pg.y_box_rows = y_box1;
     pg.k_tiles = k_tiles;
     pg.k_tiles_pass = k_tiles;
-    pg.stages = tc_pick_stages(rp);
+    pg.stages = tc_pick_stages(gbw);
     pg.mode = kTcStore;
     pg.r = static_cast<int>(r);
-    pg.tmem_cols = tmem_cols;
+    pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
     pg.out_store = Gpart;
     pg.status = status;
     pg.timeout_ns = kDefaultTimeoutNs;
-    const int gram_tiles = static_cast<int>(ceil_div(rp, kTcBlockM));
-    const int gram_splits = pick_splits(gram_tiles, k_tiles, dev.sms, kMaxGramSplits);
-    DORA_TRY(launch_gemm_tc(mA_x, mA_y1, mA_y1, pg, gram_tiles, gram_splits, stream));
-    DORA_TRY(launch_gram_reduce(Gpart, gram_splits, rp, G, Ghi, Glo, 0.5f * s, stream));
+    pg.gram_nb = gnb;
+    const int gram_blocks = gnb * (gnb + 1) / 2;
+    int gram_splits = static_cast<int>(ceil_div(dev.sms, gram_blocks));
+    if (gram_splits > kMaxGramSplits) gram_splits = kMaxGramSplits;
+    if (gram_splits > k_tiles) gram_splits = k_tiles;
+    if (gram_splits < 1) gram_splits = 1;
+    DORA_TRY(launch_gemm_tc(mA_x, mA_y1, mA_y1, pg, gram_blocks, gram_splits, stream));
+    DORA_TRY(launch_gram_reduce(Gpart, gram_splits, gnb, gbw, rp, G, Ghi, Glo, 0.5f * s,
+                                stream));
 
 
     PairParams pp{};
@@ -348,9 +365,8 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     n_base = 1;
     n_cross = n_ba;
   }
-  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, pba, n_ba,
-                           static_cast<double>(s), m, bf16, static_cast<double>(eps), wnorm, g,
-                           stream));
+  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, pba, n_ba, s, m, bf16, eps,
+                           wnorm, g, stream));
   return DORA_OK;
 }
 

@@ -28,14 +28,15 @@ __device__ __forceinline__ void record_timeout(int* status) {
   atomicExch(status, kStatusTimeout);
 }
 
-__device__ __forceinline__ float sumsq_row128(const uint8_t* row) {
+__device__ __forceinline__ float sumsq_row128(const uint8_t* row, int rot) {
   // 128 bytes = 64 bf16 of one tile row; the 128-byte swizzle only permutes the
-  // 16-byte chunks inside the row, which a sum does not see.
+  // 16-byte chunks inside the row, which a sum does not see.  Starting at chunk
+  // (row mod 8) keeps the 8 threads of a shared-memory phase on different banks.
   const uint4* p = reinterpret_cast<const uint4*>(row);
   float acc = 0.f;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
-    const uint4 v = p[c];
+    const uint4 v = p[c ^ rot];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -65,7 +66,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int lane = threadIdx.x & 31;
   const int split = blockIdx.y;
   const int splits = gridDim.y;
-  const int row0 = blockIdx.x * kTcBlockM;
+  // Gram mode: CTA x handles the upper-triangular 128x128 block (bi, bj) of
+  // G = A A^T, i.e. X rows bi*128.. and Y rows bj*128..
+  int row0 = blockIdx.x * kTcBlockM;
+  int y_row0 = 0;
+  if (p.gram_nb > 0) {
+    int b = blockIdx.x, bi = 0;
+    while (b >= p.gram_nb - bi) {
+      b -= p.gram_nb - bi;
+      ++bi;
+    }
+    row0 = bi * kTcBlockM;
+    y_row0 = (bi + b) * kTcBlockM;
+  }
   const int kt_begin = static_cast<int>((static_cast<long long>(p.k_tiles) * split) / splits);
   const int kt_end = static_cast<int>((static_cast<long long>(p.k_tiles) * (split + 1)) / splits);
   const int n_iter = kt_end - kt_begin;
@@ -101,10 +114,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol_x = l2_policy_evict_first();
       const uint64_t pol_y = l2_policy_evict_last();
       int issued = 0;
+      const int stages = p.stages;
+      int s = 0;
+      uint32_t phase = 0;
       for (int i = 0; i < n_iter; ++i) {
-        const int s = i % p.stages;
-        const uint32_t use = static_cast<uint32_t>(i / p.stages);
-        if (i >= p.stages && !mbar_wait(&empty[s], (use - 1) & 1u, deadline)) {
+        if (i >= stages && !mbar_wait(&empty[s], phase ^ 1u, deadline)) {
           record_timeout(p.status);
           *abort_flag = 1;
           break;
@@ -119,8 +133,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive_expect_tx(&full[s], stage_bytes);
         tma_load_2d(xs, &tx, &full[s], kx, row0, pol_x);
         for (int c = 0; c < p.n_pad; c += p.y_box_rows)
-          tma_load_2d(ys + c * 128, ym, &full[s], kx, c, pol_y);
+          tma_load_2d(ys + c * 128, ym, &full[s], kx, y_row0 + c, pol_y);
         issued = i + 1;
+        if (++s == stages) {
+          s = 0;
+          phase ^= 1u;
+        }
       }
       // Never leave a copy landing in shared memory after this CTA is gone:
       // wait (bounded, with a fresh limit) for the last load of every stage.
@@ -146,10 +164,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t dy1_off = static_cast<uint64_t>(n0) * 128u >> 4;
       const uint64_t stage_step = stage_bytes >> 4;
       const int stages = p.stages;
+      int s = 0;
+      uint32_t phase = 0;
       for (int i = 0; i < n_iter; ++i) {
-        const int s = i % stages;
-        const uint32_t use = static_cast<uint32_t>(i / stages);
-        if (!mbar_wait(&full[s], use & 1u, deadline)) {
+        if (!mbar_wait(&full[s], phase, deadline)) {
           record_timeout(p.status);
           *abort_flag = 1;
           break;
@@ -165,6 +183,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (two) umma_bf16(tmem1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
         }
         umma_commit(&empty[s]);
+        if (++s == stages) {
+          s = 0;
+          phase ^= 1u;
+        }
       }
       // arrives once every MMA issued above has completed
       umma_commit(accum_full);
@@ -179,19 +201,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float ss = 0.f, ss_c = 0.f;
     bool ok = true;
     if (do_sumsq) {
+      const int stages = p.stages;
+      int s = 0;
+      uint32_t phase = 0;
       for (int i = 0; i < n_iter; ++i) {
-        const int s = i % p.stages;
-        const uint32_t use = static_cast<uint32_t>(i / p.stages);
-        if (!mbar_wait(&full[s], use & 1u, deadline)) {
+        if (!mbar_wait(&full[s], phase, deadline)) {
           record_timeout(p.status);
           *abort_flag = 1;
           ok = false;
           break;
         }
-        const float part = sumsq_row128(smem + s * stage_bytes + trow * 128);
+        const float part = sumsq_row128(smem + s * stage_bytes + trow * 128, trow & 7);
         kahan_add(ss, ss_c, part);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == stages) {
+          s = 0;
+          phase ^= 1u;
+        }
       }
     }
     if (!mbar_wait(accum_full, 0, deadline)) {
@@ -231,15 +258,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (valid) p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc;
       }
       if (p.mode & kTcStore) {
-        float* dst = p.out_store + static_cast<size_t>(split) * p.n_pad * p.n_pad;
+        // this CTA's [128 x n_pad] partial, row-major, slot (split, blockIdx.x)
+        float* dst = p.out_store +
+                     (static_cast<size_t>(split) * gridDim.x + blockIdx.x) * kTcBlockM * p.n_pad +
+                     static_cast<size_t>(trow) * p.n_pad;
         for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
           float v[32];
           tmem_load_32cols(tmem_row + static_cast<uint32_t>(c0), v);
-          if (grow < p.n_pad) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c0 + c < p.n_pad) dst[static_cast<size_t>(c0 + c) * p.n_pad + grow] = v[c];
-          }
+          for (int c = 0; c < 32; c += 4)
+            if (c0 + c < p.n_pad)
+              *reinterpret_cast<float4*>(dst + c0 + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
         }
       }
       if (do_sumsq && valid) p.out_sumsq[static_cast<size_t>(split) * p.rows + grow] = ss;

@@ -166,29 +166,53 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) out[row] = acc;
 }
 
-// G = sum over splits of the partial Gram tiles (fixed order), and the split
-// of scale * G into two bf16 terms G_hi + G_lo for the tensor-core BA-norm
-// tiles (about 16 significant bits of G survive the two bf16 terms).
-constexpr int kMaxGramParts = 16;
+// G = sum over K splits of the partial 128x128 Gram blocks (fixed order); the
+// upper-triangular block (bi, bj) is also written to (bj, bi).  Alongside, the
+// split of scale * G into two bf16 terms G_hi + G_lo for the tensor-core
+// BA-norm tiles (about 16 significant bits of G survive the two terms).
+constexpr int kMaxGramParts = 64;
 
-__global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int n_pad,
-                              float* __restrict__ G, uint16_t* __restrict__ G_hi,
+__global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int nb, int bw,
+                              int n_pad, float* __restrict__ G, uint16_t* __restrict__ G_hi,
                               uint16_t* __restrict__ G_lo, float scale) {
-  const int64_t n = static_cast<int64_t>(n_pad) * n_pad;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float v[kMaxGramParts];
-#pragma unroll
-    for (int s = 0; s < kMaxGramParts; ++s) v[s] = s < splits ? __ldg(parts + s * n + i) : 0.f;
+  // partial blocks are [128 rows x bw columns]; bw = 128, or n_pad when nb == 1
+  const int nblocks = nb * (nb + 1) / 2;
+  const int64_t per_block = static_cast<int64_t>(128) * bw;
+  const int64_t n = nblocks * per_block;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(idx / per_block);
+    const int i = static_cast<int>((idx / bw) % 128);
+    const int j = static_cast<int>(idx % bw);
+    int bi = 0, rem = b;
+    while (rem >= nb - bi) {
+      rem -= nb - bi;
+      ++bi;
+    }
+    const int bj = bi + rem;
+    const int gi = bi * 128 + i, gj = bj * 128 + j;
+    if (gi >= n_pad || gj >= n_pad) continue;
+    // loads issued eight at a time ahead of the (fixed-order) sum
     float acc = 0.f;
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+      float v[8];
 #pragma unroll
-    for (int s = 0; s < kMaxGramParts; ++s) acc = __fadd_rn(acc, v[s]);
-    G[i] = acc;
-    if (G_hi) {
-      const float sc = __fmul_rn(scale, acc);
-      const uint16_t hi = f32_to_bf16_rn(sc);
-      G_hi[i] = hi;
-      G_lo[i] = f32_to_bf16_rn(__fsub_rn(sc, bf16_to_f32(hi)));
+      for (int u = 0; u < 8; ++u) v[u] = s0 + u < splits ? __ldg(parts + (s0 + u) * n + idx) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc = __fadd_rn(acc, v[u]);
+    }
+    const float sc = __fmul_rn(scale, acc);
+    const uint16_t hi = f32_to_bf16_rn(sc);
+    const uint16_t lo = f32_to_bf16_rn(__fsub_rn(sc, bf16_to_f32(hi)));
+    const int64_t o = static_cast<int64_t>(gi) * n_pad + gj;
+    G[o] = acc;
+    G_hi[o] = hi;
+    G_lo[o] = lo;
+    if (bi != bj) {
+      const int64_t t = static_cast<int64_t>(gj) * n_pad + gi;
+      G[t] = acc;
+      G_hi[t] = hi;
+      G_lo[t] = lo;
     }
   }
 }
@@ -198,35 +222,91 @@ __global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int n
 // in split order; the assembly, root and divide run in fp64 and round once.
 constexpr int kMaxFinalParts = 16;
 
-__global__ void k_finalize(int64_t d_out, const float* __restrict__ pbase, int n_base,
-                           const float* __restrict__ pcross, int n_cross,
-                           const float* __restrict__ pba, int n_ba, double s,
-                           const void* __restrict__ m, int is_bf16, double eps,
-                           float* __restrict__ wnorm, float* __restrict__ g) {
+// ---- double-float arithmetic: a value carried as hi + lo (two fp32)
+// exact sum of two floats (Knuth's TwoSum)
+__device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) {
+  hi = __fadd_rn(a, b);
+  const float bb = __fsub_rn(hi, a);
+  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+}
+
+struct df {
+  float hi, lo;
+};
+
+__device__ __forceinline__ df df_add(df a, df b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+  df r;
+  two_sum(s, e, r.hi, r.lo);
+  return r;
+}
+
+// a * c for a float c, exact product of the hi parts (FMA-based TwoProduct)
+__device__ __forceinline__ df df_mul_f(df a, float c) {
+  const float p = __fmul_rn(a.hi, c);
+  const float e = fmaf(a.hi, c, -p);
+  df r;
+  two_sum(p, fmaf(a.lo, c, e), r.hi, r.lo);
+  return r;
+}
+
+// sum of n fp32 partials in split order, as a double-float
+__device__ __forceinline__ df sum_parts(const float* __restrict__ p, int n, int64_t stride,
+                                        int64_t j) {
+  float v[kMaxFinalParts];
+#pragma unroll
+  for (int i = 0; i < kMaxFinalParts; ++i) v[i] = i < n ? __ldg(p + i * stride + j) : 0.f;
+  df acc{0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kMaxFinalParts; ++i) {
+    float e;
+    two_sum(acc.hi, v[i], acc.hi, e);
+    acc.lo = __fadd_rn(acc.lo, e);
+  }
+  return acc;
+}
+
+// wnorm = sqrt(max(base + 2 s cross + s^2 ba, 0)), g = m / max(wnorm, eps)
+// (Chinese write-up section 1.2.2, Algorithm 1 step 6).  Partials are summed
+// in split order; the assembly is carried in double-float (about 44
+// significant bits) and the root and the divide are each an IEEE fp32
+// operation refined by one Newton step on the double-float residual, then
+// rounded once -- no fp64 units involved (they are scarce on this part).
+__global__ void __launch_bounds__(64)
+    k_finalize(int64_t d_out, const float* __restrict__ pbase, int n_base,
+               const float* __restrict__ pcross, int n_cross, const float* __restrict__ pba,
+               int n_ba, float two_s, float s_sq, const void* __restrict__ m, int is_bf16,
+               float eps, float* __restrict__ wnorm, float* __restrict__ g) {
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= d_out) return;
-  // all partial loads are issued before the (fixed-order) sums
-  float vb[kMaxFinalParts], vc[kMaxFinalParts], va[kMaxFinalParts];
-#pragma unroll
-  for (int i = 0; i < kMaxFinalParts; ++i) {
-    vb[i] = i < n_base ? __ldg(pbase + i * d_out + j) : 0.f;
-    vc[i] = i < n_cross ? __ldg(pcross + i * d_out + j) : 0.f;
-    va[i] = i < n_ba ? __ldg(pba + i * d_out + j) : 0.f;
+  const df base = sum_parts(pbase, n_base, d_out, j);
+  const df cross = sum_parts(pcross, n_cross, d_out, j);
+  df w2 = df_add(base, df_mul_f(cross, two_s));
+  if (n_ba > 0) w2 = df_add(w2, df_mul_f(sum_parts(pba, n_ba, d_out, j), s_sq));
+  // clamp at zero under the root
+  if (w2.hi < 0.f || (w2.hi == 0.f && w2.lo <= 0.f)) w2 = df{0.f, 0.f};
+  // root: y = sqrt(hi) rounded, then y + (w2 - y^2) / (2 y)
+  float wn_hi = 0.f, wn_lo = 0.f;
+  if (w2.hi > 0.f) {
+    const float y = __fsqrt_rn(w2.hi);
+    const float res = __fadd_rn(fmaf(-y, y, w2.hi), w2.lo);     // w2 - y^2 (y^2 exact via FMA)
+    two_sum(y, __fdiv_rn(res, __fmul_rn(2.f, y)), wn_hi, wn_lo);
   }
-  double base = 0.0, cross = 0.0, ba = 0.0;
-#pragma unroll
-  for (int i = 0; i < kMaxFinalParts; ++i) {
-    base += static_cast<double>(vb[i]);
-    cross += static_cast<double>(vc[i]);
-    ba += static_cast<double>(va[i]);
+  const float mj = is_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(m)[j])
+                           : static_cast<const float*>(m)[j];
+  // divisor max(wnorm, eps) as a double-float
+  float d_hi = wn_hi, d_lo = wn_lo;
+  if (wn_hi < eps || (wn_hi == eps && wn_lo < 0.f)) {
+    d_hi = eps;
+    d_lo = 0.f;
   }
-  const double w2 = __dadd_rn(__dadd_rn(base, __dmul_rn(__dmul_rn(2.0, s), cross)),
-                              __dmul_rn(__dmul_rn(s, s), ba));
-  const double wn = sqrt(fmax(w2, 0.0));
-  const double mj = is_bf16 ? static_cast<double>(bf16_to_f32(static_cast<const uint16_t*>(m)[j]))
-                            : static_cast<double>(static_cast<const float*>(m)[j]);
-  wnorm[j] = static_cast<float>(wn);
-  g[j] = static_cast<float>(mj / fmax(wn, eps));
+  // quotient: q = m / d_hi rounded, then q + (m - q d) / d_hi
+  const float q = __fdiv_rn(mj, d_hi);
+  const float res = __fsub_rn(fmaf(-q, d_hi, mj), __fmul_rn(q, d_lo));   // m - q d
+  wnorm[j] = __fadd_rn(wn_hi, wn_lo);
+  g[j] = __fadd_rn(q, __fdiv_rn(res, d_hi));
 }
 
 }  // namespace
@@ -251,25 +331,28 @@ cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t c
   return cudaGetLastError();
 }
 
-cudaError_t launch_gram_reduce(const float* parts, int splits, int n_pad, float* G,
-                               uint16_t* G_hi, uint16_t* G_lo, float scale, cudaStream_t stream) {
+cudaError_t launch_gram_reduce(const float* parts, int splits, int nb, int bw, int n_pad,
+                               float* G, uint16_t* G_hi, uint16_t* G_lo, float scale,
+                               cudaStream_t stream) {
   if (splits > kMaxGramParts) return cudaErrorInvalidValue;
-  const int64_t n = static_cast<int64_t>(n_pad) * n_pad;
+  const int64_t n = static_cast<int64_t>(nb) * (nb + 1) / 2 * 128 * bw;
   const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-  k_gram_reduce<<<blocks, 256, 0, stream>>>(parts, splits, n_pad, G, G_hi, G_lo, scale);
+  k_gram_reduce<<<blocks, 256, 0, stream>>>(parts, splits, nb, bw, n_pad, G, G_hi, G_lo, scale);
   note_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
-                            int n_cross, const float* pba, int n_ba, double s, const void* m,
-                            int is_bf16, double eps, float* wnorm, float* g,
+                            int n_cross, const float* pba, int n_ba, float s, const void* m,
+                            int is_bf16, float eps, float* wnorm, float* g,
                             cudaStream_t stream) {
   if (n_base > kMaxFinalParts || n_cross > kMaxFinalParts || n_ba > kMaxFinalParts)
     return cudaErrorInvalidValue;
-  const unsigned blocks = static_cast<unsigned>((d_out + 127) / 128);
-  k_finalize<<<blocks, 128, 0, stream>>>(d_out, pbase, n_base, pcross, n_cross, pba, n_ba, s, m,
-                                         is_bf16, eps, wnorm, g);
+  const unsigned blocks = static_cast<unsigned>((d_out + 63) / 64);
+  // 2s and s^2 are exact in fp32 for the power-of-two scales; otherwise they
+  // carry one rounding each, far below the fp32 result's own rounding
+  k_finalize<<<blocks, 64, 0, stream>>>(d_out, pbase, n_base, pcross, n_cross, pba, n_ba,
+                                        2.f * s, s * s, m, is_bf16, eps, wnorm, g);
   note_launches(1);
   return cudaGetLastError();
 }
