@@ -92,8 +92,6 @@ struct PairParams {
   int prefetch;          // W tiles pulled into L2 this many tiles ahead
   uint32_t tmem_cols;
   const uint16_t* B;     // [rows x r] bf16
-  const uint16_t* W;     // [rows x d_in] bf16 (read directly for the sum of squares)
-  int d_in;
   float* out_sumsq;      // [splits][rows]
   float* out_dot;        // [splits][rows]
   int* status;

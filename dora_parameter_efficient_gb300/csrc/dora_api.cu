@@ -10,6 +10,7 @@
 
 #include "dora.h"
 #include "common.cuh"
+#include "finalize.cuh"
 
 namespace dora {
 
@@ -19,6 +20,7 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::
 namespace {
 
 constexpr int kMaxMainSplits = 16;
+static_assert(kMaxMainSplits <= kMaxFinalParts, "the fused finalize sums at most kMaxFinalParts splits");
 constexpr int kMaxGramSplits = 24;   // K splits of the Gram blocks (workspace sized for this)
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
@@ -102,7 +104,7 @@ struct Plan {
   int rp = 0;               // r rounded up to 16 (the MMA N extent)
   int main_splits = 1;      // split-K of the main pass (tensor-core path)
   int gram_splits = 1;
-  size_t off_status = 0, off_G = 0, off_Ghi = 0, off_Glo = 0, off_Gpart = 0;
+  size_t off_status = 0, zero_bytes = 0, off_G = 0, off_Ghi = 0, off_Glo = 0, off_Gpart = 0;
   size_t off_pbase = 0, off_pcross = 0, off_pba = 0, total = 0;
   int cap_base = 0, cap_cross = 0, cap_ba = 0;
 };
@@ -136,6 +138,7 @@ Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
   size_t off = 0;
   p.off_status = off;
   off += 256;
+  p.zero_bytes = off;
   const size_t rp2 = static_cast<size_t>(p.rp) * p.rp;
   p.off_G = off;
   off = align_up(off + rp2 * 4, 256);
@@ -251,7 +254,7 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
   float* pba = reinterpret_cast<float*>(ws + plan.off_pba);
 
-  DORA_TRY(cudaMemsetAsync(status, 0, 256, stream));
+  DORA_TRY(cudaMemsetAsync(status, 0, plan.zero_bytes, stream));
 
   int n_base = 0, n_cross = 0, n_ba = 0;
   if (d_in == 0) {
@@ -332,8 +335,6 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     pp.prefetch = 4;
     pp.tmem_cols = tmem_cols;
     pp.B = static_cast<const uint16_t*>(B);
-    pp.W = static_cast<const uint16_t*>(W);
-    pp.d_in = static_cast<int>(d_in);
     pp.out_sumsq = pbase;
     pp.out_dot = pcross;
     pp.status = status;

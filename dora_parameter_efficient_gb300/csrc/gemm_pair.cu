@@ -12,7 +12,8 @@
 // G'_hi + G'_lo = (s/2) G (two bf16 terms, computed beforehand).  Because the
 // epilogue is linear in D, summing dot over the splits gives
 // cross + (s/2) ba, and 2s (cross + (s/2) ba) = 2s cross + s^2 ba is exactly
-// what the norm needs; the finalize kernel adds the base term.
+// what the norm needs; the finalize kernel, launched behind this one as a
+// programmatic dependent, adds the base term.
 //
 // Tiling for sm_103a:
 //   * a cluster of 2 CTAs on 2 SMs forms one tcgen05 "CTA pair": the even CTA
@@ -23,14 +24,17 @@
 //   * the accumulator D [128 x r] of each CTA lives in its own tensor memory;
 //   * warp 0 of each CTA issues the TMA loads of its half; all loads of a
 //     stage complete on the even CTA's `full` barrier; the even CTA's MMA
-//     thread waits on it and commits `empty` to both CTAs -- the only
-//     hand-off on the shared-memory pipeline;
-//   * warps 2-9 of each CTA stay off that pipeline: while the MMAs run they
-//     stream their 128 rows of W straight from global memory (coalesced,
-//     4 rows x 128 bytes per warp instruction) for the sum of squares and
-//     fetch their half of each B row into registers; then two warps per TMEM
-//     lane quadrant read the halves of the D rows (tcgen05.ld), dot them with
-//     B and add the halves in a fixed order;
+//     thread waits on it and, once the stage's MMAs are done, commits
+//     `consumed` to both CTAs;
+//   * warps 2-9 of each CTA then take the sum of squares of the stage's W
+//     tile from shared memory (the bytes the MMAs just read: W leaves HBM
+//     once) and release the stage to the producer (`empty`); spread over
+//     the item's first tiles, each thread also fetches one 16-byte piece of
+//     its B row per tile into registers, so no burst of global loads
+//     competes with the TMA and MMA instructions;
+//   * at the end of an item two warps per TMEM lane quadrant read the halves
+//     of the D rows (tcgen05.ld), dot them with B and add the halves in a
+//     fixed order;
 //   * the grid is persistent: cluster c processes work items c, c + C, ...,
 //     an item being (256-row tile, K split); the TMA producer runs ahead into
 //     the next item while the epilogue drains the accumulator.
@@ -54,14 +58,6 @@ __device__ __forceinline__ float sumsq8(const uint4 v) {
     acc = fmaf(b, b, acc);
   }
   return acc;
-}
-
-__device__ __forceinline__ uint4 ldg_stream(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
 }
 
 // Columns [c0, c0 + 8 * N) of one row of B (bf16); columns past r read as 0.
@@ -92,6 +88,16 @@ __device__ __forceinline__ float dot_b(const uint4 (&b)[N], const float* v, floa
   return acc;
 }
 
+// 16 bytes through the read-only path; volatile so the compiler keeps each
+// load where it is written (spread over the K loop, not bunched)
+__device__ __forceinline__ uint4 ldg_keep_order(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void item_range(const PairParams& p, int item, int& tile, int& split,
                                            int& kb, int& ke) {
   tile = item / p.splits;
@@ -104,6 +110,7 @@ __device__ __forceinline__ void item_range(const PairParams& p, int item, int& t
 // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per tensor-memory lane quadrant)
 constexpr int kPairThreads = 320;
 constexpr int kPairEpiThreads = 256;
+constexpr int kPairEpiWarps = kPairEpiThreads / 32;
 
 __global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tA,
@@ -116,11 +123,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t stage_bytes = kTcXTileBytes + half_rows * 128u;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
   uint64_t* empty = full + p.stages;
-  uint64_t* accum_full = empty + p.stages;
+  uint64_t* consumed = empty + p.stages;
+  uint64_t* accum_full = consumed + p.stages;
   uint64_t* accum_empty = accum_full + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  float* dot_half = reinterpret_cast<float*>(tmem_holder + 4);   // [128] second-half dots
+  float* dot_half = reinterpret_cast<float*>(tmem_holder + 4);   // [2][128] second-half dots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -133,13 +141,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kPairEpiWarps);   // every epilogue warp has read the W tile
+      mbar_init(&consumed[s], 1);            // the stage's MMAs are done
     }
     mbar_init(accum_full, 1);
     mbar_init(accum_empty, 16);     // 8 epilogue warps in each CTA of the pair
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // the finalize kernel behind this one may start launching (it waits for
+  // this grid to finish before it reads anything)
+  griddep_launch_dependents();
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tW);
     tma_prefetch_desc(&tA);
@@ -168,12 +180,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // runtime division per tile sits on the issuing thread's critical path)
       uint32_t s = 0, phase = 0, it = 0;
       bool stop = false;
+      bool g_ready = false;      // G'_hi / G'_lo written by the preceding kernel
       for (int item = cid; item < n_items && !stop; item += ncl) {
         int tile, split, kb, ke;
         item_range(p, item, tile, split, kb, ke);
         const int row0 = tile * 256 + static_cast<int>(rank) * 128;
         for (int kt = kb; kt < ke; ++kt, ++it) {
           // the slot's previous use (parity phase ^ 1) must have been consumed
+          // by the MMAs and read by the epilogue warps
           if (it >= stages && !mbar_wait(&empty[s], phase ^ 1u, deadline)) {
             atomicExch(p.status, kStatusTimeout);
             *abort_flag = 1;
@@ -188,10 +202,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             // pull a later W tile of this item into L2 while this one loads
             const int kpf = kt + p.prefetch;
             if (kpf < ke && kpf < p.kt_w) tma_prefetch_l2_2d(&tW, kpf * kTcBlockK, row0);
-          } else if (kt < p.kt_w + p.kt_b) {
-            xm = &tB; ym = &tGhi; kx = (kt - p.kt_w) * kTcBlockK;
           } else {
-            xm = &tB; ym = &tGlo; kx = (kt - p.kt_w - p.kt_b) * kTcBlockK;
+            // a G' tile (an item may start in either half of the G' range)
+            if (!g_ready) {
+              griddep_wait();
+              g_ready = true;
+            }
+            xm = &tB;
+            if (kt < p.kt_w + p.kt_b) {
+              ym = &tGhi; kx = (kt - p.kt_w) * kTcBlockK;
+            } else {
+              ym = &tGlo; kx = (kt - p.kt_w - p.kt_b) * kTcBlockK;
+            }
           }
           uint8_t* xs = smem + s * stage_bytes;
           uint8_t* ys = xs + kTcXTileBytes;
@@ -263,7 +285,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             umma_bf16_pair(tmem_base, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
             if (two) umma_bf16_pair(tmem1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
           }
-          umma_commit_pair(&empty[s], 0x3);
+          umma_commit_pair(&consumed[s], 0x3);
           if (++s == stages) {
             s = 0;
             phase ^= 1u;
@@ -276,7 +298,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (icount > 0 && !mbar_wait(accum_full, (icount - 1) & 1, global_timer_ns() + p.timeout_ns))
         atomicExch(p.status, kStatusTimeout);
     }
-  } else {
+  } else if (warp < 2 + kPairEpiWarps) {
     // -------------------------------------------------------------- epilogue (both CTAs)
     // Warps 2-9: quadrant q = warp % 4 (the TMEM lanes = tile rows this warp
     // may read), half h = (warp - 2) / 4.  Half h owns accumulator columns
@@ -290,10 +312,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const int nchunk = (p.r + 31) / 32;              // 32-column chunks of the accumulator
     const int c_lo = h == 0 ? 0 : (nchunk + 1) / 2;
     const int c_hi = h == 0 ? (nchunk + 1) / 2 : nchunk;
-    // sum-of-squares mapping: one warp instruction reads 4 rows x 128 bytes;
-    // lane = 8 * sub + chunk reads row (16h + 4 * r4 + sub), 16-byte chunk `chunk`
+    // sum-of-squares mapping inside a stage's W tile (128 rows x 128 bytes,
+    // 16-byte chunks permuted within each row by the 128-byte swizzle, which
+    // a row sum does not see): one warp instruction reads 4 whole rows; lane
+    // 8 * sub + chunk reads chunk `chunk` of row 32q + 16h + 4 * r4 + sub.
+    // Columns and rows past the matrix were zero-filled by the TMA.
     const int sub = lane >> 3;
     const int chunk = lane & 7;
+    const uint32_t x_off = static_cast<uint32_t>((q * 32 + 16 * h + sub) * 128 + chunk * 16);
+    const uint32_t smem0 = smem_u32(smem);
+    const uint32_t stages = static_cast<uint32_t>(p.stages);
+    uint32_t s = 0, phase = 0;          // stage ring position (the producer's sequence)
+    bool alive = true;                  // false once a wait has timed out
     int icount = 0;
     for (int item = cid; item < n_items; item += ncl, ++icount) {
       int tile, split, kb, ke;
@@ -303,35 +333,50 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const bool valid = grow < p.rows;
       const uint16_t* brow = p.B + static_cast<size_t>(valid ? grow : 0) * p.r;
 
-      // ---- sum of squares of 16 rows over the item's W columns
       float sacc[4], scmp[4];
 #pragma unroll
       for (int r4 = 0; r4 < 4; ++r4) sacc[r4] = scmp[r4] = 0.f;
-      const uint16_t* wrow[4];
-      bool wvalid[4];
-#pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) {
-        const int row = rowbase + 16 * h + 4 * r4 + sub;
-        wvalid[r4] = row < p.rows;
-        wrow[r4] = p.W + static_cast<size_t>(wvalid[r4] ? row : 0) * p.d_in + chunk * 8;
-      }
-      const int kw_end = ke < p.kt_w ? ke : p.kt_w;
-      for (int kt = kb; kt < kw_end; kt += 4) {
-        uint4 v[4][4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int col = (kt + u) * kTcBlockK + chunk * 8;
-          const bool cok = kt + u < kw_end && col < p.d_in;
-#pragma unroll
-          for (int r4 = 0; r4 < 4; ++r4)
-            v[u][r4] = (cok && wvalid[r4]) ? ldg_stream(wrow[r4] + (kt + u) * kTcBlockK)
-                                           : make_uint4(0u, 0u, 0u, 0u);
+      // one tile of the item: wait for its MMAs, sum squares of the W tile, release it
+      auto epi_tile = [&](int kt) {
+        if (alive && !mbar_wait(&consumed[s], phase, deadline)) {
+          atomicExch(p.status, kStatusTimeout);
+          *abort_flag = 1;
+          alive = false;
         }
+        if (alive && kt < p.kt_w) {
+          const uint32_t xa = smem0 + s * stage_bytes + x_off;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+          for (int r4 = 0; r4 < 4; ++r4) {
+            uint4 v;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(xa + r4 * 512u));
+            kahan_add(sacc[r4], scmp[r4], sumsq8(v));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == stages) {
+          s = 0;
+          phase ^= 1u;
+        }
+      };
+      // up to 192 columns of this lane's B half-row, two 16-byte pieces per tile
+      uint4 bb[24];
+      int kt = kb;
 #pragma unroll
-          for (int r4 = 0; r4 < 4; ++r4) kahan_add(sacc[r4], scmp[r4], sumsq8(v[u][r4]));
+      for (int v = 0; v < 24; v += 2) {
+        if (kt < ke) epi_tile(kt++);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col = c_lo * 32 + (v + u) * 8;
+          bb[v + u] = (valid && col < c_hi * 32 && col < p.r) ? ldg_keep_order(brow + col)
+                                                              : make_uint4(0u, 0u, 0u, 0u);
+        }
       }
+#pragma unroll 1
+      for (; kt < ke; ++kt) epi_tile(kt);
+
       // fold the 8 chunk lanes of each row; lane L < 16 then takes row 16h + L
       float ss = 0.f;
 #pragma unroll
@@ -348,18 +393,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (lane < 16 && srow < p.rows) p.out_sumsq[static_cast<size_t>(split) * p.rows + srow] = ss;
       }
 
-      // ---- this half's part of rowsum(B o D).  Up to 192 columns of the B
-      // row are fetched into registers before the accumulator is complete.
-      uint4 bb[24];
-#pragma unroll
-      for (int v = 0; v < 24; ++v) {
-        const int col = c_lo * 32 + v * 8;
-        bb[v] = (valid && col < c_hi * 32 && col < p.r)
-                    ? __ldg(reinterpret_cast<const uint4*>(brow + col))
-                    : make_uint4(0u, 0u, 0u, 0u);
-      }
-      bool ok = mbar_wait(accum_full, icount & 1, deadline);
-      if (!ok) {
+      bool ok = alive && mbar_wait(accum_full, icount & 1, deadline);
+      if (alive && !ok) {
         atomicExch(p.status, kStatusTimeout);
         *abort_flag = 1;
       }
@@ -379,22 +414,42 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       float acc = 0.f;
       if (ok) {
+        // chunks c_lo .. c_lo + 5, B held in bb; pieces at or past the padded
+        // rank were never written by an MMA
+        const int rp = p.n0 + p.n1;
 #pragma unroll
-        for (int j = 0; j < 6; ++j) {            // chunks c_lo + j held in bb
+        for (int j = 0; j < 6; ++j) {
           const int c = c_lo + j;
-          if (c < c_hi) {
+          if (c < c_hi && c * 32 < rp) {
             float v[32];
-            tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
+            if (c * 32 + 32 <= rp) {
+              tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
+            } else {          // only the first 16 columns of this chunk exist
+              uint32_t rv[16];
+              tmem_load_16cols_async(tmem_row + static_cast<uint32_t>(c * 32), rv);
+              tmem_wait_ld(rv);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                v[i] = __uint_as_float(rv[i]);
+                v[16 + i] = 0.f;
+              }
+            }
             const uint4 part[4] = {bb[4 * j], bb[4 * j + 1], bb[4 * j + 2], bb[4 * j + 3]};
             acc = dot_b<4>(part, v, acc);
           }
         }
-        for (int c = c_lo + 6; c < c_hi; ++c) {   // ranks above 384: the rest, loaded now
-          uint4 part[4];
-          load_b_cols<4>(brow, c * 32, p.r, valid, part);
-          float v[32];
-          tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
-          acc = dot_b<4>(part, v, acc);
+        // ranks above 384: the rest of the half, B loaded now
+        const int col_end = c_hi * 32 < rp ? c_hi * 32 : rp;
+        for (int col = (c_lo + 6) * 32; col < col_end; col += 16) {
+          uint4 part[2];
+          load_b_cols<2>(brow, col, p.r, valid, part);
+          uint32_t rv[16];
+          tmem_load_16cols_async(tmem_row + static_cast<uint32_t>(col), rv);
+          tmem_wait_ld(rv);
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rv[i]);
+          acc = dot_b<2>(part, v, acc);
         }
       }
       // accumulator drained: let the even CTA start the next item's MMAs
@@ -402,12 +457,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(accum_empty0);
       if (!ok) break;
-      // first half + second half, in that order, for each row
-      if (h == 1) dot_half[trow] = acc;
+      // first half + second half, in that order, for each row (the halves
+      // alternate between two buffers, so one barrier per item suffices)
+      float* dh = dot_half + (icount & 1) * 128;
+      if (h == 1) dh[trow] = acc;
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
-      if (h == 0 && valid)
-        p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc + dot_half[trow];
-      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
+      if (h == 0 && valid) p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc + dh[trow];
     }
   }
 
@@ -425,7 +480,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 size_t pair_smem_bytes(int n_pad, int stages) {
   const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
-  return 1024 + stage * stages + (2 * stages + 2) * 8 + 16 + 128 * 4;
+  return 1024 + stage * stages + (3 * stages + 3) * 8 + 16 + 2 * 128 * 4;
 }
 
 int pair_pick_stages(int n_pad) {
@@ -473,13 +528,17 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
   cfg.blockDim = dim3(kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the Gram reduction still runs: only the TMA producer's
+  // G' loads depend on it, and they wait for it (griddep_wait)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair, tW, tA, tB, tGhi, tGlo, p);
   note_launches(1);
   if (e != cudaSuccess) return e;

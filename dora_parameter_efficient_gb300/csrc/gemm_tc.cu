@@ -51,6 +51,9 @@ __device__ __forceinline__ float sumsq_row128(const uint8_t* row, int rot) {
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap ty0,
               const __grid_constant__ CUtensorMap ty1, const TcParams p) {
+  // the kernel queued behind this one may start launching; it waits for this
+  // grid to finish before it reads any of its results
+  griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

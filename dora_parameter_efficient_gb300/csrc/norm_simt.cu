@@ -1,6 +1,6 @@
 // norm_simt.cu -- fp32-input pieces of the factored norm on CUDA cores, plus
 // the small kernels shared by both input types (row sum of squares for the
-// s = 0 branch, the Gram-partial reduction, and the fp64 finalize).
+// s = 0 branch, the Gram-partial reduction, and the stand-alone finalize).
 //
 // The fp32 path computes the same three terms as the bf16 tensor-core path
 // ("Scaling DoRA", Chinese write-up section 1.2.1; Algorithm 1, section 5.1)
@@ -11,6 +11,8 @@
 // and the sum of squares is accumulated per 16-column chunk, then
 // compensated.
 #include "common.cuh"
+#include "finalize.cuh"
+#include "ptx.cuh"
 
 namespace dora {
 
@@ -175,6 +177,13 @@ constexpr int kMaxGramParts = 64;
 __global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int nb, int bw,
                               int n_pad, float* __restrict__ G, uint16_t* __restrict__ G_hi,
                               uint16_t* __restrict__ G_lo, float scale) {
+  // the main pass (launched behind this kernel with programmatic stream
+  // serialization) may start launching now; it waits for this grid to
+  // finish before it reads G'
+  griddep_launch_dependents();
+  // launched as a programmatic dependent of the Gram kernel: its partials
+  // are read only once it has finished
+  griddep_wait();
   // partial blocks are [128 rows x bw columns]; bw = 128, or n_pad when nb == 1
   const int nblocks = nb * (nb + 1) / 2;
   const int64_t per_block = static_cast<int64_t>(128) * bw;
@@ -217,96 +226,31 @@ __global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int n
   }
 }
 
-// wnorm = sqrt(max(base + 2 s cross + s^2 ba, 0)), g = m / max(wnorm, eps)
-// (Chinese write-up section 1.2.2, Algorithm 1 step 6).  Partials are summed
-// in split order; the assembly, root and divide run in fp64 and round once.
-constexpr int kMaxFinalParts = 16;
-
-// ---- double-float arithmetic: a value carried as hi + lo (two fp32)
-// exact sum of two floats (Knuth's TwoSum)
-__device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) {
-  hi = __fadd_rn(a, b);
-  const float bb = __fsub_rn(hi, a);
-  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
-}
-
-struct df {
-  float hi, lo;
-};
-
-__device__ __forceinline__ df df_add(df a, df b) {
-  float s, e;
-  two_sum(a.hi, b.hi, s, e);
-  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
-  df r;
-  two_sum(s, e, r.hi, r.lo);
-  return r;
-}
-
-// a * c for a float c, exact product of the hi parts (FMA-based TwoProduct)
-__device__ __forceinline__ df df_mul_f(df a, float c) {
-  const float p = __fmul_rn(a.hi, c);
-  const float e = fmaf(a.hi, c, -p);
-  df r;
-  two_sum(p, fmaf(a.lo, c, e), r.hi, r.lo);
-  return r;
-}
-
 // sum of n fp32 partials in split order, as a double-float
 __device__ __forceinline__ df sum_parts(const float* __restrict__ p, int n, int64_t stride,
                                         int64_t j) {
   float v[kMaxFinalParts];
 #pragma unroll
   for (int i = 0; i < kMaxFinalParts; ++i) v[i] = i < n ? __ldg(p + i * stride + j) : 0.f;
-  df acc{0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < kMaxFinalParts; ++i) {
-    float e;
-    two_sum(acc.hi, v[i], acc.hi, e);
-    acc.lo = __fadd_rn(acc.lo, e);
-  }
-  return acc;
+  return df_sum_in_order(v);
 }
 
-// wnorm = sqrt(max(base + 2 s cross + s^2 ba, 0)), g = m / max(wnorm, eps)
-// (Chinese write-up section 1.2.2, Algorithm 1 step 6).  Partials are summed
-// in split order; the assembly is carried in double-float (about 44
-// significant bits) and the root and the divide are each an IEEE fp32
-// operation refined by one Newton step on the double-float residual, then
-// rounded once -- no fp64 units involved (they are scarce on this part).
+// One thread per output row: the finalize step written out in finalize.cuh.
 __global__ void __launch_bounds__(64)
     k_finalize(int64_t d_out, const float* __restrict__ pbase, int n_base,
                const float* __restrict__ pcross, int n_cross, const float* __restrict__ pba,
                int n_ba, float two_s, float s_sq, const void* __restrict__ m, int is_bf16,
                float eps, float* __restrict__ wnorm, float* __restrict__ g) {
+  // launched as a programmatic dependent of the pass that wrote the partials
+  griddep_wait();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= d_out) return;
   const df base = sum_parts(pbase, n_base, d_out, j);
   const df cross = sum_parts(pcross, n_cross, d_out, j);
-  df w2 = df_add(base, df_mul_f(cross, two_s));
-  if (n_ba > 0) w2 = df_add(w2, df_mul_f(sum_parts(pba, n_ba, d_out, j), s_sq));
-  // clamp at zero under the root
-  if (w2.hi < 0.f || (w2.hi == 0.f && w2.lo <= 0.f)) w2 = df{0.f, 0.f};
-  // root: y = sqrt(hi) rounded, then y + (w2 - y^2) / (2 y)
-  float wn_hi = 0.f, wn_lo = 0.f;
-  if (w2.hi > 0.f) {
-    const float y = __fsqrt_rn(w2.hi);
-    const float res = __fadd_rn(fmaf(-y, y, w2.hi), w2.lo);     // w2 - y^2 (y^2 exact via FMA)
-    two_sum(y, __fdiv_rn(res, __fmul_rn(2.f, y)), wn_hi, wn_lo);
-  }
+  const df ba = n_ba > 0 ? sum_parts(pba, n_ba, d_out, j) : df{0.f, 0.f};
   const float mj = is_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(m)[j])
                            : static_cast<const float*>(m)[j];
-  // divisor max(wnorm, eps) as a double-float
-  float d_hi = wn_hi, d_lo = wn_lo;
-  if (wn_hi < eps || (wn_hi == eps && wn_lo < 0.f)) {
-    d_hi = eps;
-    d_lo = 0.f;
-  }
-  // quotient: q = m / d_hi rounded, then q + (m - q d) / d_hi
-  const float q = __fdiv_rn(mj, d_hi);
-  const float res = __fsub_rn(fmaf(-q, d_hi, mj), __fmul_rn(q, d_lo));   // m - q d
-  wnorm[j] = __fadd_rn(wn_hi, wn_lo);
-  g[j] = __fadd_rn(q, __fdiv_rn(res, d_hi));
+  finalize_row(base, cross, n_ba > 0 ? &ba : nullptr, two_s, s_sq, mj, eps, wnorm[j], g[j]);
 }
 
 }  // namespace
@@ -337,8 +281,19 @@ cudaError_t launch_gram_reduce(const float* parts, int splits, int nb, int bw, i
   if (splits > kMaxGramParts) return cudaErrorInvalidValue;
   const int64_t n = static_cast<int64_t>(nb) * (nb + 1) / 2 * 128 * bw;
   const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-  k_gram_reduce<<<blocks, 256, 0, stream>>>(parts, splits, nb, bw, n_pad, G, G_hi, G_lo, scale);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gram_reduce, parts, splits, nb, bw, n_pad, G,
+                                           G_hi, G_lo, scale);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -351,9 +306,22 @@ cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const
   const unsigned blocks = static_cast<unsigned>((d_out + 63) / 64);
   // 2s and s^2 are exact in fp32 for the power-of-two scales; otherwise they
   // carry one rounding each, far below the fp32 result's own rounding
-  k_finalize<<<blocks, 64, 0, stream>>>(d_out, pbase, n_base, pcross, n_cross, pba, n_ba,
-                                        2.f * s, s * s, m, is_bf16, eps, wnorm, g);
+  // may start while the producing kernel still runs; griddep_wait in the
+  // kernel holds every read until that kernel has finished
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(64, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_finalize, d_out, pbase, n_base, pcross,
+                                           n_cross, pba, n_ba, 2.f * s, s * s, m, is_bf16, eps,
+                                           wnorm, g);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -98,8 +98,10 @@ size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtyp
  * multiples of 16 bytes; W, A, B 16-byte aligned; r <= DORA_MAX_RANK.
  * wnorm and g must not overlap each other or any input.
  * Precision: products of the stored inputs are exact in fp32, every sum is
- * accumulated in fp32, the three terms are assembled, square-rooted and
- * divided in fp64 and rounded once to fp32.
+ * accumulated in fp32; the three terms are assembled in double-float
+ * arithmetic (a value held as an unevaluated sum of two floats, about 48
+ * significant bits), the square root and the division each take one
+ * correction step in that arithmetic, and each result is rounded once to fp32.
  */
 int dora_factored_norm(const void* W, const void* A, const void* B, int dtype,
                        int64_t d_out, int64_t d_in, int64_t r, float s,
@@ -131,7 +133,7 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
  * workspace is instead a 32 MiB array in the library's own device memory
  * (a file-scope __device__ array): every GPU that loads the library holds it
  * until the process exits.  With bf16 inputs 32 MiB covers d_out up to
- * 91 748 rows at r = 512 (150 901 at r = 384, 238 048 at r = 128; fp32 inputs
+ * 98 300 rows at r = 512 (150 901 at r = 384, 234 192 at r = 128; fp32 inputs
  * need less); a shape whose
  * dora_norm_workspace_size exceeds 32 MiB is refused with DORA_ERR_WORKSPACE
  * before anything is enqueued.
