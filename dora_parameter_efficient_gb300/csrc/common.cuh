@@ -36,45 +36,30 @@ __device__ __forceinline__ void kahan_add(float& sum, float& c, float x) {
 // every kernel launch of the library is counted here (dora_launch_count)
 void note_launches(int n);
 
-// ------------------------------------------------------------------ tcgen05 GEMM
-// D[128 x n_pad] = X[128-row tile x K] * Y[n_pad x K]^T in tensor memory, with
-// the epilogues of the factored norm.
+// ------------------------------------------------------------------ Gram G = A A^T
 constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;                 // bf16 elements per 128-byte smem row
-constexpr int kTcThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr uint32_t kTcXTileBytes = kTcBlockM * 128;
 constexpr int kTcMaxStages = 8;
 
-enum TcMode : int {
-  kTcSumSq = 1,   // per-row sum of squares of the X tiles, from shared memory
-  kTcDotB = 2,    // per-row dot of the accumulator row with the matching row of B
-  kTcStore = 4,   // store the accumulator tile, transposed, as an fp32 partial
-};
-
-struct TcParams {
-  int rows;              // valid rows of X
-  int n_pad;             // N: multiple of 16, <= 512
-  int y_box_rows;        // rows per Y TMA box (divides n_pad)
-  int k_tiles;           // K tiles in the whole K loop
-  int k_tiles_pass;      // K tiles per pass: tile kt >= k_tiles_pass reads Y1 at kt - k_tiles_pass
-  int stages;            // shared-memory pipeline depth
-  int mode;              // TcMode bits
-  int r;                 // valid accumulator columns (DotB, Store)
-  uint32_t tmem_cols;    // power of two >= max(32, n_pad)
-  const uint16_t* B;     // DotB: [rows x r] bf16
-  float* out_sumsq;      // [splits][rows]
-  float* out_dot;        // [splits][rows]
-  float* out_store;      // [splits][gridDim.x][128][n_pad] partial tiles
+struct GramParams {
+  int nb;                // 128-row blocks per side of G (upper triangle computed)
+  int bw;                // block width: 128, or the padded rank when nb == 1
+  int rp;                // r padded to 16: G, G_hi, G_lo are [rp x rp]
+  int k_tiles;           // 64-column tiles of d_in
+  int stages;
+  int cluster;           // CTAs per block (K split), one cluster per block
+  uint32_t tmem_cols;
+  float scale;           // G' = scale * G, split into G_hi + G_lo
+  uint16_t* G_hi;
+  uint16_t* G_lo;
   int* status;
   unsigned long long timeout_ns;
-  int inject_fault;      // test hook: the producer issues no loads
-  int gram_nb;           // > 0: Gram mode over the nb x nb grid of 128-blocks (upper triangle)
 };
 
-size_t tc_smem_bytes(int n_pad, int stages);
-int tc_pick_stages(int n_pad);
-cudaError_t launch_gemm_tc(const CUtensorMap& tx, const CUtensorMap& ty0, const CUtensorMap& ty1,
-                           const TcParams& p, int row_tiles, int splits, cudaStream_t stream);
+size_t gram_smem_bytes(int bw, int stages);
+cudaError_t launch_gram(const CUtensorMap& tAx, const CUtensorMap& tAy, const GramParams& p,
+                        cudaStream_t stream);
 
 // ------------------------------------------------------------------ CTA-pair main pass
 // D [256-row pair tile x n0+n1] = X * Y^T over the K tiles of one work item,
@@ -85,7 +70,8 @@ struct PairParams {
   int y_box_rows;        // rows per Y TMA box (divides n0/2 and n1/2)
   int kt_w;              // K tiles of (W, A)
   int kt_b;              // K tiles of (B, G'_hi), and again of (B, G'_lo)
-  int splits;            // K splits per pair tile
+  int splits;            // K segments per pair tile (<= 16)
+  int seg_k[17];         // segment s covers K tiles [seg_k[s], seg_k[s + 1]); non-increasing lengths
   int pair_tiles;        // ceil(d_out / 256)
   int stages;
   int r;
@@ -94,6 +80,7 @@ struct PairParams {
   const uint16_t* B;     // [rows x r] bf16
   float* out_sumsq;      // [splits][rows]
   float* out_dot;        // [splits][rows]
+  int* work_ctr;         // next unclaimed work item; zero at launch
   int* status;
   unsigned long long timeout_ns;
 };
@@ -116,9 +103,6 @@ cudaError_t launch_gemm_simt(const float* X, const float* Y, int rows, int ncols
 // ------------------------------------------------------------------ small kernels
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,
                              float* out, cudaStream_t stream);
-cudaError_t launch_gram_reduce(const float* parts, int splits, int nb, int bw, int n_pad,
-                               float* G, uint16_t* G_hi, uint16_t* G_lo, float scale,
-                               cudaStream_t stream);
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
                             int n_cross, const float* pba, int n_ba, float s, const void* m,
                             int is_bf16, float eps, float* wnorm, float* g,

@@ -21,7 +21,11 @@ namespace {
 
 constexpr int kMaxMainSplits = 16;
 static_assert(kMaxMainSplits <= kMaxFinalParts, "the fused finalize sums at most kMaxFinalParts splits");
-constexpr int kMaxGramSplits = 24;   // K splits of the Gram blocks (workspace sized for this)
+#ifndef DORA_GRAM_CLUSTER
+#define DORA_GRAM_CLUSTER 8
+#endif
+constexpr int kGramCluster = DORA_GRAM_CLUSTER;   // CTAs (K splits) per Gram block
+constexpr int kGramStages = 6;
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -90,13 +94,9 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
 }
 
 // Gram blocks: the upper triangle of the nb x nb grid of 128-row blocks of
-// G [rp x rp]; each block partial is [128 x bw] floats.
+// G [rp x rp], each block bw columns wide.
 int gram_nb(int rp) { return static_cast<int>((rp + 127) / 128); }
 int gram_bw(int rp) { return rp > 128 ? 128 : rp; }
-size_t gram_block_floats(int rp) {
-  const size_t nb = gram_nb(rp);
-  return nb * (nb + 1) / 2 * 128 * static_cast<size_t>(gram_bw(rp));
-}
 
 // ---------------------------------------------------------------- workspace plan
 struct Plan {
@@ -104,7 +104,7 @@ struct Plan {
   int rp = 0;               // r rounded up to 16 (the MMA N extent)
   int main_splits = 1;      // split-K of the main pass (tensor-core path)
   int gram_splits = 1;
-  size_t off_status = 0, zero_bytes = 0, off_G = 0, off_Ghi = 0, off_Glo = 0, off_Gpart = 0;
+  size_t off_status = 0, zero_bytes = 0, off_G = 0, off_Ghi = 0, off_Glo = 0;
   size_t off_pbase = 0, off_pcross = 0, off_pba = 0, total = 0;
   int cap_base = 0, cap_cross = 0, cap_ba = 0;
 };
@@ -147,8 +147,6 @@ Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
     off = align_up(off + rp2 * 2, 256);
     p.off_Glo = off;
     off = align_up(off + rp2 * 2, 256);
-    p.off_Gpart = off;
-    off = align_up(off + static_cast<size_t>(kMaxGramSplits) * gram_block_floats(p.rp) * 4, 256);
   }
   p.off_pbase = off;
   off = align_up(off + static_cast<size_t>(p.cap_base) * d_out * 4, 256);
@@ -191,6 +189,30 @@ int pick_pair_splits(int64_t pair_tiles, int64_t k_tiles, int clusters, int max_
     }
   }
   return best;
+}
+
+// K segments of each pair tile.  With enough tiles to go round, four
+// segments of relative lengths 4 : 3 : 2 : 1 (long work first, short work to
+// even out the finish); with few tiles, equal segments, as many as keep the
+// pairs busy.
+void plan_pair_segments(PairParams& pp, int clusters) {
+  const int ktot = pp.kt_w + 2 * pp.kt_b;
+  int nseg;
+  if (4 * static_cast<int64_t>(pp.pair_tiles) >= clusters && ktot >= 10) {
+    static const int w[4] = {4, 3, 2, 1};
+    nseg = 4;
+    int acc = 0;
+    pp.seg_k[0] = 0;
+    for (int i = 0; i < 4; ++i) {
+      acc += w[i];
+      pp.seg_k[i + 1] = static_cast<int>((static_cast<int64_t>(ktot) * acc + 5) / 10);
+    }
+  } else {
+    nseg = pick_pair_splits(pp.pair_tiles, ktot, clusters, kMaxMainSplits);
+    for (int i = 0; i <= nseg; ++i)
+      pp.seg_k[i] = static_cast<int>((static_cast<int64_t>(ktot) * i) / nseg);
+  }
+  pp.splits = nseg;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -249,7 +271,6 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   float* G = reinterpret_cast<float*>(ws + plan.off_G);
   uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + plan.off_Ghi);
   uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + plan.off_Glo);
-  float* Gpart = reinterpret_cast<float*>(ws + plan.off_Gpart);
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
   float* pba = reinterpret_cast<float*>(ws + plan.off_pba);
@@ -266,13 +287,11 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
     n_base = 1;
   } else if (bf16) {
-    // G = A A^T (split-K partials on the single-CTA tensor-core kernel), then
-    // G' = (s/2) G split into two bf16 terms, then the CTA-pair main pass with
-    // the BA-norm tiles folded into its K loop.
+    // G = A A^T with G' = (s/2) G split into two bf16 terms (one cluster of
+    // CTAs per upper-triangular 128 x 128 block, K split across the cluster),
+    // then the CTA-pair main pass with the BA-norm tiles folded into its K loop.
     const int rp = plan.rp;
     const int gnb = gram_nb(rp), gbw = gram_bw(rp);
-    int y_box1 = 128;                       // Gram kernel: Y box rows dividing the block width
-    while (gbw % y_box1) y_box1 >>= 1;
     const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
     const uint32_t tmem_cols = [&] {
       uint32_t c = 32;
@@ -283,40 +302,31 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
     const int n1 = rp - n0;
     const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
-    CUtensorMap mW, mA_x, mA_y1, mA_y2, mB_x, mGhi, mGlo;
+    CUtensorMap mW, mA_x, mA_yg, mA_y2, mB_x, mGhi, mGlo;
     if (!make_map_bf16(&mW, W, d_in, d_out, kTcBlockM) ||
         !make_map_bf16(&mA_x, A, d_in, r, kTcBlockM) ||
-        !make_map_bf16(&mA_y1, A, d_in, r, y_box1) ||
+        !make_map_bf16(&mA_yg, A, d_in, r, gbw) ||
         !make_map_bf16(&mA_y2, A, d_in, r, y_box2) ||
         !make_map_bf16(&mB_x, B, r, d_out, kTcBlockM) ||
         !make_map_bf16(&mGhi, Ghi, rp, rp, y_box2) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box2))
       return DORA_ERR_CUDA;
 
-    // G = A A^T: upper-triangular 128x128 blocks, K split so about one CTA
-    // per SM is busy; partial blocks are summed in split order afterwards.
-    TcParams pg{};
-    pg.rows = static_cast<int>(r);
-    pg.n_pad = gbw;
-    pg.y_box_rows = y_box1;
+    GramParams pg{};
+    pg.nb = gnb;
+    pg.bw = gbw;
+    pg.rp = rp;
     pg.k_tiles = k_tiles;
-    pg.k_tiles_pass = k_tiles;
-    pg.stages = tc_pick_stages(gbw);
-    pg.mode = kTcStore;
-    pg.r = static_cast<int>(r);
+    pg.stages = kGramStages;
+    // a power of two (the 128 block rows split evenly), at most one K tile per CTA
+    pg.cluster = kGramCluster;
+    while (pg.cluster > 1 && pg.cluster > k_tiles) pg.cluster >>= 1;
     pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
-    pg.out_store = Gpart;
+    pg.scale = 0.5f * s;
+    pg.G_hi = Ghi;
+    pg.G_lo = Glo;
     pg.status = status;
     pg.timeout_ns = kDefaultTimeoutNs;
-    pg.gram_nb = gnb;
-    const int gram_blocks = gnb * (gnb + 1) / 2;
-    int gram_splits = static_cast<int>(ceil_div(dev.sms, gram_blocks));
-    if (gram_splits > kMaxGramSplits) gram_splits = kMaxGramSplits;
-    if (gram_splits > k_tiles) gram_splits = k_tiles;
-    if (gram_splits < 1) gram_splits = 1;
-    DORA_TRY(launch_gemm_tc(mA_x, mA_y1, mA_y1, pg, gram_blocks, gram_splits, stream));
-    DORA_TRY(launch_gram_reduce(Gpart, gram_splits, gnb, gbw, rp, G, Ghi, Glo, 0.5f * s,
-                                stream));
-
+    DORA_TRY(launch_gram(mA_x, mA_yg, pg, stream));
 
     PairParams pp{};
     pp.rows = static_cast<int>(d_out);
@@ -329,14 +339,14 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     pp.stages = pair_pick_stages(rp);
     const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages));
     if (clusters_max <= 0) return DORA_ERR_CUDA;
-    pp.splits = pick_pair_splits(pp.pair_tiles, pp.kt_w + 2 * pp.kt_b, clusters_max,
-                                 kMaxMainSplits);
+    plan_pair_segments(pp, clusters_max);
     pp.r = static_cast<int>(r);
     pp.prefetch = 4;
     pp.tmem_cols = tmem_cols;
     pp.B = static_cast<const uint16_t*>(B);
     pp.out_sumsq = pbase;
     pp.out_dot = pcross;
+    pp.work_ctr = status + 32;          // inside the zeroed status block
     pp.status = status;
     pp.timeout_ns = kDefaultTimeoutNs;
     const int items = pp.pair_tiles * pp.splits;

@@ -35,9 +35,17 @@
 //   * at the end of an item two warps per TMEM lane quadrant read the halves
 //     of the D rows (tcgen05.ld), dot them with B and add the halves in a
 //     fixed order;
-//   * the grid is persistent: cluster c processes work items c, c + C, ...,
-//     an item being (256-row tile, K split); the TMA producer runs ahead into
-//     the next item while the epilogue drains the accumulator.
+//   * the grid is persistent and the work is handed out dynamically: the
+//     even CTA's TMA producer claims the next work item -- a (256-row tile,
+//     K split) pair -- from a global counter when it has issued the loads of
+//     the current one and publishes it to every role of both CTAs through a
+//     small ring in shared memory.  A pair that starts late (its SMs still
+//     busy with the Gram kernel, which this kernel may overlap) simply takes
+//     fewer items.  Items are ordered segment-major with the K segments
+//     shrinking along K, so long items go first, short ones fill in at the
+//     end, and the last segment -- the one with the G' tiles -- goes last;
+//   * the TMA producer runs ahead into the next item while the epilogue
+//     drains the accumulator.
 // Every wait is bounded by %globaltimer; on expiry the kernel records a
 // timeout in the status word, stops issuing, drains what it issued and exits.
 #include "common.cuh"
@@ -98,19 +106,40 @@ __device__ __forceinline__ uint4 ldg_keep_order(const uint16_t* p) {
   return v;
 }
 
+// Work item -> (pair tile, K segment, its K tile range).  Items are handed out
+// segment by segment and the segments shrink along K, so the long pieces of
+// work go first and the short ones fill in at the end (fewer idle pairs at
+// the finish); the last segment also holds the G' tiles.
 __device__ __forceinline__ void item_range(const PairParams& p, int item, int& tile, int& split,
                                            int& kb, int& ke) {
-  tile = item / p.splits;
-  split = item - tile * p.splits;
-  const int ktot = p.kt_w + 2 * p.kt_b;
-  kb = static_cast<int>((static_cast<long long>(ktot) * split) / p.splits);
-  ke = static_cast<int>((static_cast<long long>(ktot) * (split + 1)) / p.splits);
+  split = item / p.pair_tiles;
+  tile = item - split * p.pair_tiles;
+  kb = p.seg_k[split];
+  ke = p.seg_k[split + 1];
 }
 
 // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per tensor-memory lane quadrant)
 constexpr int kPairThreads = 320;
 constexpr int kPairEpiThreads = 256;
 constexpr int kPairEpiWarps = kPairEpiThreads / 32;
+// work-item ring: claimed by the even CTA's producer, read by the even CTA's
+// MMA thread, the odd CTA's producer and the epilogue warps of both CTAs
+constexpr uint32_t kItemRing = 4;
+constexpr uint32_t kItemReaders = 2 + 2 * kPairEpiWarps;
+
+// The n-th work item of this CTA pair (-1: no more work), as published in the
+// ring; the reader releases the slot on the even CTA's `item_empty`.
+__device__ __forceinline__ int read_item(uint32_t n, uint64_t* item_full, const volatile int* item_slot,
+                                         uint32_t item_empty0, uint64_t deadline, int* status) {
+  const uint32_t slot = n % kItemRing;
+  if (!mbar_wait_cluster(&item_full[slot], (n / kItemRing) & 1u, deadline)) {
+    atomicExch(status, kStatusTimeout);
+    return -1;
+  }
+  const int item = item_slot[slot];
+  mbar_arrive_cluster(item_empty0 + slot * 8u);
+  return item;
+}
 
 __global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tA,
@@ -129,13 +158,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   float* dot_half = reinterpret_cast<float*>(tmem_holder + 4);   // [2][128] second-half dots
+  uint64_t* item_full = reinterpret_cast<uint64_t*>(dot_half + 256);
+  uint64_t* item_empty = item_full + kItemRing;
+  volatile int* item_slot = reinterpret_cast<volatile int*>(item_empty + kItemRing);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs, 1: its peer
-  const int cid = static_cast<int>(cluster_id_x());
-  const int ncl = static_cast<int>(num_clusters_x());
   const int n_items = p.pair_tiles * p.splits;
+  const uint32_t item_empty0 = map_to_rank(smem_u32(item_empty), 0);
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -146,6 +177,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
     mbar_init(accum_full, 1);
     mbar_init(accum_empty, 16);     // 8 epilogue warps in each CTA of the pair
+    for (uint32_t i = 0; i < kItemRing; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], kItemReaders);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -181,7 +216,29 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t s = 0, phase = 0, it = 0;
       bool stop = false;
       bool g_ready = false;      // G'_hi / G'_lo written by the preceding kernel
-      for (int item = cid; item < n_items && !stop; item += ncl) {
+      const uint32_t slot1 = map_to_rank(smem_u32(const_cast<int*>(item_slot)), 1);
+      const uint32_t full1 = map_to_rank(smem_u32(item_full), 1);
+      int claimed = rank == 0 ? atomicAdd(p.work_ctr, 1) : 0;
+      for (uint32_t n = 0; !stop; ++n) {
+        int item;
+        if (rank == 0) {
+          // publish the claimed item (or the end) to both CTAs
+          const uint32_t slot = n % kItemRing;
+          if (n >= kItemRing &&
+              !mbar_wait_cluster(&item_empty[slot], (n / kItemRing - 1) & 1u, deadline)) {
+            atomicExch(p.status, kStatusTimeout);
+            *abort_flag = 1;
+            break;
+          }
+          item = claimed < n_items ? claimed : -1;
+          item_slot[slot] = item;
+          st_cluster_u32(slot1 + slot * 4u, static_cast<uint32_t>(item));
+          mbar_arrive(&item_full[slot]);
+          mbar_arrive_cluster(full1 + slot * 8u);
+        } else {
+          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
+        }
+        if (item < 0) break;
         int tile, split, kb, ke;
         item_range(p, item, tile, split, kb, ke);
         const int row0 = tile * 256 + static_cast<int>(rank) * 128;
@@ -231,6 +288,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             phase ^= 1u;
           }
         }
+        if (rank == 0) claimed = atomicAdd(p.work_ctr, 1);
       }
       // The even CTA's `full` barriers count the loads of both CTAs: once the
       // last use of every stage has completed, no copy is still in flight.
@@ -259,7 +317,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       uint32_t s = 0, phase = 0;
       int icount = 0;
       bool stop = false;
-      for (int item = cid; item < n_items && !stop; item += ncl, ++icount) {
+      for (uint32_t n = 0; !stop; ++n, ++icount) {
+        const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
+        if (item < 0) break;
         int tile, split, kb, ke;
         item_range(p, item, tile, split, kb, ke);
         if (icount > 0 && !mbar_wait(accum_empty, (icount - 1) & 1, deadline)) {
@@ -325,7 +385,24 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint32_t s = 0, phase = 0;          // stage ring position (the producer's sequence)
     bool alive = true;                  // false once a wait has timed out
     int icount = 0;
-    for (int item = cid; item < n_items; item += ncl, ++icount) {
+    for (uint32_t n = 0;; ++n, ++icount) {
+      int item = -1;
+      if (alive && lane == 0) item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
+      item = __shfl_sync(0xFFFFFFFFu, item, 0);
+      {
+        // the 8 warps read the same item sequence; decide together anyway, as
+        // they meet at named barriers (a timed-out read ends all of them)
+        uint32_t all_ok;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ge.s32 p, %1, 0;\n\t"
+            "bar.red.and.pred q, 1, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(all_ok)
+            : "r"(item), "n"(kPairEpiThreads)
+            : "memory");
+        if (!all_ok) break;
+      }
       int tile, split, kb, ke;
       item_range(p, item, tile, split, kb, ke);
       const int rowbase = tile * 256 + static_cast<int>(rank) * 128 + q * 32;
@@ -480,7 +557,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 size_t pair_smem_bytes(int n_pad, int stages) {
   const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
-  return 1024 + stage * stages + (3 * stages + 3) * 8 + 16 + 2 * 128 * 4;
+  return 1024 + stage * stages + (3 * stages + 2) * 8 + 16 + 2 * 128 * 4 +
+         2 * kItemRing * 8 + kItemRing * 4;
 }
 
 int pair_pick_stages(int n_pad) {

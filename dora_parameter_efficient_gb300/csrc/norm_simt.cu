@@ -1,6 +1,6 @@
 // norm_simt.cu -- fp32-input pieces of the factored norm on CUDA cores, plus
 // the small kernels shared by both input types (row sum of squares for the
-// s = 0 branch, the Gram-partial reduction, and the stand-alone finalize).
+// s = 0 branch and the finalize).
 //
 // The fp32 path computes the same three terms as the bf16 tensor-core path
 // ("Scaling DoRA", Chinese write-up section 1.2.1; Algorithm 1, section 5.1)
@@ -168,64 +168,6 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) out[row] = acc;
 }
 
-// G = sum over K splits of the partial 128x128 Gram blocks (fixed order); the
-// upper-triangular block (bi, bj) is also written to (bj, bi).  Alongside, the
-// split of scale * G into two bf16 terms G_hi + G_lo for the tensor-core
-// BA-norm tiles (about 16 significant bits of G survive the two terms).
-constexpr int kMaxGramParts = 64;
-
-__global__ void k_gram_reduce(const float* __restrict__ parts, int splits, int nb, int bw,
-                              int n_pad, float* __restrict__ G, uint16_t* __restrict__ G_hi,
-                              uint16_t* __restrict__ G_lo, float scale) {
-  // the main pass (launched behind this kernel with programmatic stream
-  // serialization) may start launching now; it waits for this grid to
-  // finish before it reads G'
-  griddep_launch_dependents();
-  // launched as a programmatic dependent of the Gram kernel: its partials
-  // are read only once it has finished
-  griddep_wait();
-  // partial blocks are [128 rows x bw columns]; bw = 128, or n_pad when nb == 1
-  const int nblocks = nb * (nb + 1) / 2;
-  const int64_t per_block = static_cast<int64_t>(128) * bw;
-  const int64_t n = nblocks * per_block;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int b = static_cast<int>(idx / per_block);
-    const int i = static_cast<int>((idx / bw) % 128);
-    const int j = static_cast<int>(idx % bw);
-    int bi = 0, rem = b;
-    while (rem >= nb - bi) {
-      rem -= nb - bi;
-      ++bi;
-    }
-    const int bj = bi + rem;
-    const int gi = bi * 128 + i, gj = bj * 128 + j;
-    if (gi >= n_pad || gj >= n_pad) continue;
-    // loads issued eight at a time ahead of the (fixed-order) sum
-    float acc = 0.f;
-    for (int s0 = 0; s0 < splits; s0 += 8) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = s0 + u < splits ? __ldg(parts + (s0 + u) * n + idx) : 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) acc = __fadd_rn(acc, v[u]);
-    }
-    const float sc = __fmul_rn(scale, acc);
-    const uint16_t hi = f32_to_bf16_rn(sc);
-    const uint16_t lo = f32_to_bf16_rn(__fsub_rn(sc, bf16_to_f32(hi)));
-    const int64_t o = static_cast<int64_t>(gi) * n_pad + gj;
-    G[o] = acc;
-    G_hi[o] = hi;
-    G_lo[o] = lo;
-    if (bi != bj) {
-      const int64_t t = static_cast<int64_t>(gj) * n_pad + gi;
-      G[t] = acc;
-      G_hi[t] = hi;
-      G_lo[t] = lo;
-    }
-  }
-}
-
 // sum of n fp32 partials in split order, as a double-float
 __device__ __forceinline__ df sum_parts(const float* __restrict__ p, int n, int64_t stride,
                                         int64_t j) {
@@ -272,28 +214,6 @@ cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t c
   if (is_bf16) k_row_sumsq<true><<<blocks, 256, 0, stream>>>(X, rows, cols, out);
   else k_row_sumsq<false><<<blocks, 256, 0, stream>>>(X, rows, cols, out);
   note_launches(1);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gram_reduce(const float* parts, int splits, int nb, int bw, int n_pad,
-                               float* G, uint16_t* G_hi, uint16_t* G_lo, float scale,
-                               cudaStream_t stream) {
-  if (splits > kMaxGramParts) return cudaErrorInvalidValue;
-  const int64_t n = static_cast<int64_t>(nb) * (nb + 1) / 2 * 128 * bw;
-  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks, 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gram_reduce, parts, splits, nb, bw, n_pad, G,
-                                           G_hi, G_lo, scale);
-  note_launches(1);
-  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
