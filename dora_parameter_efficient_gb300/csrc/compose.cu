@@ -13,13 +13,26 @@
 //
 // Layout: base/lora/out are [T x d_out] row-major.  Rows whose byte length is
 // a multiple of 16 with 16-byte aligned pointers stream as 16-byte vectors
-// (8 bf16 or 4 fp32 per load); anything else takes the element-wise loop of
-// the same kernel.  Grid-stride, grid sized to the SM count.
+// (8 bf16 or 4 fp32 per load).  When a row holds a multiple of 256 vectors,
+// each thread keeps one column vector for all its rows: its g values (and
+// g - 1) stay in registers and no index arithmetic is left per element, so
+// the kernel is bound by HBM, not by instruction issue.  Other vector shapes
+// take a grid-stride loop, and anything unaligned the element-wise loop.
+// Grids are sized to a multiple of the SM count.
 #include "common.cuh"
 
 namespace dora {
 
 namespace {
+
+// (g - 1) is passed in: exact for g in [0.5, 2] (Sterbenz), one rounding otherwise
+__device__ __forceinline__ float compose1m(float b, float l, float g, float gm1, float s) {
+  const float sl = __fmul_rn(s, l);
+  const float sl_err = fmaf(s, l, -sl);          // s*l = sl + sl_err exactly
+  const float p = __fmul_rn(gm1, b);
+  const float p_err = fmaf(gm1, b, -p);          // (g-1)*b = p + p_err exactly
+  return __fadd_rn(fmaf(g, sl, p), fmaf(g, sl_err, p_err));
+}
 
 __device__ __forceinline__ float compose1(float b, float l, float g, float s) {
   const float gm1 = __fsub_rn(g, 1.0f);          // exact for g in [0.5, 2] (Sterbenz)
@@ -31,6 +44,74 @@ __device__ __forceinline__ float compose1(float b, float l, float g, float s) {
 }
 
 constexpr int kUnroll = 4;
+constexpr int kColThreads = 256;     // column vectors per block of the fixed-column kernel
+constexpr int kRowUnroll = 4;
+
+// two floats -> packed bf16x2 (lo in the low half), each rounded to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Fixed-column stream: block (x, y) owns column vectors [x * 256, x * 256 + 256)
+// and rows y, y + gridDim.y, ...; requires d_out / EPV to be a multiple of 256.
+template <bool BF16>
+__global__ void __launch_bounds__(kColThreads, 4)
+    k_compose_cols(const uint4* __restrict__ base, const uint4* __restrict__ lora,
+                   const float* __restrict__ g, float s, int64_t T, int64_t dv,
+                   uint4* __restrict__ out) {
+  constexpr int EPV = BF16 ? 8 : 4;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * kColThreads + threadIdx.x;
+  float gv[EPV], gm[EPV];
+#pragma unroll
+  for (int q = 0; q < EPV / 4; ++q) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(g + c * EPV) + q);
+    gv[4 * q] = t.x;
+    gv[4 * q + 1] = t.y;
+    gv[4 * q + 2] = t.z;
+    gv[4 * q + 3] = t.w;
+  }
+#pragma unroll
+  for (int e = 0; e < EPV; ++e) gm[e] = __fsub_rn(gv[e], 1.0f);
+  const int64_t rstep = gridDim.y;
+  for (int64_t r0 = blockIdx.y; r0 < T; r0 += rstep * kRowUnroll) {
+    uint4 bv[kRowUnroll], lv[kRowUnroll];
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u) {
+      const int64_t r = r0 + u * rstep;
+      if (r < T) {
+        bv[u] = __ldcs(base + r * dv + c);
+        lv[u] = __ldcs(lora + r * dv + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u) {
+      const int64_t r = r0 + u * rstep;
+      if (r >= T) continue;
+      uint4 o;
+      if (BF16) {
+        const uint32_t bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
+        const uint32_t lw[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = compose1m(bf16_lo(bw[e]), bf16_lo(lw[e]), gv[2 * e], gm[2 * e], s);
+          const float hi =
+              compose1m(bf16_hi(bw[e]), bf16_hi(lw[e]), gv[2 * e + 1], gm[2 * e + 1], s);
+          ow[e] = pack_bf16x2_rn(lo, hi);
+        }
+        o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      } else {
+        o.x = __float_as_uint(compose1m(__uint_as_float(bv[u].x), __uint_as_float(lv[u].x), gv[0], gm[0], s));
+        o.y = __float_as_uint(compose1m(__uint_as_float(bv[u].y), __uint_as_float(lv[u].y), gv[1], gm[1], s));
+        o.z = __float_as_uint(compose1m(__uint_as_float(bv[u].z), __uint_as_float(lv[u].z), gv[2], gm[2], s));
+        o.w = __float_as_uint(compose1m(__uint_as_float(bv[u].w), __uint_as_float(lv[u].w), gv[3], gm[3], s));
+      }
+      __stcs(out + r * dv + c, o);
+    }
+  }
+}
 
 template <bool BF16>
 __global__ void __launch_bounds__(256)
@@ -116,6 +197,27 @@ cudaError_t launch_compose(const void* base, const void* lora, const float* g, f
   const auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const int vec_ok = (d_out % epv == 0) && aligned(base) && aligned(lora) && aligned(out) &&
                      aligned(g);
+  const int64_t dv = d_out / epv;
+  if (vec_ok && dv % kColThreads == 0) {
+    // fixed-column kernel: one wave of 4 blocks of 256 threads per SM
+    const int64_t xblocks = dv / kColThreads;
+    const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 4;
+    int64_t yblocks = (target + xblocks - 1) / xblocks;
+    if (yblocks > T) yblocks = T;
+    if (yblocks > 65535) yblocks = 65535;
+    if (yblocks < 1) yblocks = 1;
+    const dim3 grid(static_cast<unsigned>(xblocks), static_cast<unsigned>(yblocks));
+    if (is_bf16)
+      k_compose_cols<true><<<grid, kColThreads, 0, stream>>>(
+          static_cast<const uint4*>(base), static_cast<const uint4*>(lora), g, s, T, dv,
+          static_cast<uint4*>(out));
+    else
+      k_compose_cols<false><<<grid, kColThreads, 0, stream>>>(
+          static_cast<const uint4*>(base), static_cast<const uint4*>(lora), g, s, T, dv,
+          static_cast<uint4*>(out));
+    note_launches(1);
+    return cudaGetLastError();
+  }
   const int64_t work = vec_ok ? (n / epv + kUnroll - 1) / kUnroll : n;
   int64_t blocks = (work + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 8;
