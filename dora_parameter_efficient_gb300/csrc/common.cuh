@@ -63,7 +63,9 @@ cudaError_t launch_gram(const CUtensorMap& tAx, const CUtensorMap& tAy, const Gr
 
 // ------------------------------------------------------------------ CTA-pair main pass
 // D [256-row pair tile x n0+n1] = X * Y^T over the K tiles of one work item,
-// M = 256 per CTA pair (tcgen05 cta_group::2), persistent over items.
+// M = 256 per CTA pair (tcgen05 cta_group::2), persistent over items; the
+// last K segment of each 128-row group to finish assembles wnorm and g for
+// its rows.
 struct PairParams {
   int rows;              // d_out
   int n0, n1;            // N of the first / second MMA (n1 = 0 when r <= 256)
@@ -75,11 +77,16 @@ struct PairParams {
   int pair_tiles;        // ceil(d_out / 256)
   int stages;
   int r;
-  int prefetch;          // W tiles pulled into L2 this many tiles ahead
   uint32_t tmem_cols;
+  // epilogue and the fused finalize
   const uint16_t* B;     // [rows x r] bf16
+  const uint16_t* m;     // [rows] bf16
+  float two_s, s_sq, eps;
   float* out_sumsq;      // [splits][rows]
   float* out_dot;        // [splits][rows]
+  int* tile_done;        // [pair_tiles][2] segments finished per 128-row group (zero at launch)
+  float* wnorm;          // [rows]
+  float* g;              // [rows]
   int* work_ctr;         // next unclaimed work item; zero at launch
   int* status;
   unsigned long long timeout_ns;

@@ -20,12 +20,12 @@ void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::
 namespace {
 
 constexpr int kMaxMainSplits = 16;
-static_assert(kMaxMainSplits <= kMaxFinalParts, "the fused finalize sums at most kMaxFinalParts splits");
 #ifndef DORA_GRAM_CLUSTER
 #define DORA_GRAM_CLUSTER 8
 #endif
 constexpr int kGramCluster = DORA_GRAM_CLUSTER;   // CTAs (K splits) per Gram block
 constexpr int kGramStages = 6;
+static_assert(kMaxMainSplits <= kMaxFinalParts, "the fused finalize sums at most kMaxFinalParts splits");
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -98,6 +98,11 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
 int gram_nb(int rp) { return static_cast<int>((rp + 127) / 128); }
 int gram_bw(int rp) { return rp > 128 ? 128 : rp; }
 
+// Control block at the start of the workspace, zeroed by every call (int
+// words): [0] device status, [32] work counter of the main pass,
+// [64, 64 + 2 * pair tiles) K segments finished per 128-row group.
+constexpr int kCtlWork = 32, kCtlTileDone = 64;
+
 // ---------------------------------------------------------------- workspace plan
 struct Plan {
   bool bf16 = true;
@@ -137,16 +142,18 @@ Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
   p.cap_ba = 2 > simt_cols ? 2 : simt_cols;
   size_t off = 0;
   p.off_status = off;
-  off += 256;
+  const int64_t pair_tiles = ceil_div(d_out, 2 * kTcBlockM);
+  off = align_up((kCtlTileDone + 2 * static_cast<size_t>(pair_tiles)) * 4, 256);
   p.zero_bytes = off;
   const size_t rp2 = static_cast<size_t>(p.rp) * p.rp;
-  p.off_G = off;
-  off = align_up(off + rp2 * 4, 256);
   if (p.bf16) {
     p.off_Ghi = off;
     off = align_up(off + rp2 * 2, 256);
     p.off_Glo = off;
     off = align_up(off + rp2 * 2, 256);
+  } else {
+    p.off_G = off;
+    off = align_up(off + rp2 * 4, 256);
   }
   p.off_pbase = off;
   off = align_up(off + static_cast<size_t>(p.cap_base) * d_out * 4, 256);
@@ -289,7 +296,9 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   } else if (bf16) {
     // G = A A^T with G' = (s/2) G split into two bf16 terms (one cluster of
     // CTAs per upper-triangular 128 x 128 block, K split across the cluster),
-    // then the CTA-pair main pass with the BA-norm tiles folded into its K loop.
+    // then the CTA-pair main pass with the BA-norm tiles folded into its K
+    // loop, which also finalizes every 128-row group as its last K segment
+    // lands.
     const int rp = plan.rp;
     const int gnb = gram_nb(rp), gbw = gram_bw(rp);
     const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
@@ -341,12 +350,20 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (clusters_max <= 0) return DORA_ERR_CUDA;
     plan_pair_segments(pp, clusters_max);
     pp.r = static_cast<int>(r);
-    pp.prefetch = 4;
     pp.tmem_cols = tmem_cols;
     pp.B = static_cast<const uint16_t*>(B);
+    pp.m = static_cast<const uint16_t*>(m);
+    // the sum over splits of rowsum(B o D) is cross + (s/2) ba, so the
+    // finalize's 2s * cross term carries the BA-norm term too
+    pp.two_s = 2.f * s;
+    pp.s_sq = s * s;
+    pp.eps = eps;
     pp.out_sumsq = pbase;
     pp.out_dot = pcross;
-    pp.work_ctr = status + 32;          // inside the zeroed status block
+    pp.tile_done = status + kCtlTileDone;
+    pp.wnorm = wnorm;
+    pp.g = g;
+    pp.work_ctr = status + kCtlWork;
     pp.status = status;
     pp.timeout_ns = kDefaultTimeoutNs;
     const int items = pp.pair_tiles * pp.splits;
@@ -354,10 +371,7 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
     DORA_TRY(launch_gemm_pair(mW, mA_y2, mB_x, mGhi, mGlo, pp, clusters, stream));
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
-    // sum over splits of rowsum(B o D) = cross + (s/2) ba: the finalize's
-    // 2s * cross term then carries the BA-norm term too
-    n_base = n_cross = pp.splits;
-    n_ba = 0;
+    return DORA_OK;
   } else {
     // fp32 inputs: CUDA-core path
     const float* Wf = static_cast<const float*>(W);

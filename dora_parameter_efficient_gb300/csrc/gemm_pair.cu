@@ -12,8 +12,9 @@
 // G'_hi + G'_lo = (s/2) G (two bf16 terms, computed beforehand).  Because the
 // epilogue is linear in D, summing dot over the splits gives
 // cross + (s/2) ba, and 2s (cross + (s/2) ba) = 2s cross + s^2 ba is exactly
-// what the norm needs; the finalize kernel, launched behind this one as a
-// programmatic dependent, adds the base term.
+// what the norm needs.  The last split of each 128-row group to finish sums
+// the partials of every split in split order and assembles wnorm and g for
+// those rows (the finalize of finalize.cuh): no separate kernel.
 //
 // Tiling for sm_103a:
 //   * a cluster of 2 CTAs on 2 SMs forms one tcgen05 "CTA pair": the even CTA
@@ -45,10 +46,13 @@
 //     shrinking along K, so long items go first, short ones fill in at the
 //     end, and the last segment -- the one with the G' tiles -- goes last;
 //   * the TMA producer runs ahead into the next item while the epilogue
-//     drains the accumulator.
+//     drains the accumulator;
+//   * W tiles are not prefetched into L2 ahead of their loads: with every
+//     SM streaming W, extra prefetch requests only added traffic.
 // Every wait is bounded by %globaltimer; on expiry the kernel records a
 // timeout in the status word, stops issuing, drains what it issued and exits.
 #include "common.cuh"
+#include "finalize.cuh"
 #include "ptx.cuh"
 
 namespace dora {
@@ -118,6 +122,13 @@ __device__ __forceinline__ void item_range(const PairParams& p, int item, int& t
   ke = p.seg_k[split + 1];
 }
 
+// global fp32 load that bypasses L1 (data written by other CTAs of this grid)
+__device__ __forceinline__ float ld_cg_f(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per tensor-memory lane quadrant)
 constexpr int kPairThreads = 320;
 constexpr int kPairEpiThreads = 256;
@@ -161,6 +172,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint64_t* item_full = reinterpret_cast<uint64_t*>(dot_half + 256);
   uint64_t* item_empty = item_full + kItemRing;
   volatile int* item_slot = reinterpret_cast<volatile int*>(item_empty + kItemRing);
+  volatile int* last_flag = item_slot + kItemRing;   // this CTA finished the last segment of its rows
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -184,9 +196,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // the finalize kernel behind this one may start launching (it waits for
-  // this grid to finish before it reads anything)
-  griddep_launch_dependents();
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tW);
     tma_prefetch_desc(&tA);
@@ -256,9 +265,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           int kx;
           if (kt < p.kt_w) {
             xm = &tW; ym = &tA; kx = kt * kTcBlockK;
-            // pull a later W tile of this item into L2 while this one loads
-            const int kpf = kt + p.prefetch;
-            if (kpf < ke && kpf < p.kt_w) tma_prefetch_l2_2d(&tW, kpf * kTcBlockK, row0);
           } else {
             // a G' tile (an item may start in either half of the G' range)
             if (!g_ready) {
@@ -540,6 +546,32 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (h == 1) dh[trow] = acc;
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (h == 0 && valid) p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc + dh[trow];
+      // the last segment of this 128-row group to finish assembles wnorm and
+      // g for its rows from the partials of every segment, in segment order
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
+      if (warp == 2 && lane == 0) {
+        const int prev = atomicAdd(p.tile_done + tile * 2 + static_cast<int>(rank), 1);
+        *last_flag = prev == p.splits - 1 ? 1 : 0;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
+      if (*last_flag && h == 0 && valid) {
+        __threadfence();
+        // segment partials added in segment order, carried as double-floats
+        df base{0.f, 0.f}, cross{0.f, 0.f};
+#pragma unroll 1
+        for (int i = 0; i < p.splits; ++i) {
+          float e;
+          two_sum(base.hi, ld_cg_f(p.out_sumsq + static_cast<size_t>(i) * p.rows + grow), base.hi, e);
+          base.lo = __fadd_rn(base.lo, e);
+          two_sum(cross.hi, ld_cg_f(p.out_dot + static_cast<size_t>(i) * p.rows + grow), cross.hi, e);
+          cross.lo = __fadd_rn(cross.lo, e);
+        }
+        float wn, gv;
+        finalize_row(base, cross, nullptr, p.two_s, p.s_sq, bf16_to_f32(p.m[grow]), p.eps, wn, gv);
+        p.wnorm[grow] = wn;
+        p.g[grow] = gv;
+      }
     }
   }
 
@@ -558,7 +590,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 size_t pair_smem_bytes(int n_pad, int stages) {
   const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
   return 1024 + stage * stages + (3 * stages + 2) * 8 + 16 + 2 * 128 * 4 +
-         2 * kItemRing * 8 + kItemRing * 4;
+         2 * kItemRing * 8 + kItemRing * 4 + 4;
 }
 
 int pair_pick_stages(int n_pad) {
@@ -611,7 +643,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // may start while the Gram reduction still runs: only the TMA producer's
+  // may start while the Gram kernel still runs: only the TMA producer's
   // G' loads depend on it, and they wait for it (griddep_wait)
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;

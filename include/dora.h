@@ -68,12 +68,12 @@ typedef enum dora_dtype {
 
 /*
  * Bytes of device workspace dora_factored_norm needs for this shape.
- * The workspace holds a small control block (the device status word and the
- * main pass's work counter, zeroed by every call), the Gram matrix G = A A^T
- * (fp32, for fp32 inputs) and its scaled bf16 split G'_hi + G'_lo (for bf16
- * inputs), and per-segment partial sums of the norm terms.  It does not
- * depend on d_in: about 2.4 MB at d_out = 8192, r = 384 (bf16) and 2.4 MB at
- * d_out = 8192, r = 512 (fp32).
+ * The workspace holds a small control block (the device status word, the
+ * main pass's work counter and per-row-group completion counters, zeroed by
+ * every call), the Gram matrix G = A A^T (fp32, for fp32 inputs) or its
+ * scaled bf16 split G'_hi + G'_lo (for bf16 inputs), and per-segment partial
+ * sums of the norm terms.  It does not depend on d_in: about 1.8 MB at
+ * d_out = 8192, r = 384 (bf16) and 2.4 MB at d_out = 8192, r = 512 (fp32).
  * Returns 0 for an invalid shape (negative sizes, bad dtype, r > DORA_MAX_RANK).
  */
 size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtype);
@@ -134,9 +134,8 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
  * Arguments, results and requirements are those of dora_factored_norm.  The
  * workspace is instead a 32 MiB array in the library's own device memory
  * (a file-scope __device__ array): every GPU that loads the library holds it
- * until the process exits.  With bf16 inputs 32 MiB covers d_out up to
- * 196 604 rows at r = 512 (212 988 at r = 384, 245 756 at r = 128; fp32
- * inputs need less); a shape whose
+ * until the process exits.  32 MiB covers d_out up to 203 120 rows at
+ * r = 512 (216 824 at r = 384, 246 180 at r = 128); a shape whose
  * dora_norm_workspace_size exceeds 32 MiB is refused with DORA_ERR_WORKSPACE
  * before anything is enqueued.
  *   - The first call on each device looks up the array's device address

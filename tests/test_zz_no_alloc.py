@@ -35,7 +35,7 @@ def test_oversized_shape_is_refused_before_any_launch():
     """A shape whose workspace exceeds the 32 MiB array is refused on the host."""
     lib = _lib_loaded()
     P = 1 << 20        # never dereferenced: the call returns before touching the device
-    d_out, d_in, r = 200_000, 4096, 512
+    d_out, d_in, r = 300_000, 4096, 512
     assert lib.dora_norm_workspace_size(d_out, d_in, r, _lib.DORA_BF16) > (32 << 20)
     st = lib.dora_factored_norm_noalloc(P, 2 * P, 3 * P, _lib.DORA_BF16, d_out, d_in, r, 1.0,
                                         4 * P, 1e-6, 5 * P, 6 * P, None)
