@@ -155,6 +155,57 @@ def naive_compose_f32(base32: np.ndarray, lora32: np.ndarray, g32: np.ndarray,
     return t - base32
 
 
+# ---------------------------------------------------------------- training path of the compose
+# The Chinese write-up (sections 2.2, 4.2 and 5.2) describes the training
+# tier of the compose: the forward also keeps `inner`, one activation-sized
+# tensor, for the magnitude gradient; the backward is a dual-output kernel
+# (the gradients of the base and adapter branches) and dmag is a separate,
+# deterministic column reduction, skipped when the magnitude is frozen.  The
+# norm is a detached constant in the backward (section 1.2.2, following the
+# DoRA paper), so g = m / max(wnorm, eps) depends on m alone.  The functions
+# below are the plain derivatives of compose() under that reading.
+def compose_inner(base: np.ndarray, lora: np.ndarray, s: float) -> np.ndarray:
+    """inner_ij = base_ij + s * lora_ij, float64: d out_ij / d g_j of
+    out = (g - 1) * base + g * (s * lora)."""
+    return np.asarray(base, dtype=np.float64) + float(s) * np.asarray(lora, dtype=np.float64)
+
+
+def compose_inner_stored(base, lora, s: float, dtype: str) -> np.ndarray:
+    """Stored base/lora -> inner rounded once to the stored dtype."""
+    return round_to(compose_inner(decode(base, dtype), decode(lora, dtype), s), dtype)
+
+
+def compose_backward(d_out: np.ndarray, g: np.ndarray, s: float):
+    """Gradients of out = (g - 1) * base + g * (s * lora) with respect to the
+    two activations, float64: d_base = (g - 1) * d_out, d_lora = g * s * d_out
+    (g broadcast over the T rows)."""
+    d_out = np.asarray(d_out, dtype=np.float64)
+    g = np.asarray(g, dtype=np.float64)[None, :]
+    return (g - 1.0) * d_out, g * float(s) * d_out
+
+
+def compose_backward_stored(d_out, g, s: float, dtype: str):
+    """Stored d_out + float32 g -> (d_base, d_lora), each rounded once to dtype."""
+    d_base, d_lora = compose_backward(decode(d_out, dtype), np.asarray(g, dtype=np.float32), s)
+    return round_to(d_base, dtype), round_to(d_lora, dtype)
+
+
+def magnitude_grad(d_out: np.ndarray, inner: np.ndarray, wnorm: np.ndarray,
+                   eps: float) -> np.ndarray:
+    """dL/dm_j = sum_t d_out_tj * inner_tj / max(wnorm_j, eps), float64 [d_out]
+    (the chain rule through g_j = m_j / max(wnorm_j, eps) with wnorm constant)."""
+    d_out = np.asarray(d_out, dtype=np.float64)
+    inner = np.asarray(inner, dtype=np.float64)
+    col = np.sum(d_out * inner, axis=0)
+    return col / np.maximum(np.asarray(wnorm, dtype=np.float64), float(eps))
+
+
+def magnitude_grad_stored(d_out, inner, wnorm, eps: float, dtype: str) -> np.ndarray:
+    """Stored d_out / inner + float32 wnorm -> dm in float64."""
+    return magnitude_grad(decode(d_out, dtype), decode(inner, dtype),
+                          np.asarray(wnorm, dtype=np.float32), float(np.float32(eps)))
+
+
 # ---------------------------------------------------------------- memory facts
 def dense_ba_bytes(d_out: int, d_in: int, elem_bytes: int) -> int:
     """Bytes of the dense [d_out x d_in] product B*A that the factored norm
