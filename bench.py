@@ -381,6 +381,60 @@ def run_ours(args):
                         "peak_source": f"{peak_src} HBM copy", "bytes_per_launch": cbytes,
                         "traffic": recorded_traffic(comp_src, "compose_2048x8192_bf16.md")}
 
+    # ---- training path of the compose (saved inner, dual-output backward,
+    # magnitude gradient) on the same activations, timed like the step
+    grad_x = gen.grad_inputs(cfg, seed=rank)
+    d_outs = [to_dev(grad_x)] + [to_dev(grad_x).clone() for _ in range(N_SETS - 1)]
+    inners = [torch.empty_like(outs[0]) for _ in range(N_SETS)]
+    d_bases = [torch.empty_like(outs[0]) for _ in range(N_SETS)]
+    d_loras = [torch.empty_like(outs[0]) for _ in range(N_SETS)]
+    dmags = [torch.empty(d_out, dtype=torch.float32, device=dev) for _ in range(N_SETS)]
+    bws = torch.empty(api.compose_backward_workspace_size(T, d_out), dtype=torch.uint8, device=dev)
+
+    def train_fwd(k):
+        api.dora_compose_train(sets[k]["base"], sets[k]["lora"], gg[k], cfg.s, out=outs[k],
+                               inner=inners[k])
+
+    def train_bwd(k):
+        api.dora_compose_backward(d_outs[k], gg[k], cfg.s, inner=inners[k], wnorm=wn[k],
+                                  eps=cfg.eps, d_base=d_bases[k], d_lora=d_loras[k],
+                                  dmag=dmags[k], workspace=bws)
+
+    train_steps = max(3, min(args.steps, 500))
+    for i in range(max(3, args.warmup)):
+        train_fwd(i % N_SETS)
+        train_bwd(i % N_SETS)
+    tevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(train_steps)]
+    for e in tevs:
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for i in range(train_steps):
+        e = tevs[i]
+        e[0].record(stream)
+        train_fwd(i % N_SETS)
+        e[1].record(stream)
+        train_bwd(i % N_SETS)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    tf_ms = max_over_ranks(mean(e[0].elapsed_time(e[1]) for e in tevs), world, dev)
+    tb_ms = max_over_ranks(mean(e[1].elapsed_time(e[2]) for e in tevs), world, dev)
+    tf_bytes = configs.compose_train_bytes(T, d_out, cfg.dtype)
+    tb_bytes = configs.compose_backward_bytes(T, d_out, cfg.dtype, dmag=True)
+    compose_training = {
+        "forward": {"kernel": "k_train_fwd_cols<bf16> (out and inner = base + s lora)",
+                    "ms": tf_ms, "GB/s": tf_bytes / (tf_ms * 1e-3) / 1e9,
+                    "bytes_per_launch": tf_bytes,
+                    "frac_of_measured_hbm": tf_bytes / (tf_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "backward": {"kernel": "k_train_bwd_cols<bf16, dmag> + k_train_dm_finish "
+                               "(d_base, d_lora, deterministic dmag column sums)",
+                     "ms": tb_ms, "GB/s": tb_bytes / (tb_ms * 1e-3) / 1e9,
+                     "bytes_per_call": tb_bytes,
+                     "frac_of_measured_hbm": tb_bytes / (tb_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "timing": f"CUDA events around each call, mean over {train_steps} steps, "
+                  f"{N_SETS} rotating input sets",
+    }
+
     # ---- end to end through the public API, from pinned host buffers
     e2e_steps = max(3, min(args.steps, 20))
     host = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -474,6 +528,7 @@ def run_ours(args):
                         "frac_of_measured_hbm": comp_gbs / world / peaks["hbm_gbs"],
                         "frac_of_nominal_hbm": comp_gbs / world / NOMINAL["hbm_gbs"]},
             "roofline": roofline, "roofline_compose": roofline_compose,
+            "compose_training": compose_training,
             "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
             "cpu_baseline": cpu_baseline,
         }

@@ -38,6 +38,12 @@ SIGNATURES = {
                                                   ctypes.c_float, _P, ctypes.c_float, _P, _P,
                                                   _P]),
     "dora_compose": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64, _P, _P]),
+    "dora_compose_train": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64,
+                                          _P, _P, _P]),
+    "dora_compose_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+    "dora_compose_backward": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_float, ctypes.c_float,
+                                             ctypes.c_int, _I64, _I64, _P, _P, _P, _P,
+                                             ctypes.c_size_t, _P]),
     "dora_check_status": (ctypes.c_int, [_P, _P]),
     "dora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dora_version": (ctypes.c_int, []),

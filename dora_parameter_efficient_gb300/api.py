@@ -112,6 +112,77 @@ def dora_compose(base: torch.Tensor, lora: torch.Tensor, g: torch.Tensor, s: flo
     return out
 
 
+def dora_compose_train(base: torch.Tensor, lora: torch.Tensor, g: torch.Tensor, s: float,
+                       out: Optional[torch.Tensor] = None, inner: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None
+                       ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Training forward: out as dora_compose and inner = base + s * lora (the
+    activation the magnitude gradient needs), written in one pass."""
+    code = _dtype_code(base)
+    if lora.dtype != base.dtype or lora.shape != base.shape or base.dim() != 2:
+        raise ValueError("base and lora must be 2-D [T, d_out] of one dtype")
+    T, d_out = base.shape
+    if g.dtype != torch.float32 or g.shape != (d_out,):
+        raise ValueError("g must be float32 [d_out]")
+    out = torch.empty_like(base) if out is None else out
+    inner = torch.empty_like(base) if inner is None else inner
+    for t, name in ((out, "out"), (inner, "inner")):
+        if t.dtype != base.dtype or t.shape != base.shape:
+            raise ValueError(f"{name} must match base")
+    if T == 0 or d_out == 0:
+        return out, inner
+    st = _lib.load().dora_compose_train(_dev(base, "base"), _dev(lora, "lora"), _dev(g, "g"),
+                                        float(s), code, T, d_out, _dev(out, "out"),
+                                        _dev(inner, "inner"), _stream_handle(stream))
+    check(st, "dora_compose_train")
+    return out, inner
+
+
+def compose_backward_workspace_size(T: int, d_out: int) -> int:
+    return int(_lib.load().dora_compose_backward_workspace_size(T, d_out))
+
+
+def dora_compose_backward(d_out_grad: torch.Tensor, g: torch.Tensor, s: float,
+                          inner: Optional[torch.Tensor] = None,
+                          wnorm: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                          d_base: Optional[torch.Tensor] = None,
+                          d_lora: Optional[torch.Tensor] = None,
+                          dmag: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          stream: Optional[torch.cuda.Stream] = None):
+    """Backward of the compose: (d_base, d_lora, dmag).  dmag is computed when
+    inner and wnorm are given (a trainable magnitude), else it is None."""
+    code = _dtype_code(d_out_grad)
+    if d_out_grad.dim() != 2:
+        raise ValueError("d_out_grad must be 2-D [T, d_out]")
+    T, d_out = d_out_grad.shape
+    if g.dtype != torch.float32 or g.shape != (d_out,):
+        raise ValueError("g must be float32 [d_out]")
+    d_base = torch.empty_like(d_out_grad) if d_base is None else d_base
+    d_lora = torch.empty_like(d_out_grad) if d_lora is None else d_lora
+    want_dm = inner is not None
+    if want_dm:
+        if wnorm is None or wnorm.dtype != torch.float32 or wnorm.shape != (d_out,):
+            raise ValueError("wnorm must be float32 [d_out] when inner is given")
+        if inner.dtype != d_out_grad.dtype or inner.shape != d_out_grad.shape:
+            raise ValueError("inner must match d_out_grad")
+        dmag = torch.empty(d_out, dtype=torch.float32, device=d_out_grad.device) \
+            if dmag is None else dmag
+        if workspace is None:
+            workspace = torch.empty(max(16, compose_backward_workspace_size(T, d_out)),
+                                    dtype=torch.uint8, device=d_out_grad.device)
+    if T == 0 or d_out == 0:
+        return d_base, d_lora, dmag if want_dm else None
+    st = _lib.load().dora_compose_backward(
+        _dev(d_out_grad, "d_out_grad"), _dev(inner, "inner") if want_dm else None, _dev(g, "g"),
+        _dev(wnorm, "wnorm") if want_dm else None, float(eps), float(s), code, T, d_out,
+        _dev(d_base, "d_base"), _dev(d_lora, "d_lora"), _dev(dmag, "dmag") if want_dm else None,
+        _dev(workspace, "workspace") if want_dm else None,
+        workspace.numel() if want_dm else 0, _stream_handle(stream))
+    check(st, "dora_compose_backward")
+    return d_base, d_lora, dmag if want_dm else None
+
+
 def dora_check_status(workspace: torch.Tensor,
                       stream: Optional[torch.cuda.Stream] = None) -> int:
     """Device status word of the last dora_factored_norm on this workspace
@@ -139,4 +210,5 @@ def dora_factored_norm_noalloc(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor
 
 
 __all__ = ["dora_factored_norm", "dora_factored_norm_noalloc", "dora_compose",
+           "dora_compose_train", "dora_compose_backward", "compose_backward_workspace_size",
            "dora_check_status", "workspace_size", "alloc_workspace", "DoraError"]

@@ -118,4 +118,16 @@ cudaError_t launch_compose(const void* base, const void* lora, const float* g, f
                            int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,
                            cudaStream_t stream);
 
+// ------------------------------------------------------------------ training path of the compose
+constexpr int64_t kMaxDmParts = 256;   // row blocks of the magnitude-gradient column sums
+int64_t compose_backward_parts(int64_t T);
+cudaError_t launch_compose_train(const void* base, const void* lora, const float* g, float s,
+                                 int is_bf16, int64_t T, int64_t d_out, void* out, void* inner,
+                                 int num_sms, cudaStream_t stream);
+cudaError_t launch_compose_backward(const void* dout, const void* inner, const float* g,
+                                    const float* wnorm, float eps, float s, int is_bf16,
+                                    int64_t T, int64_t d_out, void* d_base, void* d_lora,
+                                    float* dmag, float* partials, int num_sms,
+                                    cudaStream_t stream);
+
 }  // namespace dora

@@ -484,6 +484,74 @@ int dora_compose(const void* base, const void* lora, const float* g, float s, in
                                     static_cast<cudaStream_t>(stream)));
 }
 
+int dora_compose_train(const void* base, const void* lora, const float* g, float s, int dtype,
+                       int64_t T, int64_t d_out, void* out, void* inner, void* stream) {
+  if (T < 0 || d_out < 0 || (dtype != DORA_BF16 && dtype != DORA_F32) || !std::isfinite(s))
+    return DORA_ERR_INVALID_ARG;
+  if (T == 0 || d_out == 0) return DORA_OK;
+  if (!base || !lora || !g || !out || !inner) return DORA_ERR_INVALID_ARG;
+  const size_t eb = dtype == DORA_BF16 ? 2 : 4;
+  const size_t nbytes = static_cast<size_t>(T) * d_out * eb;
+  const size_t gbytes = static_cast<size_t>(d_out) * 4;
+  for (const void* o : {out, inner}) {
+    if (overlap(o, nbytes, base, nbytes) || overlap(o, nbytes, lora, nbytes) ||
+        overlap(o, nbytes, g, gbytes))
+      return DORA_ERR_INVALID_ARG;
+  }
+  if (overlap(out, nbytes, inner, nbytes)) return DORA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  return cuda_status(launch_compose_train(base, lora, g, s, dtype == DORA_BF16, T, d_out, out,
+                                          inner, dev.sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dora_compose_backward_workspace_size(int64_t T, int64_t d_out) {
+  if (T < 0 || d_out < 0) return 0;
+  return static_cast<size_t>(compose_backward_parts(T)) * static_cast<size_t>(d_out) * 4;
+}
+
+int dora_compose_backward(const void* d_out_grad, const void* inner, const float* g,
+                          const float* wnorm, float eps, float s, int dtype, int64_t T,
+                          int64_t d_out, void* d_base, void* d_lora, float* dmag,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || d_out < 0 || (dtype != DORA_BF16 && dtype != DORA_F32) || !std::isfinite(s))
+    return DORA_ERR_INVALID_ARG;
+  if (T == 0 || d_out == 0) return DORA_OK;
+  if (!d_out_grad || !g || !d_base || !d_lora) return DORA_ERR_INVALID_ARG;
+  const size_t eb = dtype == DORA_BF16 ? 2 : 4;
+  const size_t nbytes = static_cast<size_t>(T) * d_out * eb;
+  const size_t vbytes = static_cast<size_t>(d_out) * 4;
+  if (dmag) {
+    if (!inner || !wnorm || !(eps > 0.f) || !std::isfinite(eps)) return DORA_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0 ||
+        workspace_bytes < dora_compose_backward_workspace_size(T, d_out))
+      return DORA_ERR_WORKSPACE;
+  }
+  // outputs overlap nothing they are computed from, nor each other
+  const void* ins[4] = {d_out_grad, g, dmag ? inner : nullptr, dmag ? wnorm : nullptr};
+  const size_t in_bytes[4] = {nbytes, vbytes, nbytes, vbytes};
+  const void* outs[3] = {d_base, d_lora, dmag};
+  const size_t out_bytes[3] = {nbytes, nbytes, vbytes};
+  for (int o = 0; o < 3; ++o) {
+    if (!outs[o]) continue;
+    for (int i = 0; i < 4; ++i)
+      if (ins[i] && overlap(outs[o], out_bytes[o], ins[i], in_bytes[i])) return DORA_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 3; ++o2)
+      if (outs[o2] && overlap(outs[o], out_bytes[o], outs[o2], out_bytes[o2]))
+        return DORA_ERR_INVALID_ARG;
+    if (dmag && overlap(outs[o], out_bytes[o], workspace, workspace_bytes))
+      return DORA_ERR_INVALID_ARG;
+  }
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  return cuda_status(launch_compose_backward(d_out_grad, inner, g, wnorm, eps, s,
+                                             dtype == DORA_BF16, T, d_out, d_base, d_lora, dmag,
+                                             static_cast<float*>(workspace), dev.sms,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 int dora_check_status(const void* workspace, void* stream) {
   if (!workspace) return DORA_ERR_INVALID_ARG;
   int h = -1;

@@ -174,6 +174,50 @@ int dora_compose(const void* base, const void* lora, const float* g, float s,
                  int dtype, int64_t T, int64_t d_out, void* out, void* stream);
 
 /*
+ * Training path of the compose ("Scaling DoRA", Chinese write-up sections
+ * 2.2, 4.2 and 5.2: the fused backward tier).  The norm is a detached
+ * constant in the backward (section 1.2.2), so with g = m / max(wnorm, eps)
+ *
+ *   d out / d base = g - 1,   d out / d lora = g s,   d out / d g = base + s lora.
+ */
+
+/*
+ * Forward of the training path: out as dora_compose, and
+ *   inner = base + s * lora    [T x d_out], dtype (rounded once from fp32)
+ * the activation the magnitude gradient needs, written in the same pass.
+ * Skip this entry point (call dora_compose) when the magnitude is frozen.
+ * out and inner must not overlap each other or the inputs.  T == 0 or
+ * d_out == 0 is a no-op.  Any alignment and d_out are accepted.
+ */
+int dora_compose_train(const void* base, const void* lora, const float* g, float s, int dtype,
+                       int64_t T, int64_t d_out, void* out, void* inner, void* stream);
+
+/* Bytes of workspace dora_compose_backward needs when it computes dmag
+ * (the per-row-block partial column sums): 1024 * d_out at T >= 256,
+ * 4 * T * d_out below.  0 for an invalid shape. */
+size_t dora_compose_backward_workspace_size(int64_t T, int64_t d_out);
+
+/*
+ * Backward of the compose, one pass over the upstream gradient:
+ *   d_out_grad  [T x d_out] dtype   dL/d out
+ *   d_base      [T x d_out] dtype   output, (g - 1) * d_out_grad
+ *   d_lora      [T x d_out] dtype   output, g * s * d_out_grad
+ *   g           [d_out] float32
+ * and, when dmag is not NULL (a trainable magnitude),
+ *   dmag_j = sum_t d_out_grad_tj * inner_tj / max(wnorm_j, eps)   [d_out] float32
+ * with inner from dora_compose_train, wnorm [d_out] float32 from the norm,
+ * and a workspace of dora_compose_backward_workspace_size bytes (16-byte
+ * aligned; no initialisation needed).  The column sums are taken over fixed
+ * row blocks and added in block order: the same result on every call, no
+ * atomics.  With dmag NULL, inner, wnorm and workspace are not read and may
+ * be NULL.  Outputs must not overlap each other or the inputs.
+ */
+int dora_compose_backward(const void* d_out_grad, const void* inner, const float* g,
+                          const float* wnorm, float eps, float s, int dtype, int64_t T,
+                          int64_t d_out, void* d_base, void* d_lora, float* dmag,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Waits for `stream`, then reads the device status word of `workspace` (as
  * last written by dora_factored_norm on it): DORA_OK, or DORA_ERR_TIMEOUT if
  * a kernel gave up on a pipeline wait (its outputs are then undefined, the

@@ -44,6 +44,9 @@ class Config:
     std_m_rel: float = 0.0015  # m = ||W||_row * (1 + N(0, std_m_rel))
     std_base: float = 1.0
     std_lora: float = 0.05
+    # upstream gradient dL/d out of the compose (training path); the pages
+    # give no distribution for it, N(0, 0.01) is this build's choice
+    std_grad: float = 0.01
     # "norm": compose uses g produced by the norm of the same module;
     # "synthetic": g ~ N(1, g_std) drawn directly (fp32).
     g_mode: str = "norm"
@@ -111,6 +114,20 @@ def norm_bytes(d_out: int, d_in: int, r: int, dtype: str) -> int:
     wnorm and g (fp32)."""
     eb = elem_bytes(dtype)
     return eb * (d_out * d_in + r * d_in + d_out * r + d_out) + 8 * d_out
+
+
+def compose_train_bytes(tokens: int, d_out: int, dtype: str) -> int:
+    """Algorithmic bytes of the training forward: read base, lora, g; write
+    out and inner."""
+    return 4 * tokens * d_out * elem_bytes(dtype) + 4 * d_out
+
+
+def compose_backward_bytes(tokens: int, d_out: int, dtype: str, dmag: bool = True) -> int:
+    """Algorithmic bytes of the backward: read d_out (and inner), g (and
+    wnorm); write d_base, d_lora (and dmag)."""
+    eb = elem_bytes(dtype)
+    n = tokens * d_out
+    return (4 * n * eb + 12 * d_out) if dmag else (3 * n * eb + 4 * d_out)
 
 
 def compose_bytes(tokens: int, d_out: int, dtype: str) -> int:

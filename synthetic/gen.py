@@ -31,7 +31,7 @@ from .configs import BF16, F32, Config
 CHUNK_ELEMS = 1 << 22
 
 # tensor ids inside the Philox key
-T_W, T_A, T_B, T_M, T_BASE, T_LORA, T_G = range(7)
+T_W, T_A, T_B, T_M, T_BASE, T_LORA, T_G, T_DOUT = range(8)
 
 _POOL: Optional[ThreadPoolExecutor] = None
 
@@ -143,3 +143,12 @@ def compose_inputs(cfg: Config, module: int = 0, seed: int = 0,
         out["g"] = normal(base_key + (T_G, module), 1, mod.d_out, cfg.g_std, F32,
                           mean=1.0).reshape(-1)
     return out
+
+
+def grad_inputs(cfg: Config, module: int = 0, seed: int = 0,
+                tokens: Optional[int] = None) -> np.ndarray:
+    """Upstream gradient d out [T x d_out] of the compose, in stored format,
+    N(0, cfg.std_grad)."""
+    mod = cfg.modules[module]
+    T = cfg.tokens if tokens is None else tokens
+    return normal((seed, cfg.index, T_DOUT, module), T, mod.d_out, cfg.std_grad, cfg.dtype)

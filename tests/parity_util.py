@@ -7,6 +7,12 @@ Tolerances (stated once, used by every GPU test):
 * compose, bf16 output: within 1 bf16 ulp of the oracle rounded once to bf16
   (distance in representable steps <= 1).
 * compose, fp32 output: within 2 fp32 ulp of the oracle rounded to fp32.
+* training path (inner, d_base, d_lora): the compose rule above.
+* dmag: |dmag - ref| <= 1e-5 * sum_t |d_out_tj * inner_tj| / max(wnorm_j, eps).
+  The kernel sums at most ceil(T / parts) exact products per thread in fp32,
+  then the parts (<= 256) compensated, then divides once: an error bound of
+  about (T / parts + 3) * 2^-24 of the absolute sum, 1e-6 at T / parts <= 16;
+  1e-5 leaves a factor of ten.
 """
 from __future__ import annotations
 
@@ -54,3 +60,5 @@ def ulp_distance(got_stored: np.ndarray, ref_stored: np.ndarray, dtype: str) -> 
 
 
 COMPOSE_MAX_ULP = {configs.BF16: 1, configs.F32: 2}
+
+DM_RTOL = 1e-5
