@@ -359,7 +359,7 @@ def run_ours(args):
     main_src = os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "gemm_pair.cu")
     comp_src = os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "compose.cu")
     roofline = {"kernel": "k_gemm_pair main pass (U = W A^T, the folded B G' tiles, sum W^2, "
-                          "rowsum(B o D)) on tcgen05 CTA pairs",
+                          "rowsum(B o D), the fused finalize) on tcgen05 CTA pairs",
                 "bound": "tensor", "achieved": main_tflops,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": main_tflops / peaks["bf16_tflops_sustained"],
@@ -371,9 +371,10 @@ def run_ours(args):
                           f"timed region (events between launches suspend the overlap with the "
                           f"neighbouring kernels, so this includes the launch latency)",
                 "traffic": recorded_traffic(main_src, "main_pass_8192x8192_r384.md"),
-                # reads W, A, B, G'_hi, G'_lo once; one pair of fp32 partials per row
+                # reads W, A, B, G'_hi, G'_lo, m once; writes one pair of fp32
+                # partials per row and segment (counted once) and wnorm, g
                 "algorithmic_bytes_per_launch": 2 * (d_out * d_in + r * d_in + d_out * r)
-                + 2 * 2 * r * r + 8 * d_out}
+                + 2 * 2 * r * r + 2 * d_out + 8 * d_out + 8 * d_out}
     roofline_compose = {"kernel": "k_compose<bf16>", "bound": "hbm", "achieved": cbytes / (comp_ms_m * 1e-3) / 1e9,
                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": cbytes / (comp_ms_m * 1e-3) / 1e9 / peaks["hbm_gbs"],

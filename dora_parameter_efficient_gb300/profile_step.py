@@ -1,8 +1,10 @@
 """Run the hot path (factored norm + compose) of one synthetic workload for a few
 steps and print per-step CUDA-event times; meant as the target of profilers
-(ncu), which want a short program with few launches.
+(ncu), which want a short program with few launches.  With --training each
+step also runs the training path of the compose (forward keeping inner,
+backward with the magnitude gradient).
 
-    python -m dora_parameter_efficient_gb300.profile_step --config 1 --steps 3
+    python -m dora_parameter_efficient_gb300.profile_step --config 1 --steps 3 [--training]
 """
 from __future__ import annotations
 
@@ -32,6 +34,7 @@ def main() -> int:
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--module", type=int, default=0)
     ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--training", action="store_true")
     args = ap.parse_args()
     cfg = configs.get(args.config)
     x = gen.norm_inputs(cfg, module=args.module)
@@ -43,6 +46,13 @@ def main() -> int:
     wn = torch.empty(d_out, dtype=torch.float32, device="cuda")
     g = torch.empty(d_out, dtype=torch.float32, device="cuda")
     out = torch.empty_like(base)
+    if args.training:
+        grad = to_dev(gen.grad_inputs(cfg, module=args.module), cfg.dtype)
+        inner = torch.empty_like(base)
+        d_base, d_lora = torch.empty_like(base), torch.empty_like(base)
+        dmag = torch.empty(d_out, dtype=torch.float32, device="cuda")
+        bws = torch.empty(max(16, api.compose_backward_workspace_size(base.shape[0], d_out)),
+                          dtype=torch.uint8, device="cuda")
     for i in range(args.steps):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record()
@@ -50,6 +60,10 @@ def main() -> int:
         e[1].record()
         api.dora_compose(base, lora, g, cfg.s, out=out)
         e[2].record()
+        if args.training:
+            api.dora_compose_train(base, lora, g, cfg.s, out=out, inner=inner)
+            api.dora_compose_backward(grad, g, cfg.s, inner=inner, wnorm=wn, eps=cfg.eps,
+                                      d_base=d_base, d_lora=d_lora, dmag=dmag, workspace=bws)
         torch.cuda.synchronize()
         print(f"step {i}: norm {e[0].elapsed_time(e[1]) * 1e3:.1f} us, "
               f"compose {e[1].elapsed_time(e[2]) * 1e3:.1f} us")

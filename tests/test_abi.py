@@ -130,3 +130,37 @@ def test_compose_argument_checks(lib, kw, status):
 
 def test_check_status_null(lib):
     assert lib.dora_check_status(None, None) == _lib.DORA_ERR_INVALID_ARG
+
+
+def test_training_compose_rejects_bad_arguments(lib):
+    P = 1 << 20
+    T, d = 64, 128
+    n = T * d * 2
+    # forward: null inner, overlapping outputs, bad dtype
+    assert lib.dora_compose_train(P, 2 * P, 3 * P, 1.0, _lib.DORA_BF16, T, d, 4 * P, None,
+                                  None) == _lib.DORA_ERR_INVALID_ARG
+    assert lib.dora_compose_train(P, 2 * P, 3 * P, 1.0, _lib.DORA_BF16, T, d, 4 * P,
+                                  4 * P + n // 2, None) == _lib.DORA_ERR_INVALID_ARG
+    assert lib.dora_compose_train(P, 2 * P, 3 * P, 1.0, 5, T, d, 4 * P, 5 * P,
+                                  None) == _lib.DORA_ERR_INVALID_ARG
+    assert lib.dora_compose_train(P, 2 * P, 3 * P, 1.0, _lib.DORA_BF16, 0, d, 4 * P, 5 * P,
+                                  None) == _lib.DORA_OK
+    # backward: dmag without inner / wnorm, workspace too small or misaligned, outputs overlap
+    ws = lib.dora_compose_backward_workspace_size(T, d)
+    assert ws == T * d * 4
+    assert lib.dora_compose_backward_workspace_size(4096, d) == 256 * d * 4
+    assert lib.dora_compose_backward(P, None, 3 * P, 4 * P, 1e-6, 1.0, _lib.DORA_BF16, T, d,
+                                     5 * P, 6 * P, 7 * P, 8 * P, ws,
+                                     None) == _lib.DORA_ERR_INVALID_ARG
+    assert lib.dora_compose_backward(P, 2 * P, 3 * P, 4 * P, 1e-6, 1.0, _lib.DORA_BF16, T, d,
+                                     5 * P, 6 * P, 7 * P, 8 * P, ws - 4,
+                                     None) == _lib.DORA_ERR_WORKSPACE
+    assert lib.dora_compose_backward(P, 2 * P, 3 * P, 4 * P, 1e-6, 1.0, _lib.DORA_BF16, T, d,
+                                     5 * P, 6 * P, 7 * P, 8 * P + 4, ws,
+                                     None) == _lib.DORA_ERR_WORKSPACE
+    assert lib.dora_compose_backward(P, 2 * P, 3 * P, 4 * P, 1e-6, 1.0, _lib.DORA_BF16, T, d,
+                                     5 * P, 5 * P + 16, None, None, 0,
+                                     None) == _lib.DORA_ERR_INVALID_ARG
+    assert lib.dora_compose_backward(P, 2 * P, 3 * P, 4 * P, 0.0, 1.0, _lib.DORA_BF16, T, d,
+                                     5 * P, 6 * P, 7 * P, 8 * P, ws,
+                                     None) == _lib.DORA_ERR_INVALID_ARG
