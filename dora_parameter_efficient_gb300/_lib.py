@@ -26,6 +26,19 @@ DORA_F32 = 1
 # name -> (restype, argtypes), mirroring include/dora.h
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
+
+
+class NormModule(ctypes.Structure):
+    """struct dora_norm_module"""
+    _fields_ = [("W", _P), ("A", _P), ("B", _P), ("m", _P), ("wnorm", _P), ("g", _P),
+                ("d_out", _I64), ("d_in", _I64)]
+
+
+class ComposeModule(ctypes.Structure):
+    """struct dora_compose_module"""
+    _fields_ = [("base", _P), ("lora", _P), ("g", _P), ("out", _P), ("T", _I64), ("d_out", _I64)]
+
+
 SIGNATURES = {
     "dora_norm_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, ctypes.c_int]),
     "dora_factored_norm": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
@@ -38,6 +51,13 @@ SIGNATURES = {
                                                   ctypes.c_float, _P, ctypes.c_float, _P, _P,
                                                   _P]),
     "dora_compose": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64, _P, _P]),
+    "dora_norm_grouped_workspace_size": (ctypes.c_size_t, [_P, ctypes.c_int, _I64, ctypes.c_int]),
+    "dora_factored_norm_grouped": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _I64,
+                                                  ctypes.c_float, ctypes.c_float, _P,
+                                                  ctypes.c_size_t, _P]),
+    "dora_compose_grouped_workspace_size": (ctypes.c_size_t, [ctypes.c_int]),
+    "dora_compose_grouped": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_float, ctypes.c_int, _P,
+                                            ctypes.c_size_t, _P]),
     "dora_compose_train": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64,
                                           _P, _P, _P]),
     "dora_compose_backward_workspace_size": (ctypes.c_size_t, [_I64, _I64]),

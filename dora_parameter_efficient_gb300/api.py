@@ -112,6 +112,82 @@ def dora_compose(base: torch.Tensor, lora: torch.Tensor, g: torch.Tensor, s: flo
     return out
 
 
+def _norm_table(modules, wnorms, gs):
+    table = (_lib.NormModule * len(modules))()
+    for i, (W, A, B, m) in enumerate(modules):
+        d_out, d_in = W.shape
+        table[i] = _lib.NormModule(_dev(W, "W"), _dev(A, "A"), _dev(B, "B"), _dev(m, "m"),
+                                   _dev(wnorms[i], "wnorm"), _dev(gs[i], "g"), d_out, d_in)
+    return table
+
+
+def norm_grouped_workspace_size(modules, dtype: torch.dtype) -> int:
+    r = modules[0][1].shape[0] if modules else 0
+    table = (_lib.NormModule * len(modules))()
+    for i, (W, A, B, m) in enumerate(modules):
+        table[i] = _lib.NormModule(None, None, None, None, None, None, W.shape[0], W.shape[1])
+    return int(_lib.load().dora_norm_grouped_workspace_size(table, len(modules), r, _DTYPES[dtype]))
+
+
+def dora_factored_norm_grouped(modules, s: float, eps: float, wnorms=None, gs=None,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream: Optional[torch.cuda.Stream] = None):
+    """dora_factored_norm for a list of modules (W, A, B, m), all of one rank and
+    dtype, in one launch sequence; returns the lists (wnorms, gs)."""
+    modules = list(modules)
+    if not modules:
+        return [], []
+    W0, A0 = modules[0][0], modules[0][1]
+    code = _dtype_code(W0)
+    r = A0.shape[0]
+    for W, A, B, m in modules:
+        if any(t.dtype != W0.dtype for t in (W, A, B, m)):
+            raise TypeError("every tensor of a grouped call must have one dtype")
+        if A.shape[0] != r or A.shape[1] != W.shape[1] or B.shape != (W.shape[0], r) \
+                or m.shape != (W.shape[0],):
+            raise ValueError("shape mismatch in a grouped module (one rank for all modules)")
+    dev = W0.device
+    wnorms = [torch.empty(W.shape[0], dtype=torch.float32, device=dev) for W, *_ in modules] \
+        if wnorms is None else wnorms
+    gs = [torch.empty(W.shape[0], dtype=torch.float32, device=dev) for W, *_ in modules] \
+        if gs is None else gs
+    if workspace is None:
+        workspace = torch.empty(max(256, norm_grouped_workspace_size(modules, W0.dtype)),
+                                dtype=torch.uint8, device=dev)
+    table = _norm_table(modules, wnorms, gs)
+    st = _lib.load().dora_factored_norm_grouped(table, len(modules), code, r, float(s),
+                                                float(eps), _dev(workspace, "workspace"),
+                                                workspace.numel(), _stream_handle(stream))
+    check(st, "dora_factored_norm_grouped")
+    return wnorms, gs
+
+
+def dora_compose_grouped(modules, s: float, outs=None, workspace: Optional[torch.Tensor] = None,
+                         stream: Optional[torch.cuda.Stream] = None):
+    """dora_compose for a list of modules (base, lora, g) of one dtype, in one
+    launch; returns the list of outputs."""
+    modules = list(modules)
+    if not modules:
+        return []
+    code = _dtype_code(modules[0][0])
+    outs = [torch.empty_like(b) for b, _, _ in modules] if outs is None else outs
+    table = (_lib.ComposeModule * len(modules))()
+    for i, (base, lora, g) in enumerate(modules):
+        if lora.shape != base.shape or base.dim() != 2 or g.shape != (base.shape[1],) \
+                or g.dtype != torch.float32 or lora.dtype != base.dtype:
+            raise ValueError("grouped compose module: base, lora [T, d_out] of one dtype, g fp32 [d_out]")
+        table[i] = _lib.ComposeModule(_dev(base, "base"), _dev(lora, "lora"), _dev(g, "g"),
+                                      _dev(outs[i], "out"), base.shape[0], base.shape[1])
+    lib = _lib.load()
+    if workspace is None:
+        workspace = torch.empty(max(256, lib.dora_compose_grouped_workspace_size(len(modules))),
+                                dtype=torch.uint8, device=modules[0][0].device)
+    st = lib.dora_compose_grouped(table, len(modules), float(s), code, _dev(workspace, "workspace"),
+                                  workspace.numel(), _stream_handle(stream))
+    check(st, "dora_compose_grouped")
+    return outs
+
+
 def dora_compose_train(base: torch.Tensor, lora: torch.Tensor, g: torch.Tensor, s: float,
                        out: Optional[torch.Tensor] = None, inner: Optional[torch.Tensor] = None,
                        stream: Optional[torch.cuda.Stream] = None
@@ -211,4 +287,5 @@ def dora_factored_norm_noalloc(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor
 
 __all__ = ["dora_factored_norm", "dora_factored_norm_noalloc", "dora_compose",
            "dora_compose_train", "dora_compose_backward", "compose_backward_workspace_size",
+           "dora_factored_norm_grouped", "dora_compose_grouped", "norm_grouped_workspace_size",
            "dora_check_status", "workspace_size", "alloc_workspace", "DoraError"]

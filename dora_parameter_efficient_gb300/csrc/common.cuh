@@ -57,15 +57,44 @@ struct GramParams {
   unsigned long long timeout_ns;
 };
 
+// one module of a grouped Gram launch (same rank, so the same block grid)
+struct GramModule {
+  CUtensorMap tAx, tAy;
+  uint16_t* G_hi;
+  uint16_t* G_lo;
+  int k_tiles;
+};
+
 size_t gram_smem_bytes(int bw, int stages);
 cudaError_t launch_gram(const CUtensorMap& tAx, const CUtensorMap& tAy, const GramParams& p,
                         cudaStream_t stream);
+// grouped: p.k_tiles, p.G_hi, p.G_lo are taken from mods[]; p.cluster divides every
+// module's K tiles evenly enough (<= the smallest k_tiles)
+cudaError_t launch_gram_grouped(const GramModule* mods, int n_mods, const GramParams& p,
+                                cudaStream_t stream);
 
 // ------------------------------------------------------------------ CTA-pair main pass
 // D [256-row pair tile x n0+n1] = X * Y^T over the K tiles of one work item,
 // M = 256 per CTA pair (tcgen05 cta_group::2), persistent over items; the
 // last K segment of each 128-row group to finish assembles wnorm and g for
 // its rows.
+
+// One module of a grouped launch (every module of the group has the same
+// rank): its tensor maps, pointers, shape and K segments, in device memory.
+struct PairModule {
+  CUtensorMap tW, tA, tB, tGhi, tGlo;
+  const uint16_t* B;
+  const uint16_t* m;
+  float* wnorm;
+  float* g;
+  float* out_sumsq;      // [splits][rows]
+  float* out_dot;        // [splits][rows]
+  int* tile_done;        // [pair_tiles][2] (zero at launch)
+  int rows, kt_w, pair_tiles, splits;
+  int item_begin;        // first work item of this module in the grid's item sequence
+  int seg_k[17];
+};
+
 struct PairParams {
   int rows;              // d_out
   int n0, n1;            // N of the first / second MMA (n1 = 0 when r <= 256)
@@ -77,7 +106,9 @@ struct PairParams {
   int pair_tiles;        // ceil(d_out / 256)
   int stages;
   int r;
-  uint32_t tmem_cols;
+  uint32_t tmem_cols;    // acc_bufs * acc_stride
+  int acc_bufs;          // accumulator buffers (2 when two fit in the 512 TMEM columns)
+  uint32_t acc_stride;   // TMEM columns per accumulator buffer
   // epilogue and the fused finalize
   const uint16_t* B;     // [rows x r] bf16
   const uint16_t* m;     // [rows] bf16
@@ -90,6 +121,10 @@ struct PairParams {
   int* work_ctr;         // next unclaimed work item; zero at launch
   int* status;
   unsigned long long timeout_ns;
+  // grouped launch: the per-module fields above are unused, these are
+  const PairModule* mods;
+  int n_mods;
+  int n_items;
 };
 
 size_t pair_smem_bytes(int n_pad, int stages);
@@ -98,6 +133,7 @@ int pair_max_clusters(size_t smem_bytes);
 cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const CUtensorMap& tB,
                              const CUtensorMap& tGhi, const CUtensorMap& tGlo, const PairParams& p,
                              int clusters, cudaStream_t stream);
+cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStream_t stream);
 
 // ------------------------------------------------------------------ SIMT (fp32 inputs)
 enum SimtMode : int { kSimtSumSq = 1, kSimtDotB = 2, kSimtStore = 4 };
@@ -117,6 +153,19 @@ cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const
 cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
                            int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,
                            cudaStream_t stream);
+
+// one module of a grouped compose (device memory)
+struct ComposeModule {
+  const void* base;
+  const void* lora;
+  const float* g;
+  void* out;
+  int64_t T, d_out;
+  int64_t unit_begin;    // first work unit of this module
+};
+int64_t compose_grouped_units(int64_t T, int64_t d_out, int is_bf16);
+cudaError_t launch_compose_grouped(const ComposeModule* mods, int n_mods, int64_t n_units,
+                                   float s, int is_bf16, int num_sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------ training path of the compose
 constexpr int64_t kMaxDmParts = 256;   // row blocks of the magnitude-gradient column sums

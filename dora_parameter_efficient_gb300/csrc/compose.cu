@@ -186,7 +186,96 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Grouped compose over a module table: unit u = (module, 16-row block,
+// 256-vector column block), numbered module by module; block b takes units
+// b, b + gridDim.x, ...  A thread keeps one column vector and its g values
+// for the unit's rows.  Requires 16-byte rows (d_out a multiple of 8 bf16 /
+// 4 fp32) and 16-byte aligned pointers in every module.
+constexpr int kGroupRows = 16;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kColThreads)
+    k_compose_grouped(const ComposeModule* __restrict__ mods, int n_mods, int64_t n_units,
+                      float s) {
+  constexpr int EPV = BF16 ? 8 : 4;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    int lo = 0, hi = n_mods - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (mods[mid].unit_begin <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    const ComposeModule& md = mods[lo];
+    const int64_t dv = md.d_out / EPV;
+    const int64_t xblocks = (dv + kColThreads - 1) / kColThreads;
+    const int64_t local = u - md.unit_begin;
+    const int64_t rb = local / xblocks;
+    const int64_t c = (local - rb * xblocks) * kColThreads + threadIdx.x;
+    if (c >= dv) continue;
+    const uint4* base = static_cast<const uint4*>(md.base);
+    const uint4* lora = static_cast<const uint4*>(md.lora);
+    uint4* out = static_cast<uint4*>(md.out);
+    float gv[EPV], gm[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      gv[e] = __ldg(md.g + c * EPV + e);
+      gm[e] = __fsub_rn(gv[e], 1.0f);
+    }
+    const int64_t r0 = rb * kGroupRows;
+    const int64_t r1 = r0 + kGroupRows < md.T ? r0 + kGroupRows : md.T;
+    for (int64_t rr = r0; rr < r1; rr += kRowUnroll) {
+      uint4 bv[kRowUnroll], lv[kRowUnroll];
+#pragma unroll
+      for (int k = 0; k < kRowUnroll; ++k) {
+        if (rr + k < r1) {
+          bv[k] = __ldcs(base + (rr + k) * dv + c);
+          lv[k] = __ldcs(lora + (rr + k) * dv + c);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRowUnroll; ++k) {
+        if (rr + k >= r1) continue;
+        uint4 o;
+        if (BF16) {
+          const uint32_t bw[4] = {bv[k].x, bv[k].y, bv[k].z, bv[k].w};
+          const uint32_t lw[4] = {lv[k].x, lv[k].y, lv[k].z, lv[k].w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ow[e] = pack_bf16x2_rn(compose1m(bf16_lo(bw[e]), bf16_lo(lw[e]), gv[2 * e], gm[2 * e], s),
+                                   compose1m(bf16_hi(bw[e]), bf16_hi(lw[e]), gv[2 * e + 1], gm[2 * e + 1], s));
+          o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        } else {
+          o.x = __float_as_uint(compose1m(__uint_as_float(bv[k].x), __uint_as_float(lv[k].x), gv[0], gm[0], s));
+          o.y = __float_as_uint(compose1m(__uint_as_float(bv[k].y), __uint_as_float(lv[k].y), gv[1], gm[1], s));
+          o.z = __float_as_uint(compose1m(__uint_as_float(bv[k].z), __uint_as_float(lv[k].z), gv[2], gm[2], s));
+          o.w = __float_as_uint(compose1m(__uint_as_float(bv[k].w), __uint_as_float(lv[k].w), gv[3], gm[3], s));
+        }
+        __stcs(out + (rr + k) * dv + c, o);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+int64_t compose_grouped_units(int64_t T, int64_t d_out, int is_bf16) {
+  const int64_t dv = d_out / (is_bf16 ? 8 : 4);
+  return ((T + kGroupRows - 1) / kGroupRows) * ((dv + kColThreads - 1) / kColThreads);
+}
+
+cudaError_t launch_compose_grouped(const ComposeModule* mods, int n_mods, int64_t n_units,
+                                   float s, int is_bf16, int num_sms, cudaStream_t stream) {
+  if (n_units == 0) return cudaSuccess;
+  int64_t blocks = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 4;
+  if (blocks > n_units) blocks = n_units;
+  if (is_bf16)
+    k_compose_grouped<true><<<static_cast<unsigned>(blocks), kColThreads, 0, stream>>>(mods, n_mods, n_units, s);
+  else
+    k_compose_grouped<false><<<static_cast<unsigned>(blocks), kColThreads, 0, stream>>>(mods, n_mods, n_units, s);
+  note_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
                            int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,

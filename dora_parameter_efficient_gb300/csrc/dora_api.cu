@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "dora.h"
 #include "common.cuh"
@@ -351,7 +352,10 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (clusters_max <= 0) return DORA_ERR_CUDA;
     plan_pair_segments(pp, clusters_max);
     pp.r = static_cast<int>(r);
-    pp.tmem_cols = tmem_cols;
+    // two accumulators when they fit in the 512 tensor-memory columns
+    pp.acc_stride = tmem_cols;
+    pp.acc_bufs = 2 * tmem_cols <= 512 ? 2 : 1;
+    pp.tmem_cols = tmem_cols * static_cast<uint32_t>(pp.acc_bufs);
     pp.B = static_cast<const uint16_t*>(B);
     pp.m = static_cast<const uint16_t*>(m);
     // the sum over splits of rowsum(B o D) is cross + (s/2) ba, so the
@@ -393,6 +397,234 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   }
   DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, pba, n_ba, s, m, bf16, eps,
                            wnorm, g, stream));
+  return DORA_OK;
+}
+
+// ---------------------------------------------------------------- grouped norm
+// K segments of one module in a grouped launch: 3 : 2 : 1 when the K range
+// allows it (the grid is filled by all modules together), else one.
+void plan_module_segments(int ktot, int* seg_k, int* splits) {
+  if (ktot >= 6) {
+    static const int w[3] = {3, 2, 1};
+    int acc = 0;
+    seg_k[0] = 0;
+    for (int i = 0; i < 3; ++i) {
+      acc += w[i];
+      seg_k[i + 1] = static_cast<int>((static_cast<int64_t>(ktot) * acc + 3) / 6);
+    }
+    *splits = 3;
+  } else {
+    seg_k[0] = 0;
+    seg_k[1] = ktot;
+    *splits = 1;
+  }
+}
+
+struct GroupedPlan {
+  bool fused = false;         // the one-launch tensor-core path
+  size_t zero_bytes = 0, off_pmods = 0, off_gmods = 0, total = 0;
+  std::vector<size_t> off_ghi, off_glo, off_pbase, off_pcross, off_single;
+  std::vector<int> tile_done_word, splits, seg0;
+};
+
+bool grouped_fused(int dtype, int64_t r, float s) { return dtype == DORA_BF16 && r > 0 && s != 0.f; }
+
+GroupedPlan make_grouped_plan(const dora_norm_module* mods, int n, int64_t r, int dtype,
+                              bool fused) {
+  GroupedPlan gp;
+  gp.fused = fused;
+  size_t off = 0;
+  if (!fused) {
+    // the per-module path, each module with its own workspace
+    for (int i = 0; i < n; ++i) {
+      gp.off_single.push_back(off);
+      off = align_up(off + make_plan(mods[i].d_out, mods[i].d_in, r, dtype).total, 256);
+    }
+    gp.total = off;
+    return gp;
+  }
+  const int rp = static_cast<int>(ceil_div(r, 16) * 16);
+  int words = kCtlTileDone;
+  for (int i = 0; i < n; ++i) {
+    gp.tile_done_word.push_back(words);
+    words += 2 * static_cast<int>(ceil_div(mods[i].d_out, 2 * kTcBlockM));
+  }
+  off = align_up(static_cast<size_t>(words) * 4, 256);
+  gp.zero_bytes = off;
+  gp.off_pmods = off;
+  off = align_up(off + sizeof(PairModule) * n, 256);
+  gp.off_gmods = off;
+  off = align_up(off + sizeof(GramModule) * n, 256);
+  const size_t rp2 = static_cast<size_t>(rp) * rp;
+  for (int i = 0; i < n; ++i) {
+    const int ktot = static_cast<int>(ceil_div(mods[i].d_in, kTcBlockK) + 2 * ceil_div(r, kTcBlockK));
+    int seg[17], nseg = 1;
+    plan_module_segments(ktot, seg, &nseg);
+    gp.splits.push_back(nseg);
+    gp.off_ghi.push_back(off);
+    off = align_up(off + rp2 * 2, 256);
+    gp.off_glo.push_back(off);
+    off = align_up(off + rp2 * 2, 256);
+    gp.off_pbase.push_back(off);
+    off = align_up(off + static_cast<size_t>(nseg) * mods[i].d_out * 4, 256);
+    gp.off_pcross.push_back(off);
+    off = align_up(off + static_cast<size_t>(nseg) * mods[i].d_out * 4, 256);
+  }
+  gp.total = off;
+  return gp;
+}
+
+// host checks of one module, as dora_factored_norm does them
+int check_module(const dora_norm_module& md, int64_t r, int dtype, float s, float eps) {
+  if (!shape_ok(md.d_out, md.d_in, r, dtype)) {
+    if (r > DORA_MAX_RANK && md.d_out >= 0 && md.d_in >= 0) return DORA_ERR_UNSUPPORTED;
+    return DORA_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(s) || !(eps > 0.f) || !std::isfinite(eps)) return DORA_ERR_INVALID_ARG;
+  if (md.d_out == 0) return DORA_OK;
+  const size_t eb = dtype == DORA_BF16 ? 2 : 4;
+  const bool adapter = (r > 0) && (s != 0.f) && (md.d_in > 0);
+  if (!md.m || !md.wnorm || !md.g) return DORA_ERR_INVALID_ARG;
+  if (md.d_in > 0 && !md.W) return DORA_ERR_INVALID_ARG;
+  if (adapter && (!md.A || !md.B)) return DORA_ERR_INVALID_ARG;
+  const size_t vec_bytes = static_cast<size_t>(md.d_out) * 4;
+  if (overlap(md.wnorm, vec_bytes, md.g, vec_bytes)) return DORA_ERR_INVALID_ARG;
+  if (md.d_in > 0 && (overlap(md.wnorm, vec_bytes, md.W, md.d_out * md.d_in * eb) ||
+                      overlap(md.g, vec_bytes, md.W, md.d_out * md.d_in * eb)))
+    return DORA_ERR_INVALID_ARG;
+  if (overlap(md.wnorm, vec_bytes, md.m, md.d_out * eb) || overlap(md.g, vec_bytes, md.m, md.d_out * eb))
+    return DORA_ERR_INVALID_ARG;
+  if (md.d_in > 0 && ((md.d_in * eb) % 16 != 0 || !aligned16(md.W))) return DORA_ERR_UNSUPPORTED;
+  if (adapter && ((r * eb) % 16 != 0 || !aligned16(md.A) || !aligned16(md.B)))
+    return DORA_ERR_UNSUPPORTED;
+  return DORA_OK;
+}
+
+int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, int64_t r, float s,
+                               float eps, void* workspace, size_t workspace_bytes, void* stream_v) {
+  if (n < 0 || (n > 0 && !mods)) return DORA_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const int st = check_module(mods[i], r, dtype, s, eps);
+    if (st != DORA_OK) return st;
+  }
+  if (n == 0) return DORA_OK;
+  // modules with work on the tensor-core path (d_out, d_in > 0)
+  bool fused = grouped_fused(dtype, r, s);
+  for (int i = 0; i < n; ++i)
+    if (mods[i].d_out == 0 || mods[i].d_in == 0) fused = false;
+  const GroupedPlan gp = make_grouped_plan(mods, n, r, dtype, fused);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < gp.total)
+    return DORA_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (!fused) {
+    for (int i = 0; i < n; ++i) {
+      const dora_norm_module& md = mods[i];
+      const int st = factored_norm_impl(md.W, md.A, md.B, dtype, md.d_out, md.d_in, r, s, md.m,
+                                        eps, md.wnorm, md.g, ws + gp.off_single[i],
+                                        workspace_bytes - gp.off_single[i], stream_v, nullptr,
+                                        nullptr);
+      if (st != DORA_OK) return st;
+    }
+    return DORA_OK;
+  }
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  int* status = reinterpret_cast<int*>(ws);
+  const int rp = static_cast<int>(ceil_div(r, 16) * 16);
+  const int gnb = gram_nb(rp), gbw = gram_bw(rp);
+  const uint32_t tmem_cols = [&] {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(rp)) c <<= 1;
+    return c;
+  }();
+  const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
+  const int n1 = rp - n0;
+  const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
+  const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+
+  std::vector<PairModule> pm(n);
+  std::vector<GramModule> gm(n);
+  int min_kt = 1 << 30;
+  int item = 0;
+  for (int i = 0; i < n; ++i) {
+    const dora_norm_module& md = mods[i];
+    uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + gp.off_ghi[i]);
+    uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + gp.off_glo[i]);
+    PairModule& p = pm[i];
+    std::memset(&p, 0, sizeof(p));
+    if (!make_map_bf16(&p.tW, md.W, md.d_in, md.d_out, kTcBlockM) ||
+        !make_map_bf16(&p.tA, md.A, md.d_in, r, y_box2) ||
+        !make_map_bf16(&p.tB, md.B, r, md.d_out, kTcBlockM) ||
+        !make_map_bf16(&p.tGhi, Ghi, rp, rp, y_box2) || !make_map_bf16(&p.tGlo, Glo, rp, rp, y_box2))
+      return DORA_ERR_CUDA;
+    p.B = static_cast<const uint16_t*>(md.B);
+    p.m = static_cast<const uint16_t*>(md.m);
+    p.wnorm = md.wnorm;
+    p.g = md.g;
+    p.out_sumsq = reinterpret_cast<float*>(ws + gp.off_pbase[i]);
+    p.out_dot = reinterpret_cast<float*>(ws + gp.off_pcross[i]);
+    p.tile_done = status + gp.tile_done_word[i];
+    p.rows = static_cast<int>(md.d_out);
+    p.kt_w = static_cast<int>(ceil_div(md.d_in, kTcBlockK));
+    p.pair_tiles = static_cast<int>(ceil_div(md.d_out, 2 * kTcBlockM));
+    plan_module_segments(p.kt_w + 2 * kt_b, p.seg_k, &p.splits);
+    p.item_begin = item;
+    item += p.pair_tiles * p.splits;
+    GramModule& q = gm[i];
+    std::memset(&q, 0, sizeof(q));
+    if (!make_map_bf16(&q.tAx, md.A, md.d_in, r, kTcBlockM) ||
+        !make_map_bf16(&q.tAy, md.A, md.d_in, r, gbw))
+      return DORA_ERR_CUDA;
+    q.G_hi = Ghi;
+    q.G_lo = Glo;
+    q.k_tiles = p.kt_w;
+    if (p.kt_w < min_kt) min_kt = p.kt_w;
+  }
+  PairModule* pm_dev = reinterpret_cast<PairModule*>(ws + gp.off_pmods);
+  GramModule* gm_dev = reinterpret_cast<GramModule*>(ws + gp.off_gmods);
+  DORA_TRY(cudaMemsetAsync(status, 0, gp.zero_bytes, stream));
+  DORA_TRY(cudaMemcpyAsync(pm_dev, pm.data(), sizeof(PairModule) * n, cudaMemcpyHostToDevice, stream));
+  DORA_TRY(cudaMemcpyAsync(gm_dev, gm.data(), sizeof(GramModule) * n, cudaMemcpyHostToDevice, stream));
+
+  GramParams pg{};
+  pg.nb = gnb;
+  pg.bw = gbw;
+  pg.rp = rp;
+  pg.k_tiles = min_kt;
+  pg.stages = kGramStages;
+  pg.cluster = kGramCluster;
+  while (pg.cluster > 1 && pg.cluster > min_kt) pg.cluster >>= 1;
+  pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
+  pg.scale = 0.5f * s;
+  pg.status = status;
+  pg.timeout_ns = kDefaultTimeoutNs;
+  DORA_TRY(launch_gram_grouped(gm_dev, n, pg, stream));
+
+  PairParams pp{};
+  pp.n0 = n0;
+  pp.n1 = n1;
+  pp.y_box_rows = y_box2;
+  pp.kt_b = kt_b;
+  pp.stages = pair_pick_stages(rp);
+  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages));
+  if (clusters_max <= 0) return DORA_ERR_CUDA;
+  pp.r = static_cast<int>(r);
+  pp.acc_stride = tmem_cols;
+  pp.acc_bufs = 2 * tmem_cols <= 512 ? 2 : 1;
+  pp.tmem_cols = tmem_cols * static_cast<uint32_t>(pp.acc_bufs);
+  pp.two_s = 2.f * s;
+  pp.s_sq = s * s;
+  pp.eps = eps;
+  pp.work_ctr = status + kCtlWork;
+  pp.status = status;
+  pp.timeout_ns = kDefaultTimeoutNs;
+  pp.mods = pm_dev;
+  pp.n_mods = n;
+  pp.n_items = item;
+  const int clusters = item < clusters_max ? item : clusters_max;
+  DORA_TRY(launch_gemm_pair_grouped(pp, clusters, stream));
   return DORA_OK;
 }
 
@@ -483,6 +715,82 @@ int dora_compose(const void* base, const void* lora, const float* g, float s, in
   if (dst != DORA_OK) return dst;
   return cuda_status(launch_compose(base, lora, g, s, dtype == DORA_BF16, T, d_out, out, dev.sms,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t dora_norm_grouped_workspace_size(const dora_norm_module* modules, int n_modules,
+                                        int64_t r, int dtype) {
+  if (n_modules < 0 || (n_modules > 0 && !modules)) return 0;
+  bool fused = grouped_fused(dtype, r, 1.f);
+  for (int i = 0; i < n_modules; ++i) {
+    if (!shape_ok(modules[i].d_out, modules[i].d_in, r, dtype)) return 0;
+    if (modules[i].d_out == 0 || modules[i].d_in == 0) fused = false;
+  }
+  // room for both layouts: s (which decides the path) is not an argument here
+  const size_t a = make_grouped_plan(modules, n_modules, r, dtype, fused).total;
+  const size_t b = make_grouped_plan(modules, n_modules, r, dtype, false).total;
+  return a > b ? a : b;
+}
+
+int dora_factored_norm_grouped(const dora_norm_module* modules, int n_modules, int dtype,
+                               int64_t r, float s, float eps, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return factored_norm_grouped_impl(modules, n_modules, dtype, r, s, eps, workspace,
+                                    workspace_bytes, stream);
+}
+
+size_t dora_compose_grouped_workspace_size(int n_modules) {
+  if (n_modules < 0) return 0;
+  return align_up(sizeof(ComposeModule) * static_cast<size_t>(n_modules), 256);
+}
+
+int dora_compose_grouped(const dora_compose_module* modules, int n_modules, float s, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_modules < 0 || (n_modules > 0 && !modules) || (dtype != DORA_BF16 && dtype != DORA_F32) ||
+      !std::isfinite(s))
+    return DORA_ERR_INVALID_ARG;
+  const size_t eb = dtype == DORA_BF16 ? 2 : 4;
+  bool vec = true;
+  for (int i = 0; i < n_modules; ++i) {
+    const dora_compose_module& md = modules[i];
+    if (md.T < 0 || md.d_out < 0) return DORA_ERR_INVALID_ARG;
+    if (md.T == 0 || md.d_out == 0) continue;
+    if (!md.base || !md.lora || !md.g || !md.out) return DORA_ERR_INVALID_ARG;
+    const size_t nbytes = static_cast<size_t>(md.T) * md.d_out * eb;
+    if ((md.out != md.base && overlap(md.out, nbytes, md.base, nbytes)) ||
+        (md.out != md.lora && overlap(md.out, nbytes, md.lora, nbytes)) ||
+        overlap(md.g, static_cast<size_t>(md.d_out) * 4, md.out, nbytes))
+      return DORA_ERR_INVALID_ARG;
+    if ((md.d_out * eb) % 16 != 0 || !aligned16(md.base) || !aligned16(md.lora) ||
+        !aligned16(md.out) || !aligned16(md.g))
+      vec = false;
+  }
+  if (n_modules == 0) return DORA_OK;
+  if (!vec) {
+    for (int i = 0; i < n_modules; ++i) {
+      const dora_compose_module& md = modules[i];
+      const int st = dora_compose(md.base, md.lora, md.g, s, dtype, md.T, md.d_out, md.out, stream);
+      if (st != DORA_OK) return st;
+    }
+    return DORA_OK;
+  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < dora_compose_grouped_workspace_size(n_modules))
+    return DORA_ERR_WORKSPACE;
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  std::vector<ComposeModule> cm(n_modules);
+  int64_t units = 0;
+  for (int i = 0; i < n_modules; ++i) {
+    const dora_compose_module& md = modules[i];
+    cm[i] = ComposeModule{md.base, md.lora, md.g, md.out, md.T, md.d_out, units};
+    if (md.T > 0 && md.d_out > 0) units += compose_grouped_units(md.T, md.d_out, dtype == DORA_BF16);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DORA_TRY(cudaMemcpyAsync(workspace, cm.data(), sizeof(ComposeModule) * n_modules,
+                           cudaMemcpyHostToDevice, st));
+  return cuda_status(launch_compose_grouped(static_cast<const ComposeModule*>(workspace),
+                                            n_modules, units, s, dtype == DORA_BF16, dev.sms, st));
 }
 
 int dora_compose_train(const void* base, const void* lora, const float* g, float s, int dtype,

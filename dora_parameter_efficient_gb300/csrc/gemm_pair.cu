@@ -23,6 +23,8 @@
 //     N rows of the A / G' tile), so each SM stages 16 KB of W and only half
 //     of the [r x 64] A tile per K step;
 //   * the accumulator D [128 x r] of each CTA lives in its own tensor memory;
+//     for r <= 256 there are two of them, used by alternate work items, so
+//     the MMAs of an item run while the epilogue drains the previous one;
 //   * warp 0 of each CTA issues the TMA loads of its half; all loads of a
 //     stage complete on the even CTA's `full` barrier; the even CTA's MMA
 //     thread waits on it and, once the stage's MMAs are done, commits
@@ -51,6 +53,8 @@
 //     SM streaming W, extra prefetch requests only added traffic.
 // Every wait is bounded by %globaltimer; on expiry the kernel records a
 // timeout in the status word, stops issuing, drains what it issued and exits.
+#include <cstring>
+
 #include "common.cuh"
 #include "finalize.cuh"
 #include "ptx.cuh"
@@ -110,16 +114,63 @@ __device__ __forceinline__ uint4 ldg_keep_order(const uint16_t* p) {
   return v;
 }
 
-// Work item -> (pair tile, K segment, its K tile range).  Items are handed out
-// segment by segment and the segments shrink along K, so the long pieces of
-// work go first and the short ones fill in at the end (fewer idle pairs at
-// the finish); the last segment also holds the G' tiles.
-__device__ __forceinline__ void item_range(const PairParams& p, int item, int& tile, int& split,
+// What a work item needs to know about its module: the kernel parameters for
+// a single-module launch, one entry of the module table for a grouped one.
+struct ModView {
+  const CUtensorMap* tW;
+  const CUtensorMap* tA;
+  const CUtensorMap* tB;
+  const CUtensorMap* tGhi;
+  const CUtensorMap* tGlo;
+  const uint16_t* B;
+  const uint16_t* m;
+  float* wnorm;
+  float* g;
+  float* out_sumsq;
+  float* out_dot;
+  int* tile_done;
+  int rows, kt_w, pair_tiles, splits, item_begin;
+  const int* seg_k;
+};
+
+__device__ __forceinline__ ModView single_view(const PairParams& p, const CUtensorMap* tW,
+                                               const CUtensorMap* tA, const CUtensorMap* tB,
+                                               const CUtensorMap* tGhi, const CUtensorMap* tGlo) {
+  return ModView{tW, tA, tB, tGhi, tGlo, p.B, p.m, p.wnorm, p.g, p.out_sumsq, p.out_dot,
+                 p.tile_done, p.rows, p.kt_w, p.pair_tiles, p.splits, 0, p.seg_k};
+}
+
+// the module of a work item in a grouped launch (modules in item order)
+__device__ __forceinline__ ModView module_view(const PairParams& p, int item) {
+  int lo = 0, hi = p.n_mods - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.mods[mid].item_begin <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  const PairModule& md = p.mods[lo];
+  return ModView{&md.tW, &md.tA, &md.tB, &md.tGhi, &md.tGlo, md.B, md.m, md.wnorm, md.g,
+                 md.out_sumsq, md.out_dot, md.tile_done, md.rows, md.kt_w, md.pair_tiles,
+                 md.splits, md.item_begin, md.seg_k};
+}
+
+template <bool kGrouped>
+__device__ __forceinline__ ModView view_of(const PairParams& p, const ModView& single, int item) {
+  if constexpr (kGrouped) return module_view(p, item);
+  else return single;
+}
+
+// Work item -> (pair tile, K segment, its K tile range) inside its module.
+// Items are handed out segment by segment and the segments shrink along K,
+// so the long pieces of work go first and the short ones fill in at the end
+// (fewer idle pairs at the finish); the last segment also holds the G' tiles.
+__device__ __forceinline__ void item_range(const ModView& mv, int item, int& tile, int& split,
                                            int& kb, int& ke) {
-  split = item / p.pair_tiles;
-  tile = item - split * p.pair_tiles;
-  kb = p.seg_k[split];
-  ke = p.seg_k[split + 1];
+  item -= mv.item_begin;
+  split = item / mv.pair_tiles;
+  tile = item - split * mv.pair_tiles;
+  kb = mv.seg_k[split];
+  ke = mv.seg_k[split + 1];
 }
 
 // global fp32 load that bypasses L1 (data written by other CTAs of this grid)
@@ -152,10 +203,11 @@ __device__ __forceinline__ int read_item(uint32_t n, uint64_t* item_full, const 
   return item;
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tA,
                 const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tGhi,
-                const __grid_constant__ CUtensorMap tGlo, const PairParams p) {
+                const __grid_constant__ CUtensorMap tGlo, const __grid_constant__ PairParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -164,9 +216,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
   uint64_t* empty = full + p.stages;
   uint64_t* consumed = empty + p.stages;
-  uint64_t* accum_full = consumed + p.stages;
-  uint64_t* accum_empty = accum_full + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 1);
+  uint64_t* accum_full = consumed + p.stages;   // [2]: one per accumulator buffer
+  uint64_t* accum_empty = accum_full + 2;       // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   float* dot_half = reinterpret_cast<float*>(tmem_holder + 4);   // [2][128] second-half dots
   uint64_t* item_full = reinterpret_cast<uint64_t*>(dot_half + 256);
@@ -177,7 +229,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs, 1: its peer
-  const int n_items = p.pair_tiles * p.splits;
+  const int n_items = kGrouped ? p.n_items : p.pair_tiles * p.splits;
+  const ModView single = single_view(p, &tW, &tA, &tB, &tGhi, &tGlo);
   const uint32_t item_empty0 = map_to_rank(smem_u32(item_empty), 0);
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
@@ -187,8 +240,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(&empty[s], kPairEpiWarps);   // every epilogue warp has read the W tile
       mbar_init(&consumed[s], 1);            // the stage's MMAs are done
     }
-    mbar_init(accum_full, 1);
-    mbar_init(accum_empty, 16);     // 8 epilogue warps in each CTA of the pair
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accum_full[b], 1);
+      mbar_init(&accum_empty[b], 16);     // 8 epilogue warps in each CTA of the pair
+    }
     for (uint32_t i = 0; i < kItemRing; ++i) {
       mbar_init(&item_full[i], 1);
       mbar_init(&item_empty[i], kItemReaders);
@@ -196,7 +251,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (!kGrouped && warp == 0 && lane == 0) {
     tma_prefetch_desc(&tW);
     tma_prefetch_desc(&tA);
     tma_prefetch_desc(&tB);
@@ -248,8 +303,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
         }
         if (item < 0) break;
+        const ModView mv = view_of<kGrouped>(p, single, item);
+        if (kGrouped) {
+          tma_prefetch_desc(mv.tW);
+          tma_prefetch_desc(mv.tA);
+        }
         int tile, split, kb, ke;
-        item_range(p, item, tile, split, kb, ke);
+        item_range(mv, item, tile, split, kb, ke);
         const int row0 = tile * 256 + static_cast<int>(rank) * 128;
         for (int kt = kb; kt < ke; ++kt, ++it) {
           // the slot's previous use (parity phase ^ 1) must have been consumed
@@ -263,26 +323,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const CUtensorMap* xm;
           const CUtensorMap* ym;
           int kx;
-          if (kt < p.kt_w) {
-            xm = &tW; ym = &tA; kx = kt * kTcBlockK;
+          if (kt < mv.kt_w) {
+            xm = mv.tW; ym = mv.tA; kx = kt * kTcBlockK;
           } else {
             // a G' tile (an item may start in either half of the G' range)
             if (!g_ready) {
               griddep_wait();
               g_ready = true;
             }
-            xm = &tB;
-            if (kt < p.kt_w + p.kt_b) {
-              ym = &tGhi; kx = (kt - p.kt_w) * kTcBlockK;
+            xm = mv.tB;
+            if (kt < mv.kt_w + p.kt_b) {
+              ym = mv.tGhi; kx = (kt - mv.kt_w) * kTcBlockK;
             } else {
-              ym = &tGlo; kx = (kt - p.kt_w - p.kt_b) * kTcBlockK;
+              ym = mv.tGlo; kx = (kt - mv.kt_w - p.kt_b) * kTcBlockK;
             }
           }
           uint8_t* xs = smem + s * stage_bytes;
           uint8_t* ys = xs + kTcXTileBytes;
           const uint32_t bar0 = full0 + s * 8u;
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * stage_bytes);
-          tma_load_2d_pair(xs, xm, bar0, kx, row0, kt < p.kt_w ? pol_stream : pol_keep);
+          tma_load_2d_pair(xs, xm, bar0, kx, row0, kt < mv.kt_w ? pol_stream : pol_keep);
           // this CTA's half of each N chunk of the Y tile
           for (int c = 0; c < h0; c += p.y_box_rows)
             tma_load_2d_pair(ys + c * 128, ym, bar0, kx, static_cast<int>(rank) * h0 + c, pol_keep);
@@ -314,7 +374,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint32_t idesc0 = idesc_bf16_f32(256, p.n0);
       const uint32_t idesc1 = idesc_bf16_f32(256, p.n1 > 0 ? p.n1 : 16);
       const bool two = p.n1 > 0;
-      const uint32_t tmem1 = tmem_base + static_cast<uint32_t>(p.n0);
+      const uint32_t nbuf = static_cast<uint32_t>(p.acc_bufs);
       const uint64_t dx0 = smem_desc_sw128(smem_u32(smem));
       const uint64_t dy0 = smem_desc_sw128(smem_u32(smem) + kTcXTileBytes);
       const uint64_t dy1_off = static_cast<uint64_t>(p.n0 / 2) * 128u >> 4;
@@ -327,8 +387,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
         if (item < 0) break;
         int tile, split, kb, ke;
-        item_range(p, item, tile, split, kb, ke);
-        if (icount > 0 && !mbar_wait(accum_empty, (icount - 1) & 1, deadline)) {
+        item_range(view_of<kGrouped>(p, single, item), item, tile, split, kb, ke);
+        // accumulator buffer of this item, and how often it was used before
+        const uint32_t buf = static_cast<uint32_t>(icount) % nbuf;
+        const uint32_t use = static_cast<uint32_t>(icount) / nbuf;
+        const uint32_t acc0 = tmem_base + buf * p.acc_stride;
+        const uint32_t acc1 = acc0 + static_cast<uint32_t>(p.n0);
+        if (use > 0 && !mbar_wait(&accum_empty[buf], (use - 1) & 1u, deadline)) {
           // the accumulator was never drained: issue nothing more
           atomicExch(p.status, kStatusTimeout);
           *abort_flag = 1;
@@ -348,8 +413,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kTcBlockK / 16; ++ks) {
             const uint32_t acc = ks > 0 ? 1u : first;
-            umma_bf16_pair(tmem_base, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
-            if (two) umma_bf16_pair(tmem1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
+            umma_bf16_pair(acc0, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
+            if (two) umma_bf16_pair(acc1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
           }
           umma_commit_pair(&consumed[s], 0x3);
           if (++s == stages) {
@@ -358,11 +423,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           }
         }
         // both CTAs learn that this item's accumulator is complete
-        umma_commit_pair(accum_full, 0x3);
+        umma_commit_pair(&accum_full[buf], 0x3);
       }
       // do not leave tensor-core work in flight behind the final barrier
-      if (icount > 0 && !mbar_wait(accum_full, (icount - 1) & 1, global_timer_ns() + p.timeout_ns))
-        atomicExch(p.status, kStatusTimeout);
+      if (icount > 0) {
+        const uint32_t last = static_cast<uint32_t>(icount - 1);
+        if (!mbar_wait(&accum_full[last % nbuf], (last / nbuf) & 1u, global_timer_ns() + p.timeout_ns))
+          atomicExch(p.status, kStatusTimeout);
+      }
     }
   } else if (warp < 2 + kPairEpiWarps) {
     // -------------------------------------------------------------- epilogue (both CTAs)
@@ -375,6 +443,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const int trow = q * 32 + lane;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t accum_empty0 = map_to_rank(smem_u32(accum_empty), 0);
+    const uint32_t nbuf = static_cast<uint32_t>(p.acc_bufs);
     const int nchunk = (p.r + 31) / 32;              // 32-column chunks of the accumulator
     const int c_lo = h == 0 ? 0 : (nchunk + 1) / 2;
     const int c_hi = h == 0 ? (nchunk + 1) / 2 : nchunk;
@@ -409,12 +478,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             : "memory");
         if (!all_ok) break;
       }
+      const ModView mv = view_of<kGrouped>(p, single, item);
       int tile, split, kb, ke;
-      item_range(p, item, tile, split, kb, ke);
+      item_range(mv, item, tile, split, kb, ke);
       const int rowbase = tile * 256 + static_cast<int>(rank) * 128 + q * 32;
       const int grow = rowbase + lane;      // the row whose dot this lane computes
-      const bool valid = grow < p.rows;
-      const uint16_t* brow = p.B + static_cast<size_t>(valid ? grow : 0) * p.r;
+      const bool valid = grow < mv.rows;
+      const uint16_t* brow = mv.B + static_cast<size_t>(valid ? grow : 0) * p.r;
 
       float sacc[4], scmp[4];
 #pragma unroll
@@ -426,7 +496,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           *abort_flag = 1;
           alive = false;
         }
-        if (alive && kt < p.kt_w) {
+        if (alive && kt < mv.kt_w) {
           const uint32_t xa = smem0 + s * stage_bytes + x_off;
 #pragma unroll
           for (int r4 = 0; r4 < 4; ++r4) {
@@ -473,10 +543,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       {
         const int srow = rowbase + 16 * h + lane;
-        if (lane < 16 && srow < p.rows) p.out_sumsq[static_cast<size_t>(split) * p.rows + srow] = ss;
+        if (lane < 16 && srow < mv.rows) mv.out_sumsq[static_cast<size_t>(split) * mv.rows + srow] = ss;
       }
 
-      bool ok = alive && mbar_wait(accum_full, icount & 1, deadline);
+      const uint32_t buf = static_cast<uint32_t>(icount) % nbuf;
+      const uint32_t acc_row = tmem_row + buf * p.acc_stride;   // this item's accumulator
+      bool ok = alive && mbar_wait(&accum_full[buf], (static_cast<uint32_t>(icount) / nbuf) & 1u, deadline);
       if (alive && !ok) {
         atomicExch(p.status, kStatusTimeout);
         *abort_flag = 1;
@@ -506,10 +578,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           if (c < c_hi && c * 32 < rp) {
             float v[32];
             if (c * 32 + 32 <= rp) {
-              tmem_load_32cols(tmem_row + static_cast<uint32_t>(c * 32), v);
+              tmem_load_32cols(acc_row + static_cast<uint32_t>(c * 32), v);
             } else {          // only the first 16 columns of this chunk exist
               uint32_t rv[16];
-              tmem_load_16cols_async(tmem_row + static_cast<uint32_t>(c * 32), rv);
+              tmem_load_16cols_async(acc_row + static_cast<uint32_t>(c * 32), rv);
               tmem_wait_ld(rv);
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -527,7 +599,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           uint4 part[2];
           load_b_cols<2>(brow, col, p.r, valid, part);
           uint32_t rv[16];
-          tmem_load_16cols_async(tmem_row + static_cast<uint32_t>(col), rv);
+          tmem_load_16cols_async(acc_row + static_cast<uint32_t>(col), rv);
           tmem_wait_ld(rv);
           float v[16];
 #pragma unroll
@@ -538,21 +610,21 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // accumulator drained: let the even CTA start the next item's MMAs
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(accum_empty0);
+      if (lane == 0) mbar_arrive_cluster(accum_empty0 + buf * 8u);
       if (!ok) break;
       // first half + second half, in that order, for each row (the halves
       // alternate between two buffers, so one barrier per item suffices)
       float* dh = dot_half + (icount & 1) * 128;
       if (h == 1) dh[trow] = acc;
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
-      if (h == 0 && valid) p.out_dot[static_cast<size_t>(split) * p.rows + grow] = acc + dh[trow];
+      if (h == 0 && valid) mv.out_dot[static_cast<size_t>(split) * mv.rows + grow] = acc + dh[trow];
       // the last segment of this 128-row group to finish assembles wnorm and
       // g for its rows from the partials of every segment, in segment order
       __threadfence();
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (warp == 2 && lane == 0) {
-        const int prev = atomicAdd(p.tile_done + tile * 2 + static_cast<int>(rank), 1);
-        *last_flag = prev == p.splits - 1 ? 1 : 0;
+        const int prev = atomicAdd(mv.tile_done + tile * 2 + static_cast<int>(rank), 1);
+        *last_flag = prev == mv.splits - 1 ? 1 : 0;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (*last_flag && h == 0 && valid) {
@@ -560,17 +632,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // segment partials added in segment order, carried as double-floats
         df base{0.f, 0.f}, cross{0.f, 0.f};
 #pragma unroll 1
-        for (int i = 0; i < p.splits; ++i) {
+        for (int i = 0; i < mv.splits; ++i) {
           float e;
-          two_sum(base.hi, ld_cg_f(p.out_sumsq + static_cast<size_t>(i) * p.rows + grow), base.hi, e);
+          two_sum(base.hi, ld_cg_f(mv.out_sumsq + static_cast<size_t>(i) * mv.rows + grow), base.hi, e);
           base.lo = __fadd_rn(base.lo, e);
-          two_sum(cross.hi, ld_cg_f(p.out_dot + static_cast<size_t>(i) * p.rows + grow), cross.hi, e);
+          two_sum(cross.hi, ld_cg_f(mv.out_dot + static_cast<size_t>(i) * mv.rows + grow), cross.hi, e);
           cross.lo = __fadd_rn(cross.lo, e);
         }
         float wn, gv;
-        finalize_row(base, cross, nullptr, p.two_s, p.s_sq, bf16_to_f32(p.m[grow]), p.eps, wn, gv);
-        p.wnorm[grow] = wn;
-        p.g[grow] = gv;
+        finalize_row(base, cross, nullptr, p.two_s, p.s_sq, bf16_to_f32(mv.m[grow]), p.eps, wn, gv);
+        mv.wnorm[grow] = wn;
+        mv.g[grow] = gv;
       }
     }
   }
@@ -589,7 +661,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 size_t pair_smem_bytes(int n_pad, int stages) {
   const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
-  return 1024 + stage * stages + (3 * stages + 2) * 8 + 16 + 2 * 128 * 4 +
+  return 1024 + stage * stages + (3 * stages + 4) * 8 + 16 + 2 * 128 * 4 +
          2 * kItemRing * 8 + kItemRing * 4 + 4;
 }
 
@@ -622,9 +694,11 @@ int pair_max_clusters(size_t smem_bytes) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaFuncSetAttribute(k_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, k_gemm_pair, &cfg) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_gemm_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_gemm_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<false>, &cfg) != cudaSuccess)
     return 0;
   if (dev < 64) cached[dev] = n;
   return n;
@@ -649,7 +723,32 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair, tW, tA, tB, tGhi, tGlo, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair<false>, tW, tA, tB, tGhi, tGlo, p);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Grouped launch: the tensor maps live in the module table (device memory);
+// the kernel's map parameters are placeholders it never reads.
+cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  CUtensorMap none;
+  std::memset(&none, 0, sizeof(none));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair<true>, none, none, none, none, none, p);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -22,6 +22,8 @@
 // memory and no second kernel.  G'_hi = bf16(G'), G'_lo = bf16(G' - G'_hi),
 // G' = (s/2) G rounded once to fp32: the two bf16 terms carry about 16
 // significant bits of G' into the tensor core.
+#include <cstring>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -31,7 +33,6 @@ namespace {
 
 constexpr int kGramThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 TMEM -> shared memory
 constexpr int kGramTileBytes = 128 * 128;   // [128 rows x 64 bf16] with the 128-byte swizzle
-constexpr int kGramMaxCluster = 16;         // CTAs per cluster (16 needs the non-portable opt-in)
 
 // bulk copy of `bytes` from this CTA's shared memory into a cluster peer's,
 // completion (bytes) counted on the peer's mbarrier
@@ -59,9 +60,27 @@ __device__ __forceinline__ void gram_block(int b, int nb, int& bi, int& bj) {
   bj = i + b;
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kGramThreads, 1)
-    k_gram(const __grid_constant__ CUtensorMap tAx, const __grid_constant__ CUtensorMap tAy,
-           const GramParams p) {
+    k_gram(const __grid_constant__ CUtensorMap tAx_param, const __grid_constant__ CUtensorMap tAy_param,
+           const GramParams p_in, const GramModule* mods) {
+  // the module of this cluster (grouped) or the kernel parameters
+  GramParams p = p_in;
+  const CUtensorMap* tAxp = &tAx_param;
+  const CUtensorMap* tAyp = &tAy_param;
+  int block_base = 0;
+  if constexpr (kGrouped) {
+    const int per_module = p_in.nb * (p_in.nb + 1) / 2 * static_cast<int>(p_in.cluster);
+    const int mi = static_cast<int>(blockIdx.x) / per_module;
+    block_base = mi * per_module;
+    tAxp = &mods[mi].tAx;
+    tAyp = &mods[mi].tAy;
+    p.G_hi = mods[mi].G_hi;
+    p.G_lo = mods[mi].G_lo;
+    p.k_tiles = mods[mi].k_tiles;
+  }
+  const CUtensorMap& tAx = *tAxp;
+  const CUtensorMap& tAy = *tAyp;
   // the main pass queued behind this kernel may start launching; it waits
   // for this grid to finish before it reads G'
   griddep_launch_dependents();
@@ -93,7 +112,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   const uint32_t q = cluster_ctarank();
   const uint32_t C = p.cluster;
   int bi, bj;
-  gram_block(static_cast<int>(blockIdx.x / C), p.nb, bi, bj);
+  gram_block(static_cast<int>((blockIdx.x - block_base) / C), p.nb, bi, bj);
   const int kt_begin = static_cast<int>((static_cast<long long>(p.k_tiles) * q) / C);
   const int kt_end = static_cast<int>((static_cast<long long>(p.k_tiles) * (q + 1)) / C);
   const int n_iter = kt_end - kt_begin;
@@ -328,24 +347,34 @@ size_t gram_smem_bytes(int bw, int stages) {
   return 1024 + (ring > part ? ring : part) + (2 * stages + 2) * 8 + 16;
 }
 
-cudaError_t launch_gram(const CUtensorMap& tAx, const CUtensorMap& tAy, const GramParams& p,
-                        cudaStream_t stream) {
-  const size_t smem = gram_smem_bytes(p.bw, p.stages);
+namespace {
+
+cudaError_t gram_configure() {
   static int configured_for[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured_for[dev]) {
-    e = cudaFuncSetAttribute(k_gram, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_gram, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {k_gram<false>, k_gram<true>}) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     configured_for[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+template <bool kGrouped>
+cudaError_t gram_launch(const CUtensorMap& tAx, const CUtensorMap& tAy, const GramParams& p,
+                        const GramModule* mods, int n_mods, cudaStream_t stream) {
+  cudaError_t e = gram_configure();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.nb * (p.nb + 1) / 2 * p.cluster), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.nb * (p.nb + 1) / 2 * p.cluster * n_mods), 1, 1);
   cfg.blockDim = dim3(kGramThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = gram_smem_bytes(p.bw, p.stages);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -354,10 +383,24 @@ cudaError_t launch_gram(const CUtensorMap& tAx, const CUtensorMap& tAy, const Gr
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_gram, tAx, tAy, p);
+  e = cudaLaunchKernelEx(&cfg, k_gram<kGrouped>, tAx, tAy, p, mods);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gram(const CUtensorMap& tAx, const CUtensorMap& tAy, const GramParams& p,
+                        cudaStream_t stream) {
+  return gram_launch<false>(tAx, tAy, p, nullptr, 1, stream);
+}
+
+cudaError_t launch_gram_grouped(const GramModule* mods, int n_mods, const GramParams& p,
+                                cudaStream_t stream) {
+  CUtensorMap none;
+  std::memset(&none, 0, sizeof(none));
+  return gram_launch<true>(none, none, p, mods, n_mods, stream);
 }
 
 }  // namespace dora

@@ -174,6 +174,68 @@ int dora_compose(const void* base, const void* lora, const float* g, float s,
                  int dtype, int64_t T, int64_t d_out, void* out, void* stream);
 
 /*
+ * Grouped calls: one launch sequence for a whole stack of adapted modules
+ * (the Chinese write-up, sections 2.2 and 4.2, notes that launch latency
+ * dominates small shapes such as the 512-row KV projections).  Results are
+ * those of the per-module calls, up to the order of fp32 sums.
+ */
+
+/* One module of a grouped norm: the dora_factored_norm arguments that differ
+ * per module (same meaning, layout and requirements). */
+typedef struct dora_norm_module {
+    const void* W;        /* [d_out x d_in] */
+    const void* A;        /* [r x d_in] */
+    const void* B;        /* [d_out x r] */
+    const void* m;        /* [d_out] */
+    float* wnorm;         /* [d_out] output */
+    float* g;             /* [d_out] output */
+    int64_t d_out;
+    int64_t d_in;
+} dora_norm_module;
+
+/* Bytes of workspace for dora_factored_norm_grouped over these modules
+ * (0 for an invalid argument). */
+size_t dora_norm_grouped_workspace_size(const dora_norm_module* modules, int n_modules,
+                                        int64_t r, int dtype);
+
+/*
+ * dora_factored_norm for every module of `modules`, all with the same rank r,
+ * dtype, s and eps.  bf16 inputs run as one Gram launch and one persistent
+ * main-pass launch over the work items of all modules; other cases call the
+ * per-module path in turn.  The module table is read from host memory during
+ * the call (copied to the workspace), so the array may be freed on return.
+ * workspace: dora_norm_grouped_workspace_size bytes, 256-byte aligned, no
+ * initialisation needed.  Errors as dora_factored_norm (the first invalid
+ * module makes the call return before anything is enqueued).
+ */
+int dora_factored_norm_grouped(const dora_norm_module* modules, int n_modules, int dtype,
+                               int64_t r, float s, float eps, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* One module of a grouped compose: the dora_compose arguments that differ per
+ * module. */
+typedef struct dora_compose_module {
+    const void* base;     /* [T x d_out] */
+    const void* lora;     /* [T x d_out] */
+    const float* g;       /* [d_out] */
+    void* out;            /* [T x d_out] output */
+    int64_t T;
+    int64_t d_out;
+} dora_compose_module;
+
+/* Bytes of workspace for dora_compose_grouped over n_modules modules. */
+size_t dora_compose_grouped_workspace_size(int n_modules);
+
+/*
+ * dora_compose for every module, one launch when every module has 16-byte
+ * rows and 16-byte aligned pointers (else one dora_compose per module).
+ * Same s and dtype for all.  workspace: dora_compose_grouped_workspace_size
+ * bytes, 256-byte aligned.
+ */
+int dora_compose_grouped(const dora_compose_module* modules, int n_modules, float s, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Training path of the compose ("Scaling DoRA", Chinese write-up sections
  * 2.2, 4.2 and 5.2: the fused backward tier).  The norm is a detached
  * constant in the backward (section 1.2.2), so with g = m / max(wnorm, eps)
