@@ -238,6 +238,71 @@ def run_reference(args):
 BASELINE_METRIC = json.dumps("factored-norm TFLOP/s + compose GB/s (% of GB300 peak) at 8192², r=384")
 
 
+# ---------------------------------------------------------------- the stack workload
+def run_stack(api, dev, peaks, steps=10):
+    """Grouped norm + compose over the 196 modules of the 7B-like stack."""
+    import torch
+    cfg = configs.get(4)
+    gen_t = torch.Generator(device=dev)
+    gen_t.manual_seed(4)
+    mods = []
+    for m in cfg.modules:
+        def rnd(*shape, std):
+            return (torch.randn(*shape, device=dev, generator=gen_t) * std).to(torch.bfloat16)
+        mods.append(dict(
+            W=rnd(m.d_out, m.d_in, std=cfg.std_w), A=rnd(cfg.r, m.d_in, std=cfg.std_a(m.d_in)),
+            B=rnd(m.d_out, cfg.r, std=cfg.std_b),
+            m=torch.ones(m.d_out, dtype=torch.bfloat16, device=dev),
+            base=rnd(cfg.tokens, m.d_out, std=cfg.std_base),
+            lora=rnd(cfg.tokens, m.d_out, std=cfg.std_lora),
+            wn=torch.empty(m.d_out, dtype=torch.float32, device=dev),
+            g=torch.empty(m.d_out, dtype=torch.float32, device=dev), mod=m))
+        mods[-1]["out"] = torch.empty_like(mods[-1]["base"])
+    norm_mods = [(d["W"], d["A"], d["B"], d["m"]) for d in mods]
+    comp_mods = [(d["base"], d["lora"], d["g"]) for d in mods]
+    wns, gss, outs = [d["wn"] for d in mods], [d["g"] for d in mods], [d["out"] for d in mods]
+    nws = torch.empty(api.norm_grouped_workspace_size(norm_mods, torch.bfloat16),
+                      dtype=torch.uint8, device=dev)
+    cws = torch.empty(65536, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        api.dora_factored_norm_grouped(norm_mods, cfg.s, cfg.eps, wnorms=wns, gs=gss, workspace=nws)
+        if evs is not None:
+            evs[1].record(stream)
+        api.dora_compose_grouped(comp_mods, cfg.s, outs=outs, workspace=cws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in evs:
+        e[0].record(stream)
+        step(e)
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    norm_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in evs)
+    comp_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in evs)
+    nbytes = sum(configs.norm_bytes(d["mod"].d_out, d["mod"].d_in, cfg.r, cfg.dtype) for d in mods)
+    nflops = sum(configs.norm_flops(d["mod"].d_out, d["mod"].d_in, cfg.r) for d in mods)
+    cbytes = sum(configs.compose_bytes(cfg.tokens, d["mod"].d_out, cfg.dtype) for d in mods)
+    out = {"workload": cfg.name, "modules": len(mods), "r": cfg.r, "tokens": cfg.tokens,
+           "norm_ms": norm_ms, "norm_GB/s": nbytes / (norm_ms * 1e-3) / 1e9,
+           "norm_frac_of_measured_hbm": nbytes / (norm_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+           "norm_TFLOP/s": nflops / (norm_ms * 1e-3) / 1e12,
+           "compose_ms": comp_ms, "compose_GB/s": cbytes / (comp_ms * 1e-3) / 1e9,
+           "compose_frac_of_measured_hbm": cbytes / (comp_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+           "modules_per_s": len(mods) / ((norm_ms + comp_ms) * 1e-3),
+           "calls": "dora_factored_norm_grouped + dora_compose_grouped, one launch sequence "
+                    "for all 196 modules",
+           "data": "drawn on the device (torch.randn, seeded) with the config's distributions; "
+                   "m = 1 (timing only)",
+           "timing": f"CUDA events, mean over {steps} steps"}
+    del mods, norm_mods, comp_mods, nws
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -436,6 +501,12 @@ def run_ours(args):
                   f"{N_SETS} rotating input sets",
     }
 
+    # ---- the 7B-like stack (196 modules, r = 128): grouped norm + compose,
+    # one launch sequence per step for all modules; inputs drawn on the
+    # device with the config's distributions (m = 1: timing only; the parity
+    # of the grouped calls is in tests/test_grouped_gpu.py)
+    stack = run_stack(api, dev, peaks) if not args.no_stack else None
+
     # ---- end to end through the public API, from pinned host buffers
     e2e_steps = max(3, min(args.steps, 20))
     host = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -530,6 +601,7 @@ def run_ours(args):
                         "frac_of_nominal_hbm": comp_gbs / world / NOMINAL["hbm_gbs"]},
             "roofline": roofline, "roofline_compose": roofline_compose,
             "compose_training": compose_training,
+            "stack": stack,
             "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
             "cpu_baseline": cpu_baseline,
         }
@@ -547,6 +619,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
