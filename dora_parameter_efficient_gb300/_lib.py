@@ -55,6 +55,11 @@ SIGNATURES = {
     "dora_factored_norm_grouped": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _I64,
                                                   ctypes.c_float, ctypes.c_float, _P,
                                                   ctypes.c_size_t, _P]),
+    "dora_norm_grouped_plan_create": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _I64, _P,
+                                                     ctypes.c_size_t, _P,
+                                                     ctypes.POINTER(_P)]),
+    "dora_norm_grouped_plan_run": (ctypes.c_int, [_P, ctypes.c_float, ctypes.c_float, _P]),
+    "dora_norm_grouped_plan_destroy": (None, [_P]),
     "dora_compose_grouped_workspace_size": (ctypes.c_size_t, [ctypes.c_int]),
     "dora_compose_grouped": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_float, ctypes.c_int, _P,
                                             ctypes.c_size_t, _P]),

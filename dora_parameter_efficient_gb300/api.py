@@ -6,6 +6,7 @@ events; nothing here computes on tensor values.
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional, Tuple
 
 import torch
@@ -129,14 +130,9 @@ def norm_grouped_workspace_size(modules, dtype: torch.dtype) -> int:
     return int(_lib.load().dora_norm_grouped_workspace_size(table, len(modules), r, _DTYPES[dtype]))
 
 
-def dora_factored_norm_grouped(modules, s: float, eps: float, wnorms=None, gs=None,
-                               workspace: Optional[torch.Tensor] = None,
-                               stream: Optional[torch.cuda.Stream] = None):
-    """dora_factored_norm for a list of modules (W, A, B, m), all of one rank and
-    dtype, in one launch sequence; returns the lists (wnorms, gs)."""
-    modules = list(modules)
-    if not modules:
-        return [], []
+def _grouped_norm_args(modules, wnorms, gs, workspace):
+    """Checks a grouped norm's modules and allocates what the caller left out;
+    returns (dtype code, r, wnorms, gs, workspace)."""
     W0, A0 = modules[0][0], modules[0][1]
     code = _dtype_code(W0)
     r = A0.shape[0]
@@ -148,18 +144,85 @@ def dora_factored_norm_grouped(modules, s: float, eps: float, wnorms=None, gs=No
             raise ValueError("shape mismatch in a grouped module (one rank for all modules)")
     dev = W0.device
     wnorms = [torch.empty(W.shape[0], dtype=torch.float32, device=dev) for W, *_ in modules] \
-        if wnorms is None else wnorms
+        if wnorms is None else list(wnorms)
     gs = [torch.empty(W.shape[0], dtype=torch.float32, device=dev) for W, *_ in modules] \
-        if gs is None else gs
+        if gs is None else list(gs)
     if workspace is None:
         workspace = torch.empty(max(256, norm_grouped_workspace_size(modules, W0.dtype)),
                                 dtype=torch.uint8, device=dev)
+    return code, r, wnorms, gs, workspace
+
+
+def dora_factored_norm_grouped(modules, s: float, eps: float, wnorms=None, gs=None,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream: Optional[torch.cuda.Stream] = None):
+    """dora_factored_norm for a list of modules (W, A, B, m), all of one rank and
+    dtype, in one launch sequence; returns the lists (wnorms, gs)."""
+    modules = list(modules)
+    if not modules:
+        return [], []
+    code, r, wnorms, gs, workspace = _grouped_norm_args(modules, wnorms, gs, workspace)
     table = _norm_table(modules, wnorms, gs)
     st = _lib.load().dora_factored_norm_grouped(table, len(modules), code, r, float(s),
                                                 float(eps), _dev(workspace, "workspace"),
                                                 workspace.numel(), _stream_handle(stream))
     check(st, "dora_factored_norm_grouped")
     return wnorms, gs
+
+
+class NormGroupedPlan:
+    """A dora_norm_grouped_plan: the grouped norm over fixed module buffers,
+    prepared once.  It keeps every tensor it refers to (the modules, the
+    outputs and the workspace) alive until destroy()."""
+
+    def __init__(self, handle, modules, wnorms, gs, workspace):
+        self._handle = handle
+        self._keep = (modules, workspace)
+        self.wnorms = wnorms
+        self.gs = gs
+
+    def run(self, s: float, eps: float, stream: Optional[torch.cuda.Stream] = None):
+        """dora_norm_grouped_plan_run: writes (and returns) the lists (wnorms, gs)."""
+        if self._handle is None:
+            raise RuntimeError("dora_norm_grouped_plan_run on a destroyed plan")
+        st = _lib.load().dora_norm_grouped_plan_run(self._handle, float(s), float(eps),
+                                                    _stream_handle(stream))
+        check(st, "dora_norm_grouped_plan_run")
+        return self.wnorms, self.gs
+
+    def destroy(self):
+        """dora_norm_grouped_plan_destroy, after the device has finished every run."""
+        if self._handle is not None:
+            torch.cuda.synchronize(self._keep[1].device)
+            _lib.load().dora_norm_grouped_plan_destroy(self._handle)
+            self._handle = None
+            self._keep = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def dora_norm_grouped_plan_create(modules, wnorms=None, gs=None,
+                                  workspace: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None) -> NormGroupedPlan:
+    """Prepares the grouped norm of `modules` (W, A, B, m) once; the returned
+    plan's run(s, eps) is dora_factored_norm_grouped without the per-call
+    host work.  The tensors must keep their storage (update them in place)."""
+    modules = [tuple(m) for m in modules]
+    if not modules:
+        raise ValueError("a grouped norm plan needs at least one module")
+    code, r, wnorms, gs, workspace = _grouped_norm_args(modules, wnorms, gs, workspace)
+    table = _norm_table(modules, wnorms, gs)
+    handle = ctypes.c_void_p()
+    st = _lib.load().dora_norm_grouped_plan_create(table, len(modules), code, r,
+                                                   _dev(workspace, "workspace"),
+                                                   workspace.numel(), _stream_handle(stream),
+                                                   ctypes.byref(handle))
+    check(st, "dora_norm_grouped_plan_create")
+    return NormGroupedPlan(handle, modules, wnorms, gs, workspace)
 
 
 def dora_compose_grouped(modules, s: float, outs=None, workspace: Optional[torch.Tensor] = None,

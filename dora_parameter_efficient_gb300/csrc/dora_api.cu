@@ -3,10 +3,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "dora.h"
@@ -429,13 +431,27 @@ struct GroupedPlan {
 
 bool grouped_fused(int dtype, int64_t r, float s) { return dtype == DORA_BF16 && r > 0 && s != 0.f; }
 
+// Workspace of a grouped norm: the control words and the module tables of the
+// one-launch path first, then either that path's per-module regions (G'
+// halves, partial sums) or, for the per-module path, one dora_factored_norm
+// workspace per module.  The tables come before both, so a prepared plan
+// keeps them whichever path a run takes.
 GroupedPlan make_grouped_plan(const dora_norm_module* mods, int n, int64_t r, int dtype,
                               bool fused) {
   GroupedPlan gp;
   gp.fused = fused;
-  size_t off = 0;
+  int words = kCtlTileDone;
+  for (int i = 0; i < n; ++i) {
+    gp.tile_done_word.push_back(words);
+    words += 2 * static_cast<int>(ceil_div(mods[i].d_out, 2 * kTcBlockM));
+  }
+  size_t off = align_up(static_cast<size_t>(words) * 4, 256);
+  gp.zero_bytes = off;
+  gp.off_pmods = off;
+  off = align_up(off + sizeof(PairModule) * n, 256);
+  gp.off_gmods = off;
+  off = align_up(off + sizeof(GramModule) * n, 256);
   if (!fused) {
-    // the per-module path, each module with its own workspace
     for (int i = 0; i < n; ++i) {
       gp.off_single.push_back(off);
       off = align_up(off + make_plan(mods[i].d_out, mods[i].d_in, r, dtype).total, 256);
@@ -444,17 +460,6 @@ GroupedPlan make_grouped_plan(const dora_norm_module* mods, int n, int64_t r, in
     return gp;
   }
   const int rp = static_cast<int>(ceil_div(r, 16) * 16);
-  int words = kCtlTileDone;
-  for (int i = 0; i < n; ++i) {
-    gp.tile_done_word.push_back(words);
-    words += 2 * static_cast<int>(ceil_div(mods[i].d_out, 2 * kTcBlockM));
-  }
-  off = align_up(static_cast<size_t>(words) * 4, 256);
-  gp.zero_bytes = off;
-  gp.off_pmods = off;
-  off = align_up(off + sizeof(PairModule) * n, 256);
-  gp.off_gmods = off;
-  off = align_up(off + sizeof(GramModule) * n, 256);
   const size_t rp2 = static_cast<size_t>(rp) * rp;
   for (int i = 0; i < n; ++i) {
     const int ktot = static_cast<int>(ceil_div(mods[i].d_in, kTcBlockK) + 2 * ceil_div(r, kTcBlockK));
@@ -500,59 +505,92 @@ int check_module(const dora_norm_module& md, int64_t r, int dtype, float s, floa
   return DORA_OK;
 }
 
-int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, int64_t r, float s,
-                               float eps, void* workspace, size_t workspace_bytes, void* stream_v) {
-  if (n < 0 || (n > 0 && !mods)) return DORA_ERR_INVALID_ARG;
+// A grouped norm prepared once: the module list, the two workspace layouts
+// and, when every module can take the one-launch path, its tables written to
+// the workspace.  A run then only zeroes the control words and launches.
+struct NormGroupedPlan {
+  std::vector<dora_norm_module> mods;
+  int dtype = 0;
+  int64_t r = 0;
+  uint8_t* ws = nullptr;
+  size_t ws_bytes = 0;
+  int device = -1;
+  bool tables = false;  // the one-launch tables are in the workspace
+  GroupedPlan fused_gp, single_gp;
+  int n_items = 0, min_kt = 0;
+};
+
+// Whether the modules can take the one-launch path for some s != 0.
+bool modules_fusable(const dora_norm_module* mods, int n, int64_t r, int dtype) {
+  if (!grouped_fused(dtype, r, 1.f)) return false;
   for (int i = 0; i < n; ++i) {
-    const int st = check_module(mods[i], r, dtype, s, eps);
-    if (st != DORA_OK) return st;
+    const dora_norm_module& md = mods[i];
+    if (md.d_out == 0 || md.d_in == 0 || !md.A || !md.B) return false;
+    if (!aligned16(md.A) || !aligned16(md.B)) return false;
   }
+  return true;
+}
+
+// Host checks, layouts and (with write_tables) the one-launch tables, encoded
+// and copied to the workspace on `stream`.
+int grouped_prepare(const dora_norm_module* mods, int n, int dtype, int64_t r, void* workspace,
+                    size_t workspace_bytes, bool write_tables, cudaStream_t stream,
+                    NormGroupedPlan* P) {
+  if (n < 0 || (n > 0 && !mods)) return DORA_ERR_INVALID_ARG;
+  P->mods.assign(mods, mods + n);
+  P->dtype = dtype;
+  P->r = r;
+  P->ws = static_cast<uint8_t*>(workspace);
+  P->ws_bytes = workspace_bytes;
+  P->tables = false;
   if (n == 0) return DORA_OK;
-  // modules with work on the tensor-core path (d_out, d_in > 0)
-  bool fused = grouped_fused(dtype, r, s);
-  for (int i = 0; i < n; ++i)
-    if (mods[i].d_out == 0 || mods[i].d_in == 0) fused = false;
-  const GroupedPlan gp = make_grouped_plan(mods, n, r, dtype, fused);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < gp.total)
-    return DORA_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (!fused) {
-    for (int i = 0; i < n; ++i) {
-      const dora_norm_module& md = mods[i];
-      const int st = factored_norm_impl(md.W, md.A, md.B, dtype, md.d_out, md.d_in, r, s, md.m,
-                                        eps, md.wnorm, md.g, ws + gp.off_single[i],
-                                        workspace_bytes - gp.off_single[i], stream_v, nullptr,
-                                        nullptr);
-      if (st != DORA_OK) return st;
-    }
-    return DORA_OK;
+  const bool fusable = modules_fusable(mods, n, r, dtype);
+  P->single_gp = make_grouped_plan(mods, n, r, dtype, false);
+  size_t need = P->single_gp.total;
+  if (fusable) {
+    P->fused_gp = make_grouped_plan(mods, n, r, dtype, true);
+    if (P->fused_gp.total > need) need = P->fused_gp.total;
   }
-  DeviceInfo dev;
-  const int dst = current_device_info(&dev);
-  if (dst != DORA_OK) return dst;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return DORA_ERR_WORKSPACE;
+  DORA_TRY(cudaGetDevice(&P->device));
+  if (!fusable || !write_tables) return DORA_OK;
+
+  const GroupedPlan& gp = P->fused_gp;
+  uint8_t* ws = P->ws;
   int* status = reinterpret_cast<int*>(ws);
   const int rp = static_cast<int>(ceil_div(r, 16) * 16);
-  const int gnb = gram_nb(rp), gbw = gram_bw(rp);
-  const uint32_t tmem_cols = [&] {
-    uint32_t c = 32;
-    while (c < static_cast<uint32_t>(rp)) c <<= 1;
-    return c;
-  }();
+  const int gbw = gram_bw(rp);
   const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
   const int n1 = rp - n0;
   const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
   const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
 
+  // K segments only when the pair tiles of all modules are too few to fill
+  // the persistent grid a few times over; a stack of many modules fills it
+  // with whole-K items, each one accumulator drain.
+  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pair_pick_stages(rp)));
+  if (clusters_max <= 0) return DORA_ERR_CUDA;
+  int64_t total_pairs = 0;
+  for (int i = 0; i < n; ++i) total_pairs += ceil_div(mods[i].d_out, 2 * kTcBlockM);
+  const bool split_k = total_pairs < 4 * static_cast<int64_t>(clusters_max);
+  // Items are numbered module by module in this order: longest K first, so
+  // that the last items the persistent grid takes are short ones.
+  std::vector<int> order(n);
+  for (int i = 0; i < n; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int a, int b) { return mods[a].d_in > mods[b].d_in; });
+
   std::vector<PairModule> pm(n);
   std::vector<GramModule> gm(n);
   int min_kt = 1 << 30;
   int item = 0;
-  for (int i = 0; i < n; ++i) {
+  for (int j = 0; j < n; ++j) {
+    const int i = order[j];
     const dora_norm_module& md = mods[i];
     uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + gp.off_ghi[i]);
     uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + gp.off_glo[i]);
-    PairModule& p = pm[i];
+    PairModule& p = pm[j];
     std::memset(&p, 0, sizeof(p));
     if (!make_map_bf16(&p.tW, md.W, md.d_in, md.d_out, kTcBlockM) ||
         !make_map_bf16(&p.tA, md.A, md.d_in, r, y_box2) ||
@@ -569,7 +607,13 @@ int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, i
     p.rows = static_cast<int>(md.d_out);
     p.kt_w = static_cast<int>(ceil_div(md.d_in, kTcBlockK));
     p.pair_tiles = static_cast<int>(ceil_div(md.d_out, 2 * kTcBlockM));
-    plan_module_segments(p.kt_w + 2 * kt_b, p.seg_k, &p.splits);
+    if (split_k) {
+      plan_module_segments(p.kt_w + 2 * kt_b, p.seg_k, &p.splits);
+    } else {
+      p.seg_k[0] = 0;
+      p.seg_k[1] = p.kt_w + 2 * kt_b;
+      p.splits = 1;
+    }
     p.item_begin = item;
     item += p.pair_tiles * p.splits;
     GramModule& q = gm[i];
@@ -582,20 +626,69 @@ int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, i
     q.k_tiles = p.kt_w;
     if (p.kt_w < min_kt) min_kt = p.kt_w;
   }
-  PairModule* pm_dev = reinterpret_cast<PairModule*>(ws + gp.off_pmods);
-  GramModule* gm_dev = reinterpret_cast<GramModule*>(ws + gp.off_gmods);
+  // pageable sources: the copies have read them when the calls return
+  DORA_TRY(cudaMemcpyAsync(ws + gp.off_pmods, pm.data(), sizeof(PairModule) * n,
+                           cudaMemcpyHostToDevice, stream));
+  DORA_TRY(cudaMemcpyAsync(ws + gp.off_gmods, gm.data(), sizeof(GramModule) * n,
+                           cudaMemcpyHostToDevice, stream));
+  P->tables = true;
+  P->n_items = item;
+  P->min_kt = min_kt;
+  return DORA_OK;
+}
+
+// One pass of a prepared grouped norm with these s and eps.
+int grouped_run(const NormGroupedPlan& P, float s, float eps, cudaStream_t stream) {
+  const int n = static_cast<int>(P.mods.size());
+  const int64_t r = P.r;
+  const int dtype = P.dtype;
+  for (int i = 0; i < n; ++i) {
+    const int st = check_module(P.mods[i], r, dtype, s, eps);
+    if (st != DORA_OK) return st;
+  }
+  if (n == 0) return DORA_OK;
+  int cur = -1;
+  DORA_TRY(cudaGetDevice(&cur));
+  if (cur != P.device) return DORA_ERR_INVALID_ARG;
+  if (!(P.tables && grouped_fused(dtype, r, s))) {
+    const GroupedPlan& gp = P.single_gp;
+    for (int i = 0; i < n; ++i) {
+      const dora_norm_module& md = P.mods[i];
+      const int st = factored_norm_impl(md.W, md.A, md.B, dtype, md.d_out, md.d_in, r, s, md.m,
+                                        eps, md.wnorm, md.g, P.ws + gp.off_single[i],
+                                        P.ws_bytes - gp.off_single[i], stream, nullptr, nullptr);
+      if (st != DORA_OK) return st;
+    }
+    return DORA_OK;
+  }
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  const GroupedPlan& gp = P.fused_gp;
+  int* status = reinterpret_cast<int*>(P.ws);
+  const int rp = static_cast<int>(ceil_div(r, 16) * 16);
+  const int gnb = gram_nb(rp), gbw = gram_bw(rp);
+  const uint32_t tmem_cols = [&] {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(rp)) c <<= 1;
+    return c;
+  }();
+  const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
+  const int n1 = rp - n0;
+  const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
+  const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+  const PairModule* pm_dev = reinterpret_cast<const PairModule*>(P.ws + gp.off_pmods);
+  const GramModule* gm_dev = reinterpret_cast<const GramModule*>(P.ws + gp.off_gmods);
   DORA_TRY(cudaMemsetAsync(status, 0, gp.zero_bytes, stream));
-  DORA_TRY(cudaMemcpyAsync(pm_dev, pm.data(), sizeof(PairModule) * n, cudaMemcpyHostToDevice, stream));
-  DORA_TRY(cudaMemcpyAsync(gm_dev, gm.data(), sizeof(GramModule) * n, cudaMemcpyHostToDevice, stream));
 
   GramParams pg{};
   pg.nb = gnb;
   pg.bw = gbw;
   pg.rp = rp;
-  pg.k_tiles = min_kt;
+  pg.k_tiles = P.min_kt;
   pg.stages = kGramStages;
   pg.cluster = kGramCluster;
-  while (pg.cluster > 1 && pg.cluster > min_kt) pg.cluster >>= 1;
+  while (pg.cluster > 1 && pg.cluster > P.min_kt) pg.cluster >>= 1;
   pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
   pg.scale = 0.5f * s;
   pg.status = status;
@@ -622,10 +715,26 @@ int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, i
   pp.timeout_ns = kDefaultTimeoutNs;
   pp.mods = pm_dev;
   pp.n_mods = n;
-  pp.n_items = item;
-  const int clusters = item < clusters_max ? item : clusters_max;
+  pp.n_items = P.n_items;
+  const int clusters = P.n_items < clusters_max ? P.n_items : clusters_max;
   DORA_TRY(launch_gemm_pair_grouped(pp, clusters, stream));
   return DORA_OK;
+}
+
+int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, int64_t r, float s,
+                               float eps, void* workspace, size_t workspace_bytes, void* stream_v) {
+  if (n < 0 || (n > 0 && !mods)) return DORA_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const int st = check_module(mods[i], r, dtype, s, eps);
+    if (st != DORA_OK) return st;
+  }
+  if (n == 0) return DORA_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  NormGroupedPlan P;
+  const int st = grouped_prepare(mods, n, dtype, r, workspace, workspace_bytes,
+                                 grouped_fused(dtype, r, s), stream, &P);
+  if (st != DORA_OK) return st;
+  return grouped_run(P, s, eps, stream);
 }
 
 // ---------------------------------------------------------------- allocation-free variant
@@ -737,6 +846,43 @@ int dora_factored_norm_grouped(const dora_norm_module* modules, int n_modules, i
   return factored_norm_grouped_impl(modules, n_modules, dtype, r, s, eps, workspace,
                                     workspace_bytes, stream);
 }
+
+struct dora_norm_grouped_plan_s {
+  NormGroupedPlan plan;
+};
+
+int dora_norm_grouped_plan_create(const dora_norm_module* modules, int n_modules, int dtype,
+                                  int64_t r, void* workspace, size_t workspace_bytes,
+                                  void* stream, dora_norm_grouped_plan* plan) {
+  if (!plan) return DORA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  if (n_modules < 0 || (n_modules > 0 && !modules)) return DORA_ERR_INVALID_ARG;
+  // the checks of a run that do not depend on s and eps (a module without
+  // adapter pointers is still accepted: it runs with s = 0)
+  for (int i = 0; i < n_modules; ++i) {
+    const int st = check_module(modules[i], r, dtype, 0.f, 1.f);
+    if (st != DORA_OK) return st;
+  }
+  dora_norm_grouped_plan_s* h = new (std::nothrow) dora_norm_grouped_plan_s;
+  if (!h) return DORA_ERR_INVALID_ARG;
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  int st = grouped_prepare(modules, n_modules, dtype, r, workspace, workspace_bytes, true, st_,
+                           &h->plan);
+  if (st == DORA_OK && n_modules > 0 && cudaStreamSynchronize(st_) != cudaSuccess) st = DORA_ERR_CUDA;
+  if (st != DORA_OK) {
+    delete h;
+    return st;
+  }
+  *plan = h;
+  return DORA_OK;
+}
+
+int dora_norm_grouped_plan_run(dora_norm_grouped_plan plan, float s, float eps, void* stream) {
+  if (!plan) return DORA_ERR_INVALID_ARG;
+  return grouped_run(plan->plan, s, eps, static_cast<cudaStream_t>(stream));
+}
+
+void dora_norm_grouped_plan_destroy(dora_norm_grouped_plan plan) { delete plan; }
 
 size_t dora_compose_grouped_workspace_size(int n_modules) {
   if (n_modules < 0) return 0;

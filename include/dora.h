@@ -212,6 +212,48 @@ int dora_factored_norm_grouped(const dora_norm_module* modules, int n_modules, i
                                int64_t r, float s, float eps, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/*
+ * A grouped norm prepared once and run many times.  dora_factored_norm_grouped
+ * encodes a TMA descriptor set and copies a table entry for every module on
+ * each call: host work that grows with the module count and, since the copy
+ * reads pageable memory, blocks the host.  A plan does that once; a run only
+ * zeroes a few control words and launches the Gram and main-pass kernels.
+ * This fits a training loop, where the frozen weights W and the adapter
+ * parameters A, B, m keep their buffers and are updated in place.
+ *
+ * dora_norm_grouped_plan_create: checks the modules as the grouped call does
+ * (apart from s and eps, which come with each run; a module may have null A
+ * and B and then only runs with s = 0), writes the module tables into
+ * `workspace` (dora_norm_grouped_workspace_size bytes, 256-byte aligned) on
+ * `stream` and synchronizes `stream` before returning, so a run may use any
+ * stream.  On success *plan holds a new handle; on error *plan is NULL and
+ * nothing is left allocated.
+ *
+ * The plan refers to, and does not own, the workspace and every buffer named
+ * in `modules` (the array itself may be freed on return).  They must stay
+ * allocated, with the same shapes, until dora_norm_grouped_plan_destroy, and
+ * the workspace must not be used for anything else meanwhile.  The contents
+ * of W, A, B and m may change between runs.  Runs on one plan must not
+ * overlap in time (they share the workspace): issue them on one stream or
+ * order them with events.
+ *
+ * dora_norm_grouped_plan_run: dora_factored_norm_grouped's result for these
+ * s and eps, written to each module's wnorm and g.  Returns
+ * DORA_ERR_INVALID_ARG for a NULL plan or when the current device is not the
+ * one the plan was created on; otherwise errors as dora_factored_norm_grouped.
+ *
+ * dora_norm_grouped_plan_destroy: frees the handle (host memory only; NULL is
+ * accepted).  It does not wait for runs in flight, which may still read the
+ * workspace: keep the workspace until they complete.
+ */
+typedef struct dora_norm_grouped_plan_s* dora_norm_grouped_plan;
+
+int dora_norm_grouped_plan_create(const dora_norm_module* modules, int n_modules, int dtype,
+                                  int64_t r, void* workspace, size_t workspace_bytes,
+                                  void* stream, dora_norm_grouped_plan* plan);
+int dora_norm_grouped_plan_run(dora_norm_grouped_plan plan, float s, float eps, void* stream);
+void dora_norm_grouped_plan_destroy(dora_norm_grouped_plan plan);
+
 /* One module of a grouped compose: the dora_compose arguments that differ per
  * module. */
 typedef struct dora_compose_module {

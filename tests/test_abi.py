@@ -164,3 +164,28 @@ def test_training_compose_rejects_bad_arguments(lib):
     assert lib.dora_compose_backward(P, 2 * P, 3 * P, 4 * P, 0.0, 1.0, _lib.DORA_BF16, T, d,
                                      5 * P, 6 * P, 7 * P, 8 * P, ws,
                                      None) == _lib.DORA_ERR_INVALID_ARG
+
+
+def _plan_table(d_out=256, d_in=512):
+    t = (_lib.NormModule * 1)()
+    t[0] = _lib.NormModule(P, 2 * P, 3 * P, 4 * P, 5 * P, 6 * P, d_out, d_in)
+    return t
+
+
+def test_grouped_plan_rejects_before_the_gpu(lib):
+    h = ctypes.c_void_p(12345)
+    # no output handle
+    assert lib.dora_norm_grouped_plan_create(_plan_table(), 1, _lib.DORA_BF16, 64, 8 * P, 1 << 30,
+                                             None, None) == _lib.DORA_ERR_INVALID_ARG
+    # an invalid module: the handle is cleared
+    st = lib.dora_norm_grouped_plan_create(_plan_table(d_out=-1), 1, _lib.DORA_BF16, 64, 8 * P,
+                                           1 << 30, None, ctypes.byref(h))
+    assert st == _lib.DORA_ERR_INVALID_ARG and not h.value
+    # a workspace that is too small or misaligned
+    for ws, nbytes in ((8 * P, 256), (8 * P + 16, 1 << 30), (None, 1 << 30)):
+        h = ctypes.c_void_p(12345)
+        st = lib.dora_norm_grouped_plan_create(_plan_table(), 1, _lib.DORA_BF16, 64, ws, nbytes,
+                                               None, ctypes.byref(h))
+        assert st == _lib.DORA_ERR_WORKSPACE and not h.value
+    assert lib.dora_norm_grouped_plan_run(None, 1.0, 1e-6, None) == _lib.DORA_ERR_INVALID_ARG
+    lib.dora_norm_grouped_plan_destroy(None)

@@ -121,3 +121,81 @@ def test_grouped_compose_misaligned_falls_back():
     out = api.dora_compose_grouped(mods, cfg.s)[0]
     ref = oracle.compose_stored(c["base"], c["lora"], g32, cfg.s, cfg.dtype)
     assert ulp_distance(to_host_stored(out), ref, cfg.dtype).max() <= 1
+
+
+def _bits(ts):
+    return [t.cpu().numpy().view(np.uint32).copy() for t in ts]
+
+
+def test_plan_matches_grouped_call_across_in_place_updates():
+    """A plan created once gives, run after run, the grouped call's bits, also
+    after W, A, B and m are rewritten in place (the training-loop use)."""
+    cfg = configs.get(4)
+    xs = [gen.norm_inputs(cfg, module=k) for k in range(7)]
+    mods = [_dev_module(x, cfg.dtype) for x in xs]
+    plan = api.dora_norm_grouped_plan_create(mods)
+    for step in range(3):
+        if step:
+            xs = [gen.norm_inputs(cfg, module=k, seed=step) for k in range(7)]
+            for dst, x in zip(mods, xs):
+                for t, src in zip(dst, _dev_module(x, cfg.dtype)):
+                    t.copy_(src)
+        wns, gs = plan.run(cfg.s, cfg.eps)
+        got_w, got_g = _bits(wns), _bits(gs)
+        ref_w, ref_g = api.dora_factored_norm_grouped(mods, cfg.s, cfg.eps)
+        torch.cuda.synchronize()
+        for a, b in zip(got_w + got_g, _bits(ref_w) + _bits(ref_g)):
+            assert np.array_equal(a, b)
+    for k, x in enumerate(xs):
+        rows = _sample_rows(cfg.modules[k].d_out, n=64, seed=k)
+        _check_norm(cfg, x, plan.wnorms[k].cpu().numpy(), plan.gs[k].cpu().numpy(), rows)
+    plan.destroy()
+
+
+def test_plan_per_module_fallback_keeps_tables():
+    """s = 0 takes the per-module path through the same workspace; the next
+    s != 0 run must still find the one-launch tables intact."""
+    group = _mixed(configs.BF16, 48, 1.25, [(300, 256), (129, 64), (512, 1024)])
+    mods = [_dev_module(x, configs.BF16) for _, x in group]
+    plan = api.dora_norm_grouped_plan_create(mods)
+    for s in (1.25, 0.0, 1.25, -0.75):
+        wns, gs = plan.run(s, 1e-6)
+        torch.cuda.synchronize()
+        for (cfg, x), wn, g in zip(group, wns, gs):
+            c = configs.Config(cfg.name, cfg.index, cfg.dtype, cfg.modules, r=cfg.r, s=s,
+                               eps=cfg.eps, tokens=cfg.tokens)
+            _check_norm(c, x, wn.cpu().numpy(), g.cpu().numpy(), np.arange(cfg.module.d_out))
+    plan.destroy()
+
+
+def test_plan_f32_group():
+    group = _mixed(configs.F32, 24, 2.0, [(200, 136), (65, 36)])
+    mods = [_dev_module(x, configs.F32) for _, x in group]
+    plan = api.dora_norm_grouped_plan_create(mods)
+    wns, gs = plan.run(2.0, 1e-6)
+    torch.cuda.synchronize()
+    for (cfg, x), wn, g in zip(group, wns, gs):
+        _check_norm(cfg, x, wn.cpu().numpy(), g.cpu().numpy(), np.arange(cfg.module.d_out))
+    plan.destroy()
+
+
+def test_many_modules_whole_k_items():
+    """Enough pair tiles to fill the persistent grid several times over: every
+    module runs as whole-K items, numbered longest K first."""
+    rng = np.random.default_rng(5)
+    shapes = [(int(rng.choice([512, 1000, 2048, 2304])), int(rng.choice([64, 200, 512, 1024, 1536])))
+              for _ in range(80)]
+    # four waves of the 76 CTA pairs of a 152-SM part
+    assert sum((d + 255) // 256 for d, _ in shapes) >= 4 * 76
+    group = _mixed(configs.BF16, 32, 0.75, shapes, seed=3)
+    mods = [_dev_module(x, configs.BF16) for _, x in group]
+    plan = api.dora_norm_grouped_plan_create(mods)
+    wns, gs = plan.run(0.75, 1e-6)
+    torch.cuda.synchronize()
+    for k, ((cfg, x), wn, g) in enumerate(zip(group, wns, gs)):
+        rows = _sample_rows(cfg.module.d_out, n=32, seed=k)
+        _check_norm(cfg, x, wn.cpu().numpy(), g.cpu().numpy(), rows)
+    for k in (0, 17, 79):
+        wn1, _ = api.dora_factored_norm(*mods[k][:3], 0.75, mods[k][3], 1e-6)
+        assert rel_err(wns[k].cpu().numpy(), wn1.cpu().numpy()).max() <= 2e-6
+    plan.destroy()
