@@ -135,13 +135,47 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
                              int clusters, cudaStream_t stream);
 cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStream_t stream);
 
-// ------------------------------------------------------------------ SIMT (fp32 inputs)
-enum SimtMode : int { kSimtSumSq = 1, kSimtDotB = 2, kSimtStore = 4 };
-constexpr int kSimtTile = 64;
+// ------------------------------------------------------------------ fp32 inputs: 3xTF32 pair pass
+// D [256-row pair tile x one N pass] = X * Y^T over the K tiles (32 fp32 each)
+// of one work item, every product as x_hi y_hi + x_lo y_hi + x_hi y_lo.
+// Work items (pair tile, N pass, K segment) are striped over the grid.
+constexpr int kTf32BlockK = 32;               // fp32 elements per 128-byte smem row
+constexpr int kTf32MaxGramSplits = 8;         // K segments of the fp32 Gram (workspace)
 
-cudaError_t launch_gemm_simt(const float* X, const float* Y, int rows, int ncols, int K,
-                             const float* B, int ldb, float* out_sumsq, float* out_dot,
-                             float* out_store, int mode, cudaStream_t stream);
+struct Tf32Params {
+  int rows;              // rows of X: d_out (norm) or r (Gram)
+  int n_pass;            // N of one pass (multiple of 16, <= 256)
+  int passes;            // N passes: cover the padded rank
+  int kt_x;              // K tiles of (X, Y)
+  int kt_b;              // K tiles of (B, G') that follow them (norm); 0 for the Gram
+  int splits;            // K segments
+  int seg_k[17];         // segment s covers K tiles [seg_k[s], seg_k[s + 1]), none empty
+  int pair_tiles;        // ceil(rows / 256)
+  int n_items;           // pair_tiles * passes * splits
+  int stages;
+  uint32_t acc_stride;   // TMEM columns per accumulator buffer (two buffers)
+  // norm
+  const float* B;        // [rows x r]
+  int r;
+  float* out_sumsq;      // [splits][rows], written by pass-0 items
+  float* out_dot;        // [passes * splits][rows], part pass * splits + split
+  // Gram
+  float* out_g;          // [splits][rows][r] partial G
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+size_t tf32_smem_bytes(int n_pass, int stages);
+int tf32_pick_stages(int n_pass);
+int tf32_max_clusters();
+// store = false: the norm pass (X = W then B, Y = A then G'); true: the Gram (X = Y = A)
+cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const CUtensorMap& tXb,
+                             const CUtensorMap& tYb, const Tf32Params& p, bool store,
+                             int clusters, cudaStream_t stream);
+// G' [rp x rp] = scale * (sum over the splits of the partials, in split order); zero
+// outside [r x r]
+cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int rp, float scale,
+                                    float* Gp, cudaStream_t stream);
 
 // ------------------------------------------------------------------ small kernels
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,

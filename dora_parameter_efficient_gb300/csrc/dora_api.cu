@@ -96,6 +96,21 @@ bool make_map_bf16(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t o
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major [outer x inner] fp32 matrix, box [box_outer x 32], 128-byte
+// swizzle, out-of-bounds elements read as zero.
+bool make_map_f32(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
+                  uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kTf32BlockK), box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Gram blocks: the upper triangle of the nb x nb grid of 128-row blocks of
 // G [rp x rp], each block bw columns wide.
 int gram_nb(int rp) { return static_cast<int>((rp + 127) / 128); }
@@ -113,8 +128,9 @@ struct Plan {
   int main_splits = 1;      // split-K of the main pass (tensor-core path)
   int gram_splits = 1;
   size_t off_status = 0, zero_bytes = 0, off_G = 0, off_Ghi = 0, off_Glo = 0;
-  size_t off_pbase = 0, off_pcross = 0, off_pba = 0, total = 0;
-  int cap_base = 0, cap_cross = 0, cap_ba = 0;
+  size_t off_Gpart = 0;     // fp32: K-segment partials of G
+  size_t off_pbase = 0, off_pcross = 0, total = 0;
+  int cap_base = 0, cap_cross = 0;
 };
 
 // Split-K count: minimise (waves x K tiles per CTA) plus a per-wave epilogue
@@ -139,10 +155,8 @@ Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
   Plan p;
   p.bf16 = dtype == DORA_BF16;
   p.rp = static_cast<int>(ceil_div(r, 16) * 16);
-  const int simt_cols = static_cast<int>(ceil_div(r, kSimtTile));
   p.cap_base = kMaxMainSplits;
-  p.cap_cross = kMaxMainSplits > simt_cols ? kMaxMainSplits : simt_cols;
-  p.cap_ba = 2 > simt_cols ? 2 : simt_cols;
+  p.cap_cross = kMaxMainSplits;
   size_t off = 0;
   p.off_status = off;
   const int64_t pair_tiles = ceil_div(d_out, 2 * kTcBlockM);
@@ -157,13 +171,13 @@ Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
   } else {
     p.off_G = off;
     off = align_up(off + rp2 * 4, 256);
+    p.off_Gpart = off;
+    off = align_up(off + static_cast<size_t>(kTf32MaxGramSplits) * r * r * 4, 256);
   }
   p.off_pbase = off;
   off = align_up(off + static_cast<size_t>(p.cap_base) * d_out * 4, 256);
   p.off_pcross = off;
   off = align_up(off + static_cast<size_t>(p.cap_cross) * d_out * 4, 256);
-  p.off_pba = off;
-  off = align_up(off + static_cast<size_t>(p.cap_ba) * d_out * 4, 256);
   p.total = off;
   (void)d_in;
   return p;
@@ -284,11 +298,11 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + plan.off_Glo);
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
-  float* pba = reinterpret_cast<float*>(ws + plan.off_pba);
+  float* Gpart = reinterpret_cast<float*>(ws + plan.off_Gpart);
 
   DORA_TRY(cudaMemsetAsync(status, 0, plan.zero_bytes, stream));
 
-  int n_base = 0, n_cross = 0, n_ba = 0;
+  int n_base = 0, n_cross = 0;
   if (d_in == 0) {
     // W has no columns: every term is zero.
   } else if (!adapter) {
@@ -380,24 +394,83 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
     return DORA_OK;
   } else {
-    // fp32 inputs: CUDA-core path
-    const float* Wf = static_cast<const float*>(W);
-    const float* Af = static_cast<const float*>(A);
-    const float* Bf = static_cast<const float*>(B);
-    const int ri = static_cast<int>(r);
-    DORA_TRY(launch_gemm_simt(Af, Af, ri, ri, static_cast<int>(d_in), nullptr, 0, nullptr, nullptr,
-                              G, kSimtStore, stream));
-    DORA_TRY(launch_gemm_simt(Bf, G, static_cast<int>(d_out), ri, ri, Bf, ri, nullptr, pba,
-                              nullptr, kSimtDotB, stream));
-    n_ba = static_cast<int>(ceil_div(r, kSimtTile));
+    // fp32 inputs: the 3xTF32 tensor-core pass (gemm_tf32.cu).  G = A A^T in
+    // K segments, their sum scaled to G' = (s/2) G, then the pair pass over
+    // (W, A) and (B, G') tiles in N passes of up to 256 columns; the finalize
+    // kernel adds the partials.
+    const int rp = plan.rp;
+    const int passes = static_cast<int>(ceil_div(rp, 256));
+    const int n_pass = static_cast<int>(ceil_div(ceil_div(rp, passes), 16) * 16);
+    const int yr = n_pass / 2;
+    const int clusters_max = tf32_max_clusters();
+    if (clusters_max <= 0) return DORA_ERR_CUDA;
+    uint32_t acc_stride = 32;
+    while (acc_stride < static_cast<uint32_t>(n_pass)) acc_stride <<= 1;
+    const int kt_x = static_cast<int>(ceil_div(d_in, kTf32BlockK));
+    CUtensorMap mW, mA_x, mA_y, mB_x, mG_y;
+    if (!make_map_f32(&mW, W, d_in, d_out, kTcBlockM) ||
+        !make_map_f32(&mA_x, A, d_in, r, kTcBlockM) || !make_map_f32(&mA_y, A, d_in, r, yr) ||
+        !make_map_f32(&mB_x, B, r, d_out, kTcBlockM) || !make_map_f32(&mG_y, G, rp, rp, yr))
+      return DORA_ERR_CUDA;
+
+    Tf32Params pg{};
+    pg.rows = static_cast<int>(r);
+    pg.n_pass = n_pass;
+    pg.passes = passes;
+    pg.kt_x = kt_x;
+    pg.kt_b = 0;
+    pg.pair_tiles = static_cast<int>(ceil_div(r, 2 * kTcBlockM));
+    {
+      const int units = pg.pair_tiles * passes;
+      int sp = static_cast<int>(ceil_div(clusters_max, units));
+      if (sp > kTf32MaxGramSplits) sp = kTf32MaxGramSplits;
+      if (sp > kt_x) sp = kt_x;
+      if (sp < 1) sp = 1;
+      pg.splits = sp;
+      for (int i = 0; i <= sp; ++i) pg.seg_k[i] = static_cast<int>((static_cast<int64_t>(kt_x) * i) / sp);
+    }
+    pg.n_items = pg.pair_tiles * passes * pg.splits;
+    pg.stages = tf32_pick_stages(n_pass);
+    pg.acc_stride = acc_stride;
+    pg.r = static_cast<int>(r);
+    pg.out_g = Gpart;
+    pg.status = status;
+    pg.timeout_ns = kDefaultTimeoutNs;
+    DORA_TRY(launch_gemm_tf32(mA_x, mA_y, mA_x, mA_y, pg, true,
+                              pg.n_items < clusters_max ? pg.n_items : clusters_max, stream));
+    DORA_TRY(launch_gram_tf32_reduce(Gpart, pg.splits, static_cast<int>(r), rp, 0.5f * s, G, stream));
+
+    Tf32Params pm{};
+    pm.rows = static_cast<int>(d_out);
+    pm.n_pass = n_pass;
+    pm.passes = passes;
+    pm.kt_x = kt_x;
+    pm.kt_b = static_cast<int>(ceil_div(rp, kTf32BlockK));
+    pm.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
+    {
+      const int ktot = pm.kt_x + pm.kt_b;
+      const int sp = pick_pair_splits(static_cast<int64_t>(pm.pair_tiles) * passes, ktot,
+                                      clusters_max, kMaxFinalParts / passes);
+      pm.splits = sp;
+      for (int i = 0; i <= sp; ++i) pm.seg_k[i] = static_cast<int>((static_cast<int64_t>(ktot) * i) / sp);
+    }
+    pm.n_items = pm.pair_tiles * passes * pm.splits;
+    pm.stages = pg.stages;
+    pm.acc_stride = acc_stride;
+    pm.B = static_cast<const float*>(B);
+    pm.r = static_cast<int>(r);
+    pm.out_sumsq = pbase;
+    pm.out_dot = pcross;
+    pm.status = status;
+    pm.timeout_ns = kDefaultTimeoutNs;
     if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
-    DORA_TRY(launch_gemm_simt(Wf, Af, static_cast<int>(d_out), ri, static_cast<int>(d_in), Bf, ri,
-                              pbase, pcross, nullptr, kSimtSumSq | kSimtDotB, stream));
+    DORA_TRY(launch_gemm_tf32(mW, mA_y, mB_x, mG_y, pm, false,
+                              pm.n_items < clusters_max ? pm.n_items : clusters_max, stream));
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
-    n_base = 1;
-    n_cross = n_ba;
+    n_base = pm.splits;
+    n_cross = passes * pm.splits;
   }
-  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, pba, n_ba, s, m, bf16, eps,
+  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, nullptr, 0, s, m, bf16, eps,
                            wnorm, g, stream));
   return DORA_OK;
 }

@@ -1,0 +1,516 @@
+// gemm_tf32.cu -- the factored norm's GEMMs for fp32 inputs on the tensor
+// cores ("Scaling DoRA", Chinese write-up sections 1.2.1 and 1.2.2 and
+// Algorithm 1 of section 5.1: U = W A^T, G = A A^T and rowsum(B o (B G)),
+// fp32 inputs accumulated in fp32).
+//
+// Precision.  The tensor cores multiply TF32 values (10 fraction bits).  Each
+// fp32 operand value v is split in shared memory into hi = tf32(v) and
+// lo = tf32(v - hi), both exact TF32 values whose sum keeps 22 significant
+// bits of v, and every product is taken as x_hi y_hi + x_lo y_hi + x_hi y_lo
+// on kind::tf32 MMAs with fp32 accumulation (the dropped x_lo y_lo is below
+// 2^-22 of the product; this is the usual "3xTF32" scheme).  Small integers
+// split into hi = v, lo = 0, so integer-valued inputs still give exact
+// results.  The sum of squares of W is taken on the CUDA cores from the raw
+// fp32 tile, compensated across tiles.
+//
+// Two modes (template argument kStore):
+//   * norm: for each row j of W and each work item (pair tile, N pass, K
+//     segment), dot_j = rowsum(B_j o D_j) over the pass's columns, with
+//     D = W A^T followed in K by B G', G' = (s/2) G, so the sum over the
+//     items is cross + (s/2) ba, exactly as in the bf16 pass; items of N pass
+//     0 also write the segment's sum of squares.  A separate finalize adds
+//     the partials in a fixed order;
+//   * Gram: D = A A^T over the item's K range, stored as an fp32 partial; a
+//     reduce kernel adds the segments in order and scales by s/2.
+//
+// Tiling for sm_103a: CTA pairs (clusters of 2, tcgen05 cta_group::2), M = 256
+// rows of X per pair (128 in each CTA), N = one pass of at most 256 columns
+// (each CTA holds half of the pass's Y rows), K = 32 fp32 -- one 128-byte
+// swizzled row -- per pipeline stage.  Per stage and CTA:
+//   * warp 0 loads its X tile and its half of the Y tile (TMA) and counts the
+//     bytes on its own `full` barrier;
+//   * warps 2-9 split both tiles (hi in place, lo into a second buffer), take
+//     the sum of squares of X when it is a W tile, fence their writes for the
+//     async proxy and arrive on the even CTA's `ready` barrier;
+//   * warp 1 of the even CTA issues the 12 MMAs of the stage (4 K steps x 3
+//     terms) and commits `consumed` to both CTAs, which frees the stage;
+//   * warps 10-13 (one per TMEM lane quadrant) drain the accumulator of each
+//     item -- two TMEM buffers, used by alternate items, so the MMAs of the
+//     next item run meanwhile.
+// The grid is persistent and the items are striped over it (cluster c takes
+// items c, c + clusters, ...): they are of equal size, and every role walks
+// the same sequence with no hand-off.  Every wait is bounded by %globaltimer;
+// on expiry the kernel records a timeout in the status word and stops.
+#include <cstring>
+
+#include "common.cuh"
+#include "finalize.cuh"
+#include "ptx.cuh"
+
+namespace dora {
+
+namespace {
+
+constexpr int kTfThreads = 448;        // warp 0 TMA, 1 MMA, 2-9 split, 10-13 drain
+constexpr int kTfSplitWarps = 8;
+constexpr int kTfDrainWarps = 4;
+constexpr uint32_t kTfXBytes = 128u * 128u;   // [128 rows x 32 fp32], 128-byte swizzle
+
+__device__ __forceinline__ float4 lds4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts4(uint32_t addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// hi = tf32(v), lo = tf32(v - hi); v - hi is exact (hi is within a factor of
+// two of v, Sterbenz)
+__device__ __forceinline__ void split4(const float4 v, float4& hi, float4& lo) {
+  hi.x = tf32_round(v.x);
+  hi.y = tf32_round(v.y);
+  hi.z = tf32_round(v.z);
+  hi.w = tf32_round(v.w);
+  lo.x = tf32_round(__fsub_rn(v.x, hi.x));
+  lo.y = tf32_round(__fsub_rn(v.y, hi.y));
+  lo.z = tf32_round(__fsub_rn(v.z, hi.z));
+  lo.w = tf32_round(__fsub_rn(v.w, hi.w));
+}
+
+struct TfItem {
+  int tile, pass, split, kb, ke;
+};
+
+// work item -> (pair tile, N pass, K segment): segment-major
+__device__ __forceinline__ TfItem tf_item(const Tf32Params& p, int item) {
+  TfItem t;
+  const int per_split = p.pair_tiles * p.passes;
+  t.split = item / per_split;
+  const int rem = item - t.split * per_split;
+  t.pass = rem / p.pair_tiles;
+  t.tile = rem - t.pass * p.pair_tiles;
+  t.kb = p.seg_k[t.split];
+  t.ke = p.seg_k[t.split + 1];
+  return t;
+}
+
+// acc += sum over 32 columns of B (fp32, from global) times D (v); columns at
+// or past r contribute nothing (r is a multiple of 4)
+__device__ __forceinline__ float dot_b32(const float* brow, int col0, int r, bool valid,
+                                         const float (&v)[32], int n, float acc) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (4 * g < n && valid && col0 + 4 * g < r) {
+      const float4 b = __ldg(reinterpret_cast<const float4*>(brow + col0 + 4 * g));
+      acc = fmaf(b.x, v[4 * g], acc);
+      acc = fmaf(b.y, v[4 * g + 1], acc);
+      acc = fmaf(b.z, v[4 * g + 2], acc);
+      acc = fmaf(b.w, v[4 * g + 3], acc);
+    }
+  }
+  return acc;
+}
+
+template <bool kStore>
+__global__ void __launch_bounds__(kTfThreads, 1)
+    k_gemm_tf32(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tY,
+                const __grid_constant__ CUtensorMap tXb, const __grid_constant__ CUtensorMap tYb,
+                const __grid_constant__ Tf32Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t yr = static_cast<uint32_t>(p.n_pass) / 2u;   // Y rows per CTA
+  const uint32_t ybytes = yr * 128u;
+  const uint32_t stage_bytes = 2u * kTfXBytes + 2u * ybytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
+  uint64_t* ready = full + p.stages;
+  uint64_t* consumed = ready + p.stages;
+  uint64_t* accum_full = consumed + p.stages;   // [2]
+  uint64_t* accum_empty = accum_full + 2;       // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(num_clusters_x());
+  const uint32_t stages = static_cast<uint32_t>(p.stages);
+  const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (uint32_t s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&ready[s], 2 * kTfSplitWarps);   // the split warps of both CTAs
+      mbar_init(&consumed[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accum_full[b], 1);
+      mbar_init(&accum_empty[b], 2 * kTfDrainWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tX);
+    tma_prefetch_desc(&tY);
+    if (!kStore) {
+      tma_prefetch_desc(&tXb);
+      tma_prefetch_desc(&tYb);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_holder, 2u * p.acc_stride);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+  const uint32_t smem0 = smem_u32(smem);
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- TMA producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_stream = l2_policy_evict_first();
+      const uint64_t pol_keep = l2_policy_evict_last();
+      uint32_t s = 0, phase = 0, it = 0;
+      bool stop = false, g_ready = false;
+      for (int item = cid; item < p.n_items && !stop; item += ncl) {
+        const TfItem t = tf_item(p, item);
+        const int row0 = t.tile * 256 + static_cast<int>(rank) * 128;
+        const int yrow0 = t.pass * p.n_pass + static_cast<int>(rank * yr);
+        for (int kt = t.kb; kt < t.ke; ++kt, ++it) {
+          // the slot's previous use must have been consumed by the MMAs
+          if (it >= stages && !mbar_wait(&consumed[s], phase ^ 1u, deadline)) {
+            atomicExch(p.status, kStatusTimeout);
+            stop = true;
+            break;
+          }
+          uint8_t* xs = smem + s * stage_bytes;
+          uint8_t* ys = xs + 2u * kTfXBytes;
+          mbar_arrive_expect_tx(&full[s], kTfXBytes + ybytes);
+          if (kt < p.kt_x) {
+            tma_load_2d(xs, &tX, &full[s], kt * kTf32BlockK, row0, kStore ? pol_keep : pol_stream);
+            tma_load_2d(ys, &tY, &full[s], kt * kTf32BlockK, yrow0, pol_keep);
+          } else {
+            // (B, G') tiles: G' comes from the preceding kernels
+            if (!g_ready) {
+              griddep_wait();
+              g_ready = true;
+            }
+            const int kk = (kt - p.kt_x) * kTf32BlockK;
+            tma_load_2d(xs, &tXb, &full[s], kk, row0, pol_keep);
+            tma_load_2d(ys, &tYb, &full[s], kk, yrow0, pol_keep);
+          }
+          if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // no copy may still be in flight when the CTA exits
+      const uint64_t drain_deadline = global_timer_ns() + p.timeout_ns;
+      const uint32_t first = it > stages ? it - stages : 0;
+      for (uint32_t i = first; i < it; ++i)
+        if (!mbar_wait(&full[i % stages], (i / stages) & 1u, drain_deadline))
+          atomicExch(p.status, kStatusTimeout);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_tf32_f32(256, static_cast<uint32_t>(p.n_pass));
+      const uint64_t dX0 = smem_desc_sw128(smem0);
+      const uint64_t dXL0 = smem_desc_sw128(smem0 + kTfXBytes);
+      const uint64_t dY0 = smem_desc_sw128(smem0 + 2u * kTfXBytes);
+      const uint64_t dYL0 = smem_desc_sw128(smem0 + 2u * kTfXBytes + ybytes);
+      const uint64_t step = stage_bytes >> 4;
+      uint32_t s = 0, phase = 0;
+      int icount = 0;
+      bool stop = false;
+      for (int item = cid; item < p.n_items && !stop; item += ncl, ++icount) {
+        const TfItem t = tf_item(p, item);
+        const uint32_t buf = static_cast<uint32_t>(icount) & 1u;
+        const uint32_t use = static_cast<uint32_t>(icount) >> 1;
+        if (use > 0 && !mbar_wait(&accum_empty[buf], (use - 1) & 1u, deadline)) {
+          atomicExch(p.status, kStatusTimeout);
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t acc = tmem_base + buf * p.acc_stride;
+        for (int kt = t.kb; kt < t.ke; ++kt) {
+          if (!mbar_wait_cluster(&ready[s], phase, deadline)) {
+            atomicExch(p.status, kStatusTimeout);
+            stop = true;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t o = static_cast<uint64_t>(s) * step;
+#pragma unroll
+          for (int ks = 0; ks < kTf32BlockK / 8; ++ks) {
+            const uint64_t k = o + 2u * static_cast<uint64_t>(ks);   // 32 bytes per K step
+            const uint32_t first = (kt == t.kb && ks == 0) ? 0u : 1u;
+            umma_tf32_pair(acc, dX0 + k, dY0 + k, idesc, first);
+            umma_tf32_pair(acc, dXL0 + k, dY0 + k, idesc, 1u);
+            umma_tf32_pair(acc, dX0 + k, dYL0 + k, idesc, 1u);
+          }
+          umma_commit_pair(&consumed[s], 0x3);
+          if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+        // also after a timeout: the wait below then covers every MMA issued
+        umma_commit_pair(&accum_full[buf], 0x3);
+      }
+      if (icount > 0) {
+        const uint32_t last = static_cast<uint32_t>(icount - 1);
+        if (!mbar_wait(&accum_full[last & 1u], (last >> 1) & 1u, global_timer_ns() + p.timeout_ns))
+          atomicExch(p.status, kStatusTimeout);
+      }
+    }
+  } else if (warp < 2 + kTfSplitWarps) {
+    // -------------------------------------------------------------- split (both CTAs)
+    // Warp w handles rows 16w .. 16w + 15 of the X tile and of the Y half:
+    // one instruction covers 4 whole rows (lane 8 * sub + chunk reads 16-byte
+    // chunk `chunk` of row 16w + 4i + sub).  The 128-byte swizzle permutes
+    // chunks within a row, which neither the split nor a row sum sees.
+    const int w = warp - 2;
+    const int sub = lane >> 3;
+    const int chunk = lane & 7;
+    const uint32_t ready0 = map_to_rank(smem_u32(ready), 0);
+    uint32_t s = 0, phase = 0;
+    bool alive = true;
+    for (int item = cid; item < p.n_items; item += ncl) {
+      const TfItem t = tf_item(p, item);
+      const bool do_sq = !kStore && t.pass == 0;
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, scmp[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kt = t.kb; kt < t.ke; ++kt) {
+        if (alive && !mbar_wait(&full[s], phase, deadline)) {
+          atomicExch(p.status, kStatusTimeout);
+          alive = false;
+        }
+        if (alive) {
+          const uint32_t xa = smem0 + s * stage_bytes;
+          const bool sq = do_sq && kt < p.kt_x;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t off = static_cast<uint32_t>((16 * w + 4 * i + sub) * 128 + chunk * 16);
+            const float4 v = lds4(xa + off);
+            if (sq) {
+              float q = __fmul_rn(v.x, v.x);
+              q = fmaf(v.y, v.y, q);
+              q = fmaf(v.z, v.z, q);
+              q = fmaf(v.w, v.w, q);
+              kahan_add(sacc[i], scmp[i], q);
+            }
+            float4 hi, lo;
+            split4(v, hi, lo);
+            sts4(xa + off, hi);
+            sts4(xa + kTfXBytes + off, lo);
+          }
+          const uint32_t ya = xa + 2u * kTfXBytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t row = static_cast<uint32_t>(16 * w + 4 * i + sub);
+            if (row < yr) {
+              const uint32_t off = row * 128u + static_cast<uint32_t>(chunk * 16);
+              const float4 v = lds4(ya + off);
+              float4 hi, lo;
+              split4(v, hi, lo);
+              sts4(ya + off, hi);
+              sts4(ya + ybytes + off, lo);
+            }
+          }
+          fence_async_smem_writes();
+        }
+        __syncwarp();
+        if (alive && lane == 0) mbar_arrive_cluster(ready0 + s * 8u);
+        if (++s == stages) {
+          s = 0;
+          phase ^= 1u;
+        }
+      }
+      if (do_sq) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float v = __fsub_rn(sacc[i], scmp[i]);
+          v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+          v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+          v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+          const int grow = t.tile * 256 + static_cast<int>(rank) * 128 + 16 * w + 4 * i + sub;
+          if (alive && chunk == 0 && grow < p.rows)
+            p.out_sumsq[static_cast<size_t>(t.split) * p.rows + grow] = v;
+        }
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- drain (both CTAs)
+    const int q = warp & 3;                       // TMEM lane quadrant this warp may read
+    const uint32_t accum_empty0 = map_to_rank(smem_u32(accum_empty), 0);
+    int icount = 0;
+    for (int item = cid; item < p.n_items; item += ncl, ++icount) {
+      const TfItem t = tf_item(p, item);
+      const uint32_t buf = static_cast<uint32_t>(icount) & 1u;
+      if (!mbar_wait(&accum_full[buf], (static_cast<uint32_t>(icount) >> 1) & 1u, deadline)) {
+        atomicExch(p.status, kStatusTimeout);
+        break;
+      }
+      tc_fence_after_sync();
+      const int row = t.tile * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+      const bool valid = row < p.rows;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * p.acc_stride;
+      const int col_base = t.pass * p.n_pass;
+      float acc = 0.f;
+      for (int c = 0; c < p.n_pass; c += 32) {
+        const int n = p.n_pass - c >= 32 ? 32 : 16;   // n_pass is a multiple of 16
+        float v[32];
+        if (n == 32) {
+          tmem_load_32cols(taddr + static_cast<uint32_t>(c), v);
+        } else {
+          uint32_t rv[16];
+          tmem_load_16cols_async(taddr + static_cast<uint32_t>(c), rv);
+          tmem_wait_ld(rv);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            v[i] = __uint_as_float(rv[i]);
+            v[16 + i] = 0.f;
+          }
+        }
+        if constexpr (!kStore) {
+          const float* brow = p.B + static_cast<size_t>(valid ? row : 0) * p.r;
+          acc = dot_b32(brow, col_base + c, p.r, valid, v, n, acc);
+        } else {
+          float* grow = p.out_g + (static_cast<size_t>(t.split) * p.rows + (valid ? row : 0)) * p.r;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const int col = col_base + c + 4 * g;
+            if (4 * g < n && valid && col < p.r)
+              *reinterpret_cast<float4*>(grow + col) =
+                  make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(accum_empty0 + buf * 8u);
+      if (!kStore && valid)
+        p.out_dot[(static_cast<size_t>(t.pass) * p.splits + t.split) * p.rows + row] = acc;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();            // the peer may still read this CTA's shared memory until here
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, 2u * p.acc_stride);
+  }
+}
+
+// G' = scale * (sum of the K-segment partials in segment order), zero padded
+__global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, int r, int rp,
+                                   float scale, float* __restrict__ Gp) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(rp) * rp) return;
+  const int i = static_cast<int>(idx / rp);
+  const int j = static_cast<int>(idx - static_cast<int64_t>(i) * rp);
+  float out = 0.f;
+  if (i < r && j < r) {
+    df acc{0.f, 0.f};
+    for (int sp = 0; sp < splits; ++sp) {
+      float e;
+      two_sum(acc.hi, parts[(static_cast<size_t>(sp) * r + i) * r + j], acc.hi, e);
+      acc.lo = __fadd_rn(acc.lo, e);
+    }
+    out = __fmul_rn(scale, __fadd_rn(acc.hi, acc.lo));
+  }
+  Gp[idx] = out;
+}
+
+}  // namespace
+
+size_t tf32_smem_bytes(int n_pass, int stages) {
+  const size_t stage = 2 * static_cast<size_t>(kTfXBytes) + 2 * static_cast<size_t>(n_pass / 2) * 128u;
+  return 1024 + stage * static_cast<size_t>(stages) + (3 * static_cast<size_t>(stages) + 4) * 8 + 16;
+}
+
+int tf32_pick_stages(int n_pass) {
+  const size_t budget = 227 * 1024;
+  int st = kTcMaxStages;
+  while (st > 2 && tf32_smem_bytes(n_pass, st) > budget) --st;
+  return st;
+}
+
+// Co-resident CTA pairs (one CTA per SM: every shape needs most of an SM's
+// shared memory); the attribute is raised to the largest size once per device.
+int tf32_max_clusters() {
+  constexpr int kMaxSmem = 227 * 1024;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static int cached[64] = {0};
+  if (dev < 64 && cached[dev]) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kTfThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMaxSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaFuncSetAttribute(k_gemm_tf32<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_gemm_tf32<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_gemm_tf32<false>, &cfg) != cudaSuccess)
+    return 0;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const CUtensorMap& tXb,
+                             const CUtensorMap& tYb, const Tf32Params& p, bool store,
+                             int clusters, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kTfThreads, 1, 1);
+  cfg.dynamicSmemBytes = tf32_smem_bytes(p.n_pass, p.stages);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // the norm pass may start while the G' reduce still runs: only its (B, G')
+  // loads depend on it, and they wait for it (griddep_wait)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = store ? 1 : 2;
+  cudaError_t e = store ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<true>, tX, tY, tXb, tYb, p)
+                        : cudaLaunchKernelEx(&cfg, k_gemm_tf32<false>, tX, tY, tXb, tYb, p);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int rp, float scale,
+                                    float* Gp, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(rp) * rp;
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  k_gram_tf32_reduce<<<blocks, 256, 0, stream>>>(parts, splits, r, rp, scale, Gp);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace dora

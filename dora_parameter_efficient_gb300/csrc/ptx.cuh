@@ -378,4 +378,38 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::tf32 with TF32 A/B, fp32 D, both K-major
+// (same fields as above; format code 2 = TF32).
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem, both CTAs] (+)= A * B^T with TF32 operands (fp32 containers whose
+// low 13 fraction bits are zero) and fp32 accumulation, M = 256 over the CTA
+// pair, K = 8 per instruction.  Issued by the pair's even CTA.
+__device__ __forceinline__ void umma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// Makes this thread's generic-proxy writes to its CTA's shared memory visible
+// to later async-proxy reads (TMA stores, tensor-core operand fetches) that
+// are ordered after it by an mbarrier.
+__device__ __forceinline__ void fence_async_smem_writes() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// v rounded to TF32 (10 fraction bits), to nearest with ties away from zero,
+// returned in an fp32 container whose low 13 fraction bits are zero.  Plain
+// bit arithmetic on the IEEE encoding: adding half of the dropped unit to the
+// magnitude bits and clearing them rounds the magnitude (a carry moves into
+// the exponent as it should).  Finite inputs below the largest TF32 value.
+__device__ __forceinline__ float tf32_round(float v) {
+  return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
+}
+
 }  // namespace dora
