@@ -140,7 +140,7 @@ cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStre
 // of one work item, every product as x_hi y_hi + x_lo y_hi + x_hi y_lo.
 // Work items (pair tile, N pass, K segment) are striped over the grid.
 constexpr int kTf32BlockK = 32;               // fp32 elements per 128-byte smem row
-constexpr int kTf32MaxGramSplits = 8;         // K segments of the fp32 Gram (workspace)
+constexpr int kTf32MaxGramSplits = 16;        // K segments of the fp32 Gram (workspace)
 
 struct Tf32Params {
   int rows;              // rows of X: d_out (norm) or r (Gram)

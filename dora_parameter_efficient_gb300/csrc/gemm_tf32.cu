@@ -3,14 +3,16 @@
 // Algorithm 1 of section 5.1: U = W A^T, G = A A^T and rowsum(B o (B G)),
 // fp32 inputs accumulated in fp32).
 //
-// Precision.  The tensor cores multiply TF32 values (10 fraction bits).  Each
-// fp32 operand value v is split in shared memory into hi = tf32(v) and
-// lo = tf32(v - hi), both exact TF32 values whose sum keeps 22 significant
-// bits of v, and every product is taken as x_hi y_hi + x_lo y_hi + x_hi y_lo
-// on kind::tf32 MMAs with fp32 accumulation (the dropped x_lo y_lo is below
-// 2^-22 of the product; this is the usual "3xTF32" scheme).  Small integers
-// split into hi = v, lo = 0, so integer-valued inputs still give exact
-// results.  The sum of squares of W is taken on the CUDA cores from the raw
+// Precision.  The tensor cores multiply TF32 values: from an fp32 container
+// they take the sign, the exponent and the top 10 fraction bits and ignore
+// the low 13.  So the fp32 tile as loaded serves as hi = trunc_tf32(v), and
+// the split warps write lo = v - hi (exact in fp32, |lo| < 2^-10 |v|) to a
+// second tile; every product is taken as x_hi y_hi + x_lo y_hi + x_hi y_lo
+// on kind::tf32 MMAs with fp32 accumulation -- the usual "3xTF32" scheme.
+// The tensor core reads lo in turn to TF32 (an error below 2^-10 |lo|), and
+// the dropped x_lo y_lo is below 2^-20 of the product, so each product is
+// good to a few units of 2^-20.  Small integers split into hi = v, lo = 0,
+// so integer-valued inputs still give exact results.  The sum of squares of W is taken on the CUDA cores from the raw
 // fp32 tile, compensated across tiles.
 //
 // Two modes (template argument kStore):
@@ -26,17 +28,23 @@
 // Tiling for sm_103a: CTA pairs (clusters of 2, tcgen05 cta_group::2), M = 256
 // rows of X per pair (128 in each CTA), N = one pass of at most 256 columns
 // (each CTA holds half of the pass's Y rows), K = 32 fp32 -- one 128-byte
-// swizzled row -- per pipeline stage.  Per stage and CTA:
-//   * warp 0 loads its X tile and its half of the Y tile (TMA) and counts the
-//     bytes on its own `full` barrier;
-//   * warps 2-9 split both tiles (hi in place, lo into a second buffer), take
-//     the sum of squares of X when it is a W tile, fence their writes for the
-//     async proxy and arrive on the even CTA's `ready` barrier;
+// swizzled row -- per pipeline stage.  Two rings of shared-memory slots: raw
+// slots receive the TMA loads, split slots hold the four TF32 operand tiles
+// the MMAs read.  Per stage and CTA:
+//   * warp 0 loads its X tile and its half of the Y tile (TMA) into a raw
+//     slot and counts the bytes on its own `raw_full` barrier;
+//   * warps 2-17 read the raw slot, write x_lo and y_lo into a split slot,
+//     take the sum of squares of X when it is a W tile, fence their writes
+//     for the async proxy and arrive on the even CTA's `sp_ready` barrier;
 //   * warp 1 of the even CTA issues the 12 MMAs of the stage (4 K steps x 3
-//     terms) and commits `consumed` to both CTAs, which frees the stage;
-//   * warps 10-13 (one per TMEM lane quadrant) drain the accumulator of each
+//     terms, reading hi from the raw slot and lo from the split slot) and
+//     commits `raw_empty` and `sp_empty` to both CTAs, which frees both;
+//   * warps 18-21 (one per TMEM lane quadrant) drain the accumulator of each
 //     item -- two TMEM buffers, used by alternate items, so the MMAs of the
 //     next item run meanwhile.
+// The split slots are busy only from the split to the MMAs, so two of them
+// leave the rest of shared memory to raw slots: the loads run several
+// stages ahead of the MMAs.
 // The grid is persistent and the items are striped over it (cluster c takes
 // items c, c + clusters, ...): they are of equal size, and every role walks
 // the same sequence with no hand-off.  Every wait is bounded by %globaltimer;
@@ -51,10 +59,13 @@ namespace dora {
 
 namespace {
 
-constexpr int kTfThreads = 448;        // warp 0 TMA, 1 MMA, 2-9 split, 10-13 drain
-constexpr int kTfSplitWarps = 8;
+constexpr int kTfThreads = 704;        // warp 0 TMA, 1 MMA, 2-17 split, 18-21 drain
+constexpr int kTfSplitWarps = 16;
+constexpr int kTfSplitRows = 128 / kTfSplitWarps;   // tile rows per split warp
+constexpr int kTfSplitIters = kTfSplitRows / 4;     // one warp instruction covers 4 rows
 constexpr int kTfDrainWarps = 4;
 constexpr uint32_t kTfXBytes = 128u * 128u;   // [128 rows x 32 fp32], 128-byte swizzle
+constexpr uint32_t kTfSplitSlots = 2;
 
 __device__ __forceinline__ float4 lds4(uint32_t addr) {
   float4 v;
@@ -71,17 +82,11 @@ __device__ __forceinline__ void sts4(uint32_t addr, float4 v) {
                : "memory");
 }
 
-// hi = tf32(v), lo = tf32(v - hi); v - hi is exact (hi is within a factor of
-// two of v, Sterbenz)
-__device__ __forceinline__ void split4(const float4 v, float4& hi, float4& lo) {
-  hi.x = tf32_round(v.x);
-  hi.y = tf32_round(v.y);
-  hi.z = tf32_round(v.z);
-  hi.w = tf32_round(v.w);
-  lo.x = tf32_round(__fsub_rn(v.x, hi.x));
-  lo.y = tf32_round(__fsub_rn(v.y, hi.y));
-  lo.z = tf32_round(__fsub_rn(v.z, hi.z));
-  lo.w = tf32_round(__fsub_rn(v.w, hi.w));
+// lo = v - trunc_tf32(v), the part of v the tensor core does not read; the
+// subtraction is exact (both are within a factor of two, Sterbenz)
+__device__ __forceinline__ float4 tf32_lo4(const float4 v) {
+  return make_float4(__fsub_rn(v.x, tf32_trunc(v.x)), __fsub_rn(v.y, tf32_trunc(v.y)),
+                     __fsub_rn(v.z, tf32_trunc(v.z)), __fsub_rn(v.w, tf32_trunc(v.w)));
 }
 
 struct TfItem {
@@ -128,12 +133,16 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t yr = static_cast<uint32_t>(p.n_pass) / 2u;   // Y rows per CTA
   const uint32_t ybytes = yr * 128u;
-  const uint32_t stage_bytes = 2u * kTfXBytes + 2u * ybytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
-  uint64_t* ready = full + p.stages;
-  uint64_t* consumed = ready + p.stages;
-  uint64_t* accum_full = consumed + p.stages;   // [2]
-  uint64_t* accum_empty = accum_full + 2;       // [2]
+  const uint32_t raw_bytes = kTfXBytes + ybytes;                // X, Y (the hi parts)
+  const uint32_t sp_bytes = kTfXBytes + ybytes;                 // X lo, Y lo
+  const uint32_t nraw = static_cast<uint32_t>(p.stages);
+  uint8_t* sp_base = smem + nraw * raw_bytes;
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(sp_base + kTfSplitSlots * sp_bytes);
+  uint64_t* raw_empty = raw_full + nraw;
+  uint64_t* sp_ready = raw_empty + nraw;                 // [kTfSplitSlots]
+  uint64_t* sp_empty = sp_ready + kTfSplitSlots;         // [kTfSplitSlots]
+  uint64_t* accum_full = sp_empty + kTfSplitSlots;       // [2]
+  uint64_t* accum_empty = accum_full + 2;                // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum_empty + 2);
 
   const int warp = threadIdx.x >> 5;
@@ -141,14 +150,16 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(num_clusters_x());
-  const uint32_t stages = static_cast<uint32_t>(p.stages);
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (uint32_t s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&ready[s], 2 * kTfSplitWarps);   // the split warps of both CTAs
-      mbar_init(&consumed[s], 1);
+    for (uint32_t s = 0; s < nraw; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], 1);               // the MMAs that read it are done
+    }
+    for (uint32_t s = 0; s < kTfSplitSlots; ++s) {
+      mbar_init(&sp_ready[s], 2 * kTfSplitWarps);   // the split warps of both CTAs
+      mbar_init(&sp_empty[s], 1);                   // the MMAs that read it are done
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accum_full[b], 1);
@@ -186,18 +197,18 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         const int row0 = t.tile * 256 + static_cast<int>(rank) * 128;
         const int yrow0 = t.pass * p.n_pass + static_cast<int>(rank * yr);
         for (int kt = t.kb; kt < t.ke; ++kt, ++it) {
-          // the slot's previous use must have been consumed by the MMAs
-          if (it >= stages && !mbar_wait(&consumed[s], phase ^ 1u, deadline)) {
+          // the slot's previous contents must have been read by the split warps
+          if (it >= nraw && !mbar_wait(&raw_empty[s], phase ^ 1u, deadline)) {
             atomicExch(p.status, kStatusTimeout);
             stop = true;
             break;
           }
-          uint8_t* xs = smem + s * stage_bytes;
-          uint8_t* ys = xs + 2u * kTfXBytes;
-          mbar_arrive_expect_tx(&full[s], kTfXBytes + ybytes);
+          uint8_t* xs = smem + s * raw_bytes;
+          uint8_t* ys = xs + kTfXBytes;
+          mbar_arrive_expect_tx(&raw_full[s], raw_bytes);
           if (kt < p.kt_x) {
-            tma_load_2d(xs, &tX, &full[s], kt * kTf32BlockK, row0, kStore ? pol_keep : pol_stream);
-            tma_load_2d(ys, &tY, &full[s], kt * kTf32BlockK, yrow0, pol_keep);
+            tma_load_2d(xs, &tX, &raw_full[s], kt * kTf32BlockK, row0, kStore ? pol_keep : pol_stream);
+            tma_load_2d(ys, &tY, &raw_full[s], kt * kTf32BlockK, yrow0, pol_keep);
           } else {
             // (B, G') tiles: G' comes from the preceding kernels
             if (!g_ready) {
@@ -205,10 +216,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
               g_ready = true;
             }
             const int kk = (kt - p.kt_x) * kTf32BlockK;
-            tma_load_2d(xs, &tXb, &full[s], kk, row0, pol_keep);
-            tma_load_2d(ys, &tYb, &full[s], kk, yrow0, pol_keep);
+            tma_load_2d(xs, &tXb, &raw_full[s], kk, row0, pol_keep);
+            tma_load_2d(ys, &tYb, &raw_full[s], kk, yrow0, pol_keep);
           }
-          if (++s == stages) {
+          if (++s == nraw) {
             s = 0;
             phase ^= 1u;
           }
@@ -216,21 +227,24 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       }
       // no copy may still be in flight when the CTA exits
       const uint64_t drain_deadline = global_timer_ns() + p.timeout_ns;
-      const uint32_t first = it > stages ? it - stages : 0;
+      const uint32_t first = it > nraw ? it - nraw : 0;
       for (uint32_t i = first; i < it; ++i)
-        if (!mbar_wait(&full[i % stages], (i / stages) & 1u, drain_deadline))
+        if (!mbar_wait(&raw_full[i % nraw], (i / nraw) & 1u, drain_deadline))
           atomicExch(p.status, kStatusTimeout);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && rank == 0) {
       const uint32_t idesc = idesc_tf32_f32(256, static_cast<uint32_t>(p.n_pass));
+      const uint32_t sp0 = smem_u32(sp_base);
       const uint64_t dX0 = smem_desc_sw128(smem0);
-      const uint64_t dXL0 = smem_desc_sw128(smem0 + kTfXBytes);
-      const uint64_t dY0 = smem_desc_sw128(smem0 + 2u * kTfXBytes);
-      const uint64_t dYL0 = smem_desc_sw128(smem0 + 2u * kTfXBytes + ybytes);
-      const uint64_t step = stage_bytes >> 4;
-      uint32_t s = 0, phase = 0;
+      const uint64_t dY0 = smem_desc_sw128(smem0 + kTfXBytes);
+      const uint64_t dXL0 = smem_desc_sw128(sp0);
+      const uint64_t dYL0 = smem_desc_sw128(sp0 + kTfXBytes);
+      const uint64_t raw_step = raw_bytes >> 4;
+      const uint64_t sp_step = sp_bytes >> 4;
+      uint32_t s = 0, phase = 0;          // split ring
+      uint32_t rs = 0;                    // raw ring
       int icount = 0;
       bool stop = false;
       for (int item = cid; item < p.n_items && !stop; item += ncl, ++icount) {
@@ -244,23 +258,26 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         tc_fence_after_sync();
         const uint32_t acc = tmem_base + buf * p.acc_stride;
         for (int kt = t.kb; kt < t.ke; ++kt) {
-          if (!mbar_wait_cluster(&ready[s], phase, deadline)) {
+          if (!mbar_wait_cluster(&sp_ready[s], phase, deadline)) {
             atomicExch(p.status, kStatusTimeout);
             stop = true;
             break;
           }
           tc_fence_after_sync();
-          const uint64_t o = static_cast<uint64_t>(s) * step;
+          const uint64_t ro = static_cast<uint64_t>(rs) * raw_step;
+          const uint64_t so = static_cast<uint64_t>(s) * sp_step;
 #pragma unroll
           for (int ks = 0; ks < kTf32BlockK / 8; ++ks) {
-            const uint64_t k = o + 2u * static_cast<uint64_t>(ks);   // 32 bytes per K step
+            const uint64_t k = 2u * static_cast<uint64_t>(ks);   // 32 bytes per K step
             const uint32_t first = (kt == t.kb && ks == 0) ? 0u : 1u;
-            umma_tf32_pair(acc, dX0 + k, dY0 + k, idesc, first);
-            umma_tf32_pair(acc, dXL0 + k, dY0 + k, idesc, 1u);
-            umma_tf32_pair(acc, dX0 + k, dYL0 + k, idesc, 1u);
+            umma_tf32_pair(acc, dX0 + ro + k, dY0 + ro + k, idesc, first);
+            umma_tf32_pair(acc, dXL0 + so + k, dY0 + ro + k, idesc, 1u);
+            umma_tf32_pair(acc, dX0 + ro + k, dYL0 + so + k, idesc, 1u);
           }
-          umma_commit_pair(&consumed[s], 0x3);
-          if (++s == stages) {
+          umma_commit_pair(&raw_empty[rs], 0x3);
+          umma_commit_pair(&sp_empty[s], 0x3);
+          if (++rs == nraw) rs = 0;
+          if (++s == kTfSplitSlots) {
             s = 0;
             phase ^= 1u;
           }
@@ -276,31 +293,42 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     }
   } else if (warp < 2 + kTfSplitWarps) {
     // -------------------------------------------------------------- split (both CTAs)
-    // Warp w handles rows 16w .. 16w + 15 of the X tile and of the Y half:
-    // one instruction covers 4 whole rows (lane 8 * sub + chunk reads 16-byte
-    // chunk `chunk` of row 16w + 4i + sub).  The 128-byte swizzle permutes
+    // Warp w handles rows 8w .. 8w + 7 of the X tile and of the Y half: one
+    // instruction covers 4 whole rows (lane 8 * sub + chunk reads 16-byte
+    // chunk `chunk` of row 8w + 4i + sub).  The 128-byte swizzle permutes
     // chunks within a row, which neither the split nor a row sum sees.
     const int w = warp - 2;
     const int sub = lane >> 3;
     const int chunk = lane & 7;
-    const uint32_t ready0 = map_to_rank(smem_u32(ready), 0);
-    uint32_t s = 0, phase = 0;
+    const uint32_t ready0 = map_to_rank(smem_u32(sp_ready), 0);
+    const uint32_t sp0 = smem_u32(sp_base);
+    uint32_t s = 0, phase = 0;          // raw ring
+    uint32_t q = 0, qphase = 0, it = 0; // split ring
     bool alive = true;
     for (int item = cid; item < p.n_items; item += ncl) {
       const TfItem t = tf_item(p, item);
       const bool do_sq = !kStore && t.pass == 0;
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, scmp[4] = {0.f, 0.f, 0.f, 0.f};
+      float sacc[kTfSplitIters], scmp[kTfSplitIters];
+#pragma unroll
+      for (int i = 0; i < kTfSplitIters; ++i) sacc[i] = scmp[i] = 0.f;
       for (int kt = t.kb; kt < t.ke; ++kt) {
-        if (alive && !mbar_wait(&full[s], phase, deadline)) {
+        if (alive && !mbar_wait(&raw_full[s], phase, deadline)) {
+          atomicExch(p.status, kStatusTimeout);
+          alive = false;
+        }
+        // the split slot's previous use must have been read by the MMAs
+        if (alive && it >= kTfSplitSlots && !mbar_wait(&sp_empty[q], qphase ^ 1u, deadline)) {
           atomicExch(p.status, kStatusTimeout);
           alive = false;
         }
         if (alive) {
-          const uint32_t xa = smem0 + s * stage_bytes;
+          const uint32_t xa = smem0 + s * raw_bytes;
+          const uint32_t xd = sp0 + q * sp_bytes;
           const bool sq = do_sq && kt < p.kt_x;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t off = static_cast<uint32_t>((16 * w + 4 * i + sub) * 128 + chunk * 16);
+          for (int i = 0; i < kTfSplitIters; ++i) {
+            const uint32_t off =
+                static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
             const float4 v = lds4(xa + off);
             if (sq) {
               float q = __fmul_rn(v.x, v.x);
@@ -309,41 +337,41 @@ __global__ void __launch_bounds__(kTfThreads, 1)
               q = fmaf(v.w, v.w, q);
               kahan_add(sacc[i], scmp[i], q);
             }
-            float4 hi, lo;
-            split4(v, hi, lo);
-            sts4(xa + off, hi);
-            sts4(xa + kTfXBytes + off, lo);
+            sts4(xd + off, tf32_lo4(v));
           }
-          const uint32_t ya = xa + 2u * kTfXBytes;
+          const uint32_t ya = xa + kTfXBytes;
+          const uint32_t yd = xd + kTfXBytes;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t row = static_cast<uint32_t>(16 * w + 4 * i + sub);
+          for (int i = 0; i < kTfSplitIters; ++i) {
+            const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
             if (row < yr) {
               const uint32_t off = row * 128u + static_cast<uint32_t>(chunk * 16);
-              const float4 v = lds4(ya + off);
-              float4 hi, lo;
-              split4(v, hi, lo);
-              sts4(ya + off, hi);
-              sts4(ya + ybytes + off, lo);
+              sts4(yd + off, tf32_lo4(lds4(ya + off)));
             }
           }
           fence_async_smem_writes();
         }
         __syncwarp();
-        if (alive && lane == 0) mbar_arrive_cluster(ready0 + s * 8u);
-        if (++s == stages) {
+        if (alive && lane == 0) mbar_arrive_cluster(ready0 + q * 8u);
+        if (++s == nraw) {
           s = 0;
           phase ^= 1u;
+        }
+        ++it;
+        if (++q == kTfSplitSlots) {
+          q = 0;
+          qphase ^= 1u;
         }
       }
       if (do_sq) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < kTfSplitIters; ++i) {
           float v = __fsub_rn(sacc[i], scmp[i]);
           v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
           v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
           v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
-          const int grow = t.tile * 256 + static_cast<int>(rank) * 128 + 16 * w + 4 * i + sub;
+          const int grow =
+              t.tile * 256 + static_cast<int>(rank) * 128 + kTfSplitRows * w + 4 * i + sub;
           if (alive && chunk == 0 && grow < p.rows)
             p.out_sumsq[static_cast<size_t>(t.split) * p.rows + grow] = v;
         }
@@ -423,10 +451,17 @@ __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, 
   const int j = static_cast<int>(idx - static_cast<int64_t>(i) * rp);
   float out = 0.f;
   if (i < r && j < r) {
+    // all loads first (they are independent), then the sum in segment order
+    float v[kTf32MaxGramSplits];
+    const size_t plane = static_cast<size_t>(r) * r;
+    const float* src = parts + static_cast<size_t>(i) * r + j;
+#pragma unroll
+    for (int sp = 0; sp < kTf32MaxGramSplits; ++sp) v[sp] = sp < splits ? __ldg(src + sp * plane) : 0.f;
     df acc{0.f, 0.f};
-    for (int sp = 0; sp < splits; ++sp) {
+#pragma unroll
+    for (int sp = 0; sp < kTf32MaxGramSplits; ++sp) {
       float e;
-      two_sum(acc.hi, parts[(static_cast<size_t>(sp) * r + i) * r + j], acc.hi, e);
+      two_sum(acc.hi, v[sp], acc.hi, e);
       acc.lo = __fadd_rn(acc.lo, e);
     }
     out = __fmul_rn(scale, __fadd_rn(acc.hi, acc.lo));
@@ -436,9 +471,13 @@ __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, 
 
 }  // namespace
 
+// `stages` raw slots plus the split slots and the barriers
 size_t tf32_smem_bytes(int n_pass, int stages) {
-  const size_t stage = 2 * static_cast<size_t>(kTfXBytes) + 2 * static_cast<size_t>(n_pass / 2) * 128u;
-  return 1024 + stage * static_cast<size_t>(stages) + (3 * static_cast<size_t>(stages) + 4) * 8 + 16;
+  const size_t ybytes = static_cast<size_t>(n_pass / 2) * 128u;
+  const size_t raw = kTfXBytes + ybytes;
+  const size_t sp = kTfXBytes + ybytes;
+  return 1024 + raw * static_cast<size_t>(stages) + sp * kTfSplitSlots +
+         (2 * static_cast<size_t>(stages) + 2 * kTfSplitSlots + 4) * 8 + 16;
 }
 
 int tf32_pick_stages(int n_pass) {

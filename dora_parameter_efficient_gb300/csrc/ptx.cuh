@@ -403,13 +403,11 @@ __device__ __forceinline__ void fence_async_smem_writes() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// v rounded to TF32 (10 fraction bits), to nearest with ties away from zero,
-// returned in an fp32 container whose low 13 fraction bits are zero.  Plain
-// bit arithmetic on the IEEE encoding: adding half of the dropped unit to the
-// magnitude bits and clearing them rounds the magnitude (a carry moves into
-// the exponent as it should).  Finite inputs below the largest TF32 value.
-__device__ __forceinline__ float tf32_round(float v) {
-  return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
+// v truncated to TF32 (sign, exponent, top 10 fraction bits; the low 13
+// fraction bits cleared): the value a kind::tf32 MMA reads from an fp32
+// container.
+__device__ __forceinline__ float tf32_trunc(float v) {
+  return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
 }
 
 }  // namespace dora

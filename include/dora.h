@@ -70,10 +70,11 @@ typedef enum dora_dtype {
  * Bytes of device workspace dora_factored_norm needs for this shape.
  * The workspace holds a small control block (the device status word, the
  * main pass's work counter and per-row-group completion counters, zeroed by
- * every call), the Gram matrix G = A A^T (fp32, for fp32 inputs) or its
- * scaled bf16 split G'_hi + G'_lo (for bf16 inputs), and per-segment partial
- * sums of the norm terms.  It does not depend on d_in: about 1.8 MB at
- * d_out = 8192, r = 384 (bf16) and 2.4 MB at d_out = 8192, r = 512 (fp32).
+ * every call), the scaled Gram matrix G' = (s/2) A A^T -- as a bf16 split
+ * G'_hi + G'_lo for bf16 inputs; in fp32, with the K-segment partials of
+ * A A^T (up to 16 x r x r), for fp32 inputs -- and per-segment partial sums
+ * of the norm terms.  It does not depend on d_in: about 1.6 MB at
+ * d_out = 8192, r = 384 (bf16) and 18.9 MB at d_out = 8192, r = 512 (fp32).
  * Returns 0 for an invalid shape (negative sizes, bad dtype, r > DORA_MAX_RANK).
  */
 size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtype);
@@ -99,8 +100,12 @@ size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtyp
  * Requirements (else DORA_ERR_UNSUPPORTED): d_in * elem_size and r * elem_size
  * multiples of 16 bytes; W, A, B 16-byte aligned; r <= DORA_MAX_RANK.
  * wnorm and g must not overlap each other or any input.
- * Precision: products of the stored inputs are exact in fp32, every sum is
- * accumulated in fp32; the three terms are assembled in double-float
+ * Precision: for bf16 inputs every product of stored values is exact in
+ * fp32; for fp32 inputs the products of W A^T, A A^T and B G' are each
+ * formed from three TF32 tensor-core products (hi*hi + lo*hi + hi*lo, the
+ * "3xTF32" scheme: a few units of 2^-20 relative), and the sum of squares
+ * of W is taken in fp32 on the CUDA cores.  Every sum is accumulated in
+ * fp32; the three terms are assembled in double-float
  * arithmetic (a value held as an unevaluated sum of two floats, about 48
  * significant bits), the square root and the division each take one
  * correction step in that arithmetic, and each result is rounded once to fp32.
@@ -134,8 +139,10 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
  * Arguments, results and requirements are those of dora_factored_norm.  The
  * workspace is instead a 32 MiB array in the library's own device memory
  * (a file-scope __device__ array): every GPU that loads the library holds it
- * until the process exits.  32 MiB covers d_out up to 203 120 rows at
- * r = 512 (216 824 at r = 384, 246 180 at r = 128); a shape whose
+ * until the process exits.  32 MiB covers d_out up to 253 888 rows at
+ * r = 512 (257 468 at r = 384, 261 564 at r = 128) for bf16 inputs and
+ * 122 848 rows at r = 512 (183 760 at r = 384, 253 376 at r = 128) for fp32
+ * inputs; a shape whose
  * dora_norm_workspace_size exceeds 32 MiB is refused with DORA_ERR_WORKSPACE
  * before anything is enqueued.
  *   - The first call on each device looks up the array's device address

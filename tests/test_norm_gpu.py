@@ -188,6 +188,36 @@ def test_small_integers_bit_exact(dtype, d_out, d_in, r, ab_max):
     np.testing.assert_array_equal(g, g_ref.astype(np.float32))
 
 
+def test_fp32_low_bits_reach_the_tensor_cores():
+    """fp32 operands whose bits below the TF32 precision are set, chosen so
+    that the part the tensor core does not read (v minus v truncated to 10
+    fraction bits) is itself a TF32 value: the three-term product is then
+    exact.  U, the cross term and the BA-norm term are of the size of the
+    base term, so a pass that dropped or double-counted those bits (2^-10
+    relative) would miss the oracle by about 1e-4; the tolerance is 1e-6."""
+    d_out, d_in, r, s = 256, 64, 16, 1.0
+    j = np.arange(d_out)
+    sign = np.where(j % 2 == 0, 1.0, -1.0)
+    a = sign * (1.0 + (j % 7) * 2.0 ** -10 + 2.0 ** -11 + 2.0 ** -13 + 2.0 ** -19)
+    b = 1.0 + 2.0 ** -11 + 2.0 ** -15
+    W = np.zeros((d_out, d_in), np.float32)
+    W[:, 0] = a                      # low bits in W
+    W[:, 1] = 1.0
+    A = np.zeros((r, d_in), np.float32)
+    A[0, 0] = 1.0
+    A[1, 1] = b                      # low bits in A
+    B = np.zeros((d_out, r), np.float32)
+    B[:, :2] = 1.0
+    m = np.ones(d_out, np.float32)
+    for v in (W, A):
+        assert np.all(v.astype(np.float64) == v)          # exactly representable
+    x = {"W": W, "A": A, "B": B, "m": m}
+    cfg = _custom("tf32bits", configs.F32, d_out, d_in, r, s)
+    wn, g = _run(x, cfg)
+    wn_ref, g_ref = _oracle(x, cfg)
+    _check(cfg, wn, g, wn_ref, g_ref)
+
+
 @pytest.mark.parametrize("dtype", [configs.BF16, configs.F32])
 def test_cancelling_adapter_clamps_to_zero(dtype):
     """W = -s B A exactly: the factored sum is exactly zero, the clamp keeps the
