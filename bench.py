@@ -336,6 +336,9 @@ def run_fp32(api, dev, peaks, calls=20):
     wn = torch.empty(d_out, device=dev)
     g = torch.empty(d_out, device=dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(calls)]
+    for e in evs:            # create the CUDA events (the library records e[1], e[2])
+        for x in e:
+            x.record()
     for _ in range(3):
         api.dora_factored_norm(W, A, B, cfg.s, m, cfg.eps, wnorm=wn, g=g, workspace=ws)
     torch.cuda.synchronize()

@@ -27,6 +27,7 @@ constexpr int kMaxMainSplits = 16;
 #define DORA_GRAM_CLUSTER 8
 #endif
 constexpr int kGramCluster = DORA_GRAM_CLUSTER;   // CTAs (K splits) per Gram block
+constexpr int kGramClusterGrouped = 2;            // the same for a grouped launch
 constexpr int kGramStages = 6;
 static_assert(kMaxMainSplits <= kMaxFinalParts, "the fused finalize sums at most kMaxFinalParts splits");
 constexpr int kMaxDevices = 64;
@@ -760,7 +761,12 @@ int grouped_run(const NormGroupedPlan& P, float s, float eps, cudaStream_t strea
   pg.rp = rp;
   pg.k_tiles = P.min_kt;
   pg.stages = kGramStages;
-  pg.cluster = kGramCluster;
+  // Many modules fill the grid with blocks of their own: a short K split
+  // (2 CTAs per block) beats the single-module choice of 8, whose per-CTA
+  // setup and cluster-wide reduction then dominate (196-module stack at
+  // r = 128 on one GB300: 2.87 ms per grouped norm with 1 or 2, 2.89 with 4,
+  // 2.96 with 8).
+  pg.cluster = kGramClusterGrouped;
   while (pg.cluster > 1 && pg.cluster > P.min_kt) pg.cluster >>= 1;
   pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
   pg.scale = 0.5f * s;
