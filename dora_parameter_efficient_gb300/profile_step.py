@@ -5,6 +5,10 @@ step also runs the training path of the compose (forward keeping inner,
 backward with the magnitude gradient).
 
     python -m dora_parameter_efficient_gb300.profile_step --config 1 --steps 3 [--training]
+
+With --grouped it runs every module of the config instead (the 196-module
+stack: --config 4) as one grouped norm per step through a plan created once,
+then one grouped compose, with inputs drawn on the device.
 """
 from __future__ import annotations
 
@@ -29,14 +33,50 @@ def to_dev(a: np.ndarray, dtype: str) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
+def run_grouped(cfg, steps: int) -> int:
+    gen_t = torch.Generator(device="cuda")
+    gen_t.manual_seed(cfg.index)
+    dt = torch.bfloat16 if cfg.dtype == configs.BF16 else torch.float32
+
+    def rnd(*shape, std):
+        return (torch.randn(*shape, device="cuda", generator=gen_t) * std).to(dt)
+
+    norm_mods, comp_mods = [], []
+    for mod in cfg.modules:
+        norm_mods.append((rnd(mod.d_out, mod.d_in, std=cfg.std_w),
+                          rnd(cfg.r, mod.d_in, std=cfg.std_a(mod.d_in)),
+                          rnd(mod.d_out, cfg.r, std=cfg.std_b),
+                          torch.ones(mod.d_out, dtype=dt, device="cuda")))
+    plan = api.dora_norm_grouped_plan_create(norm_mods)
+    for (W, *_), g in zip(norm_mods, plan.gs):
+        comp_mods.append((rnd(cfg.tokens, W.shape[0], std=cfg.std_base),
+                          rnd(cfg.tokens, W.shape[0], std=cfg.std_lora), g))
+    outs = [torch.empty_like(b) for b, _, _ in comp_mods]
+    for i in range(steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        plan.run(cfg.s, cfg.eps)
+        e[1].record()
+        api.dora_compose_grouped(comp_mods, cfg.s, outs=outs)
+        e[2].record()
+        torch.cuda.synchronize()
+        print(f"step {i}: grouped norm {e[0].elapsed_time(e[1]) * 1e3:.1f} us, "
+              f"grouped compose {e[1].elapsed_time(e[2]) * 1e3:.1f} us")
+    plan.destroy()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--module", type=int, default=0)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--training", action="store_true")
+    ap.add_argument("--grouped", action="store_true")
     args = ap.parse_args()
     cfg = configs.get(args.config)
+    if args.grouped:
+        return run_grouped(cfg, args.steps)
     x = gen.norm_inputs(cfg, module=args.module)
     c = gen.compose_inputs(cfg, module=args.module)
     W, A, B, m = (to_dev(x[k], cfg.dtype) for k in ("W", "A", "B", "m"))
