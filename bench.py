@@ -367,6 +367,11 @@ def run_fp32(api, dev, peaks, calls=20):
            "main_pass_tf32_TFLOP/s": mma_flops / (main_ms * 1e-3) / 1e12,
            "main_pass_frac_of_measured_derived_tf32": mma_flops / (main_ms * 1e-3) / 1e12 / tf32_peak,
            "tf32_peak_note": "measured bf16 burst x the nominal tf32 / bf16 ratio (1100 / 2250)",
+           # W, A, B, G' once; the segment partials (at most 16 + 16 fp32 per row)
+           "main_pass_algorithmic_bytes": 4 * (d_out * d_in + r * d_in + d_out * r + rp * rp),
+           "main_pass_traffic": recorded_traffic(
+               os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "gemm_tf32.cu"),
+               "tf32_pass_8192x8192_r512_f32.md"),
            "data": "drawn on the device (torch.randn, seeded) with the config's distributions; "
                    "m = 1 (timing only)",
            "timing": f"CUDA events, mean over {calls} calls (W is 256 MB, larger than L2)"}
