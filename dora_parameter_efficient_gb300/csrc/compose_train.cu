@@ -23,6 +23,7 @@
 // order (compensated) and divide.  Anything else takes element-wise kernels
 // with the same arithmetic.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dora {
 
@@ -164,6 +165,9 @@ __global__ void __launch_bounds__(kTrainThreads, 4)
                      uint4* __restrict__ d_base, uint4* __restrict__ d_lora,
                      float* __restrict__ partials) {
   constexpr int N = Vec<BF16>::N;
+  // the finish kernel may be scheduled as blocks of this grid exit; it
+  // waits for the whole grid (griddep_wait) before reading the partials
+  if (DM) griddep_launch_dependents();
   const int64_t c = static_cast<int64_t>(blockIdx.x) * kTrainThreads + threadIdx.x;
   if (c >= dv) return;
   float gv[N], gm[N], acc[N];
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(256)
                     const float* __restrict__ g, float s, int64_t T, int64_t d_out,
                     void* __restrict__ d_base, void* __restrict__ d_lora,
                     float* __restrict__ partials) {
+  if (DM) griddep_launch_dependents();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= d_out) return;
   const float gj = g[j], gm = __fsub_rn(gj, 1.0f);
@@ -237,30 +242,31 @@ __global__ void __launch_bounds__(256)
 
 // dmag_j = (sum over p of partials[p][j]) / max(wnorm_j, eps).  A block of
 // 256 threads takes 32 columns: warp w sums parts [w n / 8, (w + 1) n / 8)
-// for column lane (compensated, four loads in flight), then warp 0 adds the
-// eight warp sums in warp order.  The order depends only on n: the same
-// result on every call.
+// for column lane (compensated; the at most 32 loads of a warp's range are
+// all issued before the first add), then warp 0 adds the eight warp sums in
+// warp order.  The order depends only on n: the same result on every call.
+// Launched as a programmatic dependent of the backward kernel.
 constexpr int kFinishCols = 32;
 constexpr int kFinishWarps = 8;
+constexpr int kFinishPartsPerWarp = (kMaxDmParts + kFinishWarps - 1) / kFinishWarps;
 
 __global__ void __launch_bounds__(kFinishCols * kFinishWarps)
     k_train_dm_finish(const float* __restrict__ partials, int nparts, int64_t d_out,
                       const float* __restrict__ wnorm, float eps, float* __restrict__ dmag) {
   __shared__ float ws_sum[kFinishWarps][kFinishCols], ws_cmp[kFinishWarps][kFinishCols];
+  griddep_wait();            // the partials of the backward kernel
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t j = static_cast<int64_t>(blockIdx.x) * kFinishCols + lane;
   const bool ok = j < d_out;
   const int p0 = (nparts * w) / kFinishWarps, p1 = (nparts * (w + 1)) / kFinishWarps;
+  float v[kFinishPartsPerWarp];
+#pragma unroll
+  for (int u = 0; u < kFinishPartsPerWarp; ++u)
+    v[u] = (ok && p0 + u < p1) ? partials[static_cast<int64_t>(p0 + u) * d_out + j] : 0.f;
   float sum = 0.f, comp = 0.f;
-  int p = p0;
-  for (; p + 4 <= p1; p += 4) {
-    float v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = ok ? partials[static_cast<int64_t>(p + u) * d_out + j] : 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) kahan_add(sum, comp, v[u]);
-  }
-  for (; p < p1; ++p) kahan_add(sum, comp, ok ? partials[static_cast<int64_t>(p) * d_out + j] : 0.f);
+  for (int u = 0; u < kFinishPartsPerWarp; ++u)
+    if (p0 + u < p1) kahan_add(sum, comp, v[u]);
   ws_sum[w][lane] = sum;
   ws_cmp[w][lane] = comp;
   __syncthreads();
@@ -375,10 +381,19 @@ cudaError_t launch_compose_backward(const void* dout, const void* inner, const f
   note_launches(1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !dm) return e;
-  k_train_dm_finish<<<static_cast<unsigned>((d_out + kFinishCols - 1) / kFinishCols),
-                      kFinishCols * kFinishWarps, 0, stream>>>(
-      partials, static_cast<int>(nparts), d_out, wnorm, eps, dmag);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((d_out + kFinishCols - 1) / kFinishCols), 1, 1);
+  cfg.blockDim = dim3(kFinishCols * kFinishWarps, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_train_dm_finish, static_cast<const float*>(partials),
+                         static_cast<int>(nparts), d_out, wnorm, eps, dmag);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
