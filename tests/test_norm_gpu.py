@@ -98,7 +98,11 @@ def test_config4_stack_layer0_sampled_rows(module):
     (configs.BF16, 640, 4096, 384, 1.0),     # several K splits
     (configs.F32, 200, 136, 24, 1.5),
     (configs.F32, 65, 36, 4, 2.0),
-    (configs.F32, 70, 100, 512, 0.5),
+    (configs.F32, 70, 100, 512, 0.5),        # two N passes of 256
+    (configs.F32, 300, 260, 300, 1.0),       # two N passes of 160 (80-row Y halves), K tail
+    (configs.F32, 1000, 1028, 384, -0.75),   # two N passes of 192, four pair tiles, K tail
+    (configs.F32, 520, 2048, 128, 2.0),      # one pass of 128, many K segments
+    (configs.F32, 1, 4, 8, 1.0),             # single row, single short K tile
 ])
 def test_edge_shapes(dtype, d_out, d_in, r, s):
     cfg = _custom(f"edge-{dtype}-{d_out}x{d_in}-r{r}", dtype, d_out, d_in, r, s)
