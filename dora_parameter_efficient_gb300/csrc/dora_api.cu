@@ -216,22 +216,30 @@ int pick_pair_splits(int64_t pair_tiles, int64_t k_tiles, int clusters, int max_
   return best;
 }
 
-// K segments of each pair tile.  With enough tiles to go round, three
-// segments of relative lengths 3 : 2 : 1 (long work first, short work to even
-// out the finish; on one GB300 at 8192 x 8192, r = 384 this beat 4:3:2:1,
-// 5:4:3:2:1, 4:3:2, 5:3:2 and 2:1 -- every extra item costs an accumulator
-// drain); with few tiles, equal segments, as many as keep the pairs busy.
+// K segments of each pair tile: long work first, short work to even out the
+// finish; every extra item costs an accumulator drain.  With fewer pair tiles
+// than pairs, each pair runs one or two items and the long first items set
+// the finish: relative lengths 7 : 4 : 2 (on one GB300 at 8192 x 8192,
+// r = 384 -- 140 K tiles, 32 pair tiles, 76 pairs of which the 24 that share
+// SMs with the Gram kernel start late -- 7:4:2 and 9:5:3 took 49.3 us per
+// norm, 3:2:1 51.0, 4:2:1 51.4, 7:3:2 52.8; four or more segments were
+// slower).  With more pair tiles than pairs, 3 : 2 : 1 (28672 x 8192, 112
+// pair tiles: 140.0 us against 142.3 with 7:4:2).  With few tiles, equal
+// segments, as many as keep the pairs busy.
 void plan_pair_segments(PairParams& pp, int clusters) {
   const int ktot = pp.kt_w + 2 * pp.kt_b;
   int nseg;
   if (3 * static_cast<int64_t>(pp.pair_tiles) >= clusters && ktot >= 6) {
-    static const int w[3] = {3, 2, 1};
+    static const int w_few[3] = {7, 4, 2};
+    static const int w_many[3] = {3, 2, 1};
+    const int* w = pp.pair_tiles < clusters ? w_few : w_many;
+    const int wsum = w[0] + w[1] + w[2];
     nseg = 3;
     int acc = 0;
     pp.seg_k[0] = 0;
     for (int i = 0; i < 3; ++i) {
       acc += w[i];
-      pp.seg_k[i + 1] = static_cast<int>((static_cast<int64_t>(ktot) * acc + 3) / 6);
+      pp.seg_k[i + 1] = static_cast<int>((static_cast<int64_t>(ktot) * acc + wsum / 2) / wsum);
     }
   } else {
     nseg = pick_pair_splits(pp.pair_tiles, ktot, clusters, kMaxMainSplits);

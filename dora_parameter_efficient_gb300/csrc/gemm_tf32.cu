@@ -12,8 +12,9 @@
 // The tensor core reads lo in turn to TF32 (an error below 2^-10 |lo|), and
 // the dropped x_lo y_lo is below 2^-20 of the product, so each product is
 // good to a few units of 2^-20.  Small integers split into hi = v, lo = 0,
-// so integer-valued inputs still give exact results.  The sum of squares of W is taken on the CUDA cores from the raw
-// fp32 tile, compensated across tiles.
+// so integer-valued inputs still give exact results.  The sum of squares of
+// W is taken on the CUDA cores from the raw fp32 tile, compensated across
+// tiles.
 //
 // Two modes (template argument kStore):
 //   * norm: for each row j of W and each work item (pair tile, N pass, K
