@@ -43,9 +43,11 @@
 //   * warps 18-21 (one per TMEM lane quadrant) drain the accumulator of each
 //     item -- two TMEM buffers, used by alternate items, so the MMAs of the
 //     next item run meanwhile.
-// The split slots are busy only from the split to the MMAs, so two of them
-// leave the rest of shared memory to raw slots: the loads run several
-// stages ahead of the MMAs.
+// The split slots are busy only from the split to the MMAs: three of them
+// give the split of the next stages slack against the MMAs and leave the
+// rest of shared memory to raw slots, so the loads run several stages ahead
+// (8192 x 8192, r = 512 on one GB300: 322 us per norm with 3 split + 4 raw
+// slots, 338 with 2 + 5, 343 with 4 + 3).
 // The grid is persistent and the items are striped over it (cluster c takes
 // items c, c + clusters, ...): they are of equal size, and every role walks
 // the same sequence with no hand-off.  Every wait is bounded by %globaltimer;
@@ -66,7 +68,7 @@ constexpr int kTfSplitRows = 128 / kTfSplitWarps;   // tile rows per split warp
 constexpr int kTfSplitIters = kTfSplitRows / 4;     // one warp instruction covers 4 rows
 constexpr int kTfDrainWarps = 4;
 constexpr uint32_t kTfXBytes = 128u * 128u;   // [128 rows x 32 fp32], 128-byte swizzle
-constexpr uint32_t kTfSplitSlots = 2;
+constexpr uint32_t kTfSplitSlots = 3;
 
 __device__ __forceinline__ float4 lds4(uint32_t addr) {
   float4 v;
