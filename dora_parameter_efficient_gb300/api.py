@@ -330,6 +330,16 @@ def dora_check_status(workspace: torch.Tensor,
                                              _stream_handle(stream)))
 
 
+def dora_selftest_timeout(workspace: torch.Tensor, timeout_us: int,
+                          stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Enqueues the failure-detection self-test on `workspace` (a wait that
+    runs out after `timeout_us` and records DORA_ERR_TIMEOUT; read it with
+    dora_check_status)."""
+    st = _lib.load().dora_selftest_timeout(_dev(workspace, "workspace"), workspace.numel(),
+                                           int(timeout_us), _stream_handle(stream))
+    check(st, "dora_selftest_timeout")
+
+
 def dora_factored_norm_noalloc(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
                                m: torch.Tensor, eps: float, wnorm: torch.Tensor,
                                g: torch.Tensor,

@@ -178,6 +178,8 @@ cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int r
                                     float* Gp, cudaStream_t stream);
 
 // ------------------------------------------------------------------ small kernels
+cudaError_t launch_selftest_timeout(int* status, unsigned long long timeout_ns,
+                                    cudaStream_t stream);
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,
                              float* out, cudaStream_t stream);
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,

@@ -1094,6 +1094,20 @@ int dora_compose_backward(const void* d_out_grad, const void* inner, const float
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned timeout_us,
+                          void* stream) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < 256)
+    return DORA_ERR_WORKSPACE;
+  if (timeout_us == 0 || timeout_us > 1000000u) return DORA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = static_cast<int*>(workspace);
+  DORA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
+  return cuda_status(launch_selftest_timeout(status, 1000ull * timeout_us, st));
+}
+
 int dora_check_status(const void* workspace, void* stream) {
   if (!workspace) return DORA_ERR_INVALID_ARG;
   int h = -1;

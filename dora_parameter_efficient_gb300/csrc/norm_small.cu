@@ -3,6 +3,7 @@
 // the Chinese write-up, section 5.1, notes: no U and no G when s = 0) and
 // the stand-alone finalize of finalize.cuh, which adds the K-segment
 // partials of the fp32 pass in segment order and assembles wnorm and g.
+// Also the self-test of the device-side failure detection.
 #include "common.cuh"
 #include "finalize.cuh"
 #include "ptx.cuh"
@@ -85,7 +86,26 @@ __global__ void __launch_bounds__(64)
   finalize_row(base, cross, n_ba > 0 ? &ba : nullptr, two_s, s_sq, mj, eps, wnorm[j], g[j]);
 }
 
+// One thread waits, with the pipelines' bounded wait, on an mbarrier that
+// nothing arrives on; when the limit passes it records the timeout in the
+// status word, as a pipeline role does, and the kernel returns.
+__global__ void k_selftest_timeout(int* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0u, global_timer_ns() + timeout_ns)) atomicExch(status, kStatusTimeout);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_timeout(int* status, unsigned long long timeout_ns,
+                                    cudaStream_t stream) {
+  k_selftest_timeout<<<1, 32, 0, stream>>>(status, timeout_ns);
+  note_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols, float* out,
                              cudaStream_t stream) {

@@ -336,6 +336,20 @@ int dora_compose_backward(const void* d_out_grad, const void* inner, const float
  */
 int dora_check_status(const void* workspace, void* stream);
 
+/*
+ * Self-test of the device-side failure detection: zeroes the status word at
+ * the start of `workspace` (256-byte aligned, at least 256 bytes), then runs
+ * one block that waits -- with the bounded wait every pipeline role uses -- on
+ * a barrier that nothing completes, gives up after `timeout_us` microseconds
+ * (1 .. 1 000 000) and records DORA_ERR_TIMEOUT in that word, as a pipeline
+ * role does when a wait runs out.  The kernel then returns and the CUDA
+ * context stays usable; dora_check_status(workspace, stream) reads the word.
+ * Returns DORA_ERR_WORKSPACE / DORA_ERR_INVALID_ARG for bad arguments before
+ * anything is enqueued.
+ */
+int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned timeout_us,
+                          void* stream);
+
 /* Number of CUDA kernels this library has launched in this process so far
  * (all devices, all entry points); a diagnostic counter. */
 uint64_t dora_launch_count(void);

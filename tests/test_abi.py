@@ -190,3 +190,11 @@ def test_grouped_plan_rejects_before_the_gpu(lib):
         assert st == _lib.DORA_ERR_WORKSPACE and not h.value
     assert lib.dora_norm_grouped_plan_run(None, 1.0, 1e-6, None) == _lib.DORA_ERR_INVALID_ARG
     lib.dora_norm_grouped_plan_destroy(None)
+
+
+def test_selftest_timeout_rejects_before_the_gpu(lib):
+    assert lib.dora_selftest_timeout(None, 1 << 20, 1000, None) == _lib.DORA_ERR_WORKSPACE
+    assert lib.dora_selftest_timeout(8 * P + 16, 1 << 20, 1000, None) == _lib.DORA_ERR_WORKSPACE
+    assert lib.dora_selftest_timeout(8 * P, 128, 1000, None) == _lib.DORA_ERR_WORKSPACE
+    assert lib.dora_selftest_timeout(8 * P, 1 << 20, 0, None) == _lib.DORA_ERR_INVALID_ARG
+    assert lib.dora_selftest_timeout(8 * P, 1 << 20, 2_000_000, None) == _lib.DORA_ERR_INVALID_ARG
