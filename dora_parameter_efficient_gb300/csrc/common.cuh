@@ -127,8 +127,10 @@ struct PairParams {
   int n_items;
 };
 
-size_t pair_smem_bytes(int n_pad, int stages);
-int pair_pick_stages(int n_pad);
+// modules of a grouped launch whose first item is kept in shared memory
+constexpr int kPairModCache = 2048;
+size_t pair_smem_bytes(int n_pad, int stages, bool grouped);
+int pair_pick_stages(int n_pad, bool grouped);
 int pair_max_clusters(size_t smem_bytes);
 cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const CUtensorMap& tB,
                              const CUtensorMap& tGhi, const CUtensorMap& tGlo, const PairParams& p,

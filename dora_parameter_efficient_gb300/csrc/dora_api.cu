@@ -372,8 +372,8 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     pp.kt_w = k_tiles;
     pp.kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
     pp.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
-    pp.stages = pair_pick_stages(rp);
-    const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages));
+    pp.stages = pair_pick_stages(rp, false);
+    const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, false));
     if (clusters_max <= 0) return DORA_ERR_CUDA;
     plan_pair_segments(pp, clusters_max);
     pp.r = static_cast<int>(r);
@@ -651,7 +651,8 @@ int grouped_prepare(const dora_norm_module* mods, int n, int dtype, int64_t r, v
   // K segments only when the pair tiles of all modules are too few to fill
   // the persistent grid a few times over; a stack of many modules fills it
   // with whole-K items, each one accumulator drain.
-  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pair_pick_stages(rp)));
+  const int clusters_max =
+      pair_max_clusters(pair_smem_bytes(rp, pair_pick_stages(rp, true), true));
   if (clusters_max <= 0) return DORA_ERR_CUDA;
   int64_t total_pairs = 0;
   for (int i = 0; i < n; ++i) total_pairs += ceil_div(mods[i].d_out, 2 * kTcBlockM);
@@ -787,8 +788,8 @@ int grouped_run(const NormGroupedPlan& P, float s, float eps, cudaStream_t strea
   pp.n1 = n1;
   pp.y_box_rows = y_box2;
   pp.kt_b = kt_b;
-  pp.stages = pair_pick_stages(rp);
-  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages));
+  pp.stages = pair_pick_stages(rp, true);
+  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, true));
   if (clusters_max <= 0) return DORA_ERR_CUDA;
   pp.r = static_cast<int>(r);
   pp.acc_stride = tmem_cols;

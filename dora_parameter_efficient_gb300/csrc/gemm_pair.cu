@@ -140,12 +140,18 @@ __device__ __forceinline__ ModView single_view(const PairParams& p, const CUtens
                  p.tile_done, p.rows, p.kt_w, p.pair_tiles, p.splits, 0, p.seg_k};
 }
 
-// the module of a work item in a grouped launch (modules in item order)
-__device__ __forceinline__ ModView module_view(const PairParams& p, int item) {
+// the module of a work item in a grouped launch (modules in item order): a
+// binary search over the modules' first items, read from the copy in shared
+// memory (`begins`, the first kPairModCache modules) -- in global memory the
+// search is a chain of dependent L2 reads that held up every item's first
+// load and first MMA by a few microseconds
+__device__ __forceinline__ ModView module_view(const PairParams& p, const int* begins, int item) {
+  const bool cached = p.n_mods <= kPairModCache;
   int lo = 0, hi = p.n_mods - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.mods[mid].item_begin <= item) lo = mid;
+    const int b = cached ? begins[mid] : p.mods[mid].item_begin;
+    if (b <= item) lo = mid;
     else hi = mid - 1;
   }
   const PairModule& md = p.mods[lo];
@@ -155,8 +161,9 @@ __device__ __forceinline__ ModView module_view(const PairParams& p, int item) {
 }
 
 template <bool kGrouped>
-__device__ __forceinline__ ModView view_of(const PairParams& p, const ModView& single, int item) {
-  if constexpr (kGrouped) return module_view(p, item);
+__device__ __forceinline__ ModView view_of(const PairParams& p, const ModView& single,
+                                           const int* begins, int item) {
+  if constexpr (kGrouped) return module_view(p, begins, item);
   else return single;
 }
 
@@ -225,6 +232,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint64_t* item_empty = item_full + kItemRing;
   volatile int* item_slot = reinterpret_cast<volatile int*>(item_empty + kItemRing);
   volatile int* last_flag = item_slot + kItemRing;   // this CTA finished the last segment of its rows
+  // grouped launch: the first item of each module (up to kPairModCache)
+  int* mod_begin = reinterpret_cast<int*>(
+      (reinterpret_cast<uintptr_t>(last_flag + 1) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -261,6 +271,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (warp == 1) {
     tmem_alloc_pair(tmem_holder, p.tmem_cols);
     tmem_relinquish_pair();
+  }
+  if (kGrouped && p.n_mods <= kPairModCache) {
+    for (int i = threadIdx.x; i < p.n_mods; i += kPairThreads) mod_begin[i] = p.mods[i].item_begin;
   }
   tc_fence_before_sync();
   cluster_sync();          // barriers of both CTAs initialised, TMEM allocated in both
@@ -303,7 +316,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
         }
         if (item < 0) break;
-        const ModView mv = view_of<kGrouped>(p, single, item);
+        const ModView mv = view_of<kGrouped>(p, single, mod_begin, item);
         if (kGrouped) {
           tma_prefetch_desc(mv.tW);
           tma_prefetch_desc(mv.tA);
@@ -387,7 +400,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
         if (item < 0) break;
         int tile, split, kb, ke;
-        item_range(view_of<kGrouped>(p, single, item), item, tile, split, kb, ke);
+        item_range(view_of<kGrouped>(p, single, mod_begin, item), item, tile, split, kb, ke);
         // accumulator buffer of this item, and how often it was used before
         const uint32_t buf = static_cast<uint32_t>(icount) % nbuf;
         const uint32_t use = static_cast<uint32_t>(icount) / nbuf;
@@ -478,7 +491,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             : "memory");
         if (!all_ok) break;
       }
-      const ModView mv = view_of<kGrouped>(p, single, item);
+      const ModView mv = view_of<kGrouped>(p, single, mod_begin, item);
       int tile, split, kb, ke;
       item_range(mv, item, tile, split, kb, ke);
       const int rowbase = tile * 256 + static_cast<int>(rank) * 128 + q * 32;
@@ -659,16 +672,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 }  // namespace
 
-size_t pair_smem_bytes(int n_pad, int stages) {
+size_t pair_smem_bytes(int n_pad, int stages, bool grouped) {
   const size_t stage = kTcXTileBytes + static_cast<size_t>(n_pad / 2) * 128u;
   return 1024 + stage * stages + (3 * stages + 4) * 8 + 16 + 2 * 128 * 4 +
-         2 * kItemRing * 8 + kItemRing * 4 + 4;
+         2 * kItemRing * 8 + kItemRing * 4 + 4 + (grouped ? 16 + 4 * kPairModCache : 0);
 }
 
-int pair_pick_stages(int n_pad) {
+int pair_pick_stages(int n_pad, bool grouped) {
   const size_t budget = 227 * 1024;
   int st = kTcMaxStages;
-  while (st > 2 && pair_smem_bytes(n_pad, st) > budget) --st;
+  while (st > 2 && pair_smem_bytes(n_pad, st, grouped) > budget) --st;
   return st;
 }
 
@@ -710,7 +723,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages);
+  cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages, false);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -735,7 +748,7 @@ cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStre
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages);
+  cfg.dynamicSmemBytes = pair_smem_bytes(p.n0 + p.n1, p.stages, true);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
