@@ -199,3 +199,27 @@ def test_many_modules_whole_k_items():
         wn1, _ = api.dora_factored_norm(*mods[k][:3], 0.75, mods[k][3], 1e-6)
         assert rel_err(wns[k].cpu().numpy(), wn1.cpu().numpy()).max() <= 2e-6
     plan.destroy()
+
+
+def test_more_modules_than_the_shared_memory_cache():
+    """2100 modules: more than the main pass keeps in shared memory, so the
+    item -> module search reads the module table in global memory."""
+    n = 2100
+    cfg = configs.Config("many", 60, configs.BF16, (configs.Module("many", 256, 64),), r=16,
+                         s=1.0, eps=1e-6, tokens=8)
+    x = gen.norm_inputs(cfg, seed=9)
+    base = _dev_module(x, configs.BF16)
+    # distinct modules: each a copy scaled by a power of two (exact in bf16),
+    # so every result follows from the first module's (the norm is homogeneous
+    # of degree 1 in W and B; g = m / wnorm with m scaled alike is unchanged)
+    scales = [2.0 ** ((i % 5) - 2) for i in range(n)]
+    mods = [(base[0] * sc, base[1], base[2] * sc, base[3] * sc) for sc in scales]
+    plan = api.dora_norm_grouped_plan_create(mods)
+    wns, gs = plan.run(cfg.s, cfg.eps)
+    torch.cuda.synchronize()
+    wn_ref, g_ref = oracle.norm_and_scale(x["W"], x["A"], x["B"], x["m"], cfg.s,
+                                          float(np.float32(cfg.eps)), cfg.dtype)
+    for i in (0, 1, 777, 2047, 2048, 2099):
+        assert rel_err(wns[i].cpu().numpy() / scales[i], wn_ref).max() <= NORM_RTOL[cfg.dtype]
+        assert rel_err(gs[i].cpu().numpy(), g_ref).max() <= NORM_RTOL[cfg.dtype]
+    plan.destroy()
