@@ -126,31 +126,11 @@ constexpr int kCtlWork = 32, kCtlTileDone = 64;
 struct Plan {
   bool bf16 = true;
   int rp = 0;               // r rounded up to 16 (the MMA N extent)
-  int main_splits = 1;      // split-K of the main pass (tensor-core path)
-  int gram_splits = 1;
   size_t off_status = 0, zero_bytes = 0, off_G = 0, off_Ghi = 0, off_Glo = 0;
   size_t off_Gpart = 0;     // fp32: K-segment partials of G
   size_t off_pbase = 0, off_pcross = 0, total = 0;
   int cap_base = 0, cap_cross = 0;
 };
-
-// Split-K count: minimise (waves x K tiles per CTA) plus a per-wave epilogue
-// cost of about two K tiles, for `units` row tiles on `sms` SMs.
-int pick_splits(int64_t row_tiles, int64_t k_tiles, int sms, int max_splits) {
-  int best = 1;
-  double best_cost = 1e300;
-  const int lim = static_cast<int>(k_tiles < max_splits ? k_tiles : max_splits);
-  for (int s = 1; s <= (lim > 0 ? lim : 1); ++s) {
-    const int64_t ctas = row_tiles * s;
-    const int64_t waves = ceil_div(ctas, sms);
-    const double cost = static_cast<double>(waves) * (ceil_div(k_tiles, s) + 2.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
-    }
-  }
-  return best;
-}
 
 Plan make_plan(int64_t d_out, int64_t d_in, int64_t r, int dtype) {
   Plan p;
