@@ -17,9 +17,15 @@ Printed (rank 0, one JSON line):
   e2e        the same metrics through the public API from pinned host buffers,
              host<->device copies inside the timed region
   cpu_baseline  the float64 CPU oracle on the host cores, bounded sample
+  compose_training  the training forward (out, inner) and backward (d_base,
+             d_lora, dmag) at the same shape, GB/s
+  stack      the 196-module 7B-like stack at r = 128: grouped norm through a
+             plan and grouped compose, modules per second
+  fp32_norm  the fp32 norm at 8192 x 8192, r = 512 (3xTF32 tensor-core pass)
 
---impl reference times the CPU oracle (the only reference this build has) on
-the same metric, per step a bounded sample sized so the run ends in minutes.
+--impl reference times the CPU oracle (the method's write-ups ship no code to
+run) on the same metric, per step a bounded sample sized so the run ends in
+minutes.
 """
 from __future__ import annotations
 

@@ -44,8 +44,9 @@ class Config:
     std_m_rel: float = 0.0015  # m = ||W||_row * (1 + N(0, std_m_rel))
     std_base: float = 1.0
     std_lora: float = 0.05
-    # upstream gradient dL/d out of the compose (training path); the pages
-    # give no distribution for it, N(0, 0.01) is this build's choice
+    # upstream gradient dL/d out of the compose (training path); the
+    # "Scaling DoRA" write-ups give no distribution for it; N(0, 0.01) is
+    # chosen here
     std_grad: float = 0.01
     # "norm": compose uses g produced by the norm of the same module;
     # "synthetic": g ~ N(1, g_std) drawn directly (fp32).
