@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         const int row0 = t.tile * 256 + static_cast<int>(rank) * 128;
         const int yrow0 = t.pass * p.n_pass + static_cast<int>(rank * yr);
         for (int kt = t.kb; kt < t.ke; ++kt, ++it) {
-          // the slot's previous contents must have been read by the split warps
+          // the slot's previous contents must have been read by the MMAs (the
+          // loaded tile is their hi operand; the split warps read it earlier)
           if (it >= nraw && !mbar_wait(&raw_empty[s], phase ^ 1u, deadline)) {
             atomicExch(p.status, kStatusTimeout);
             stop = true;
@@ -334,11 +335,11 @@ __global__ void __launch_bounds__(kTfThreads, 1)
                 static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
             const float4 v = lds4(xa + off);
             if (sq) {
-              float q = __fmul_rn(v.x, v.x);
-              q = fmaf(v.y, v.y, q);
-              q = fmaf(v.z, v.z, q);
-              q = fmaf(v.w, v.w, q);
-              kahan_add(sacc[i], scmp[i], q);
+              float sq4 = __fmul_rn(v.x, v.x);
+              sq4 = fmaf(v.y, v.y, sq4);
+              sq4 = fmaf(v.z, v.z, sq4);
+              sq4 = fmaf(v.w, v.w, sq4);
+              kahan_add(sacc[i], scmp[i], sq4);
             }
             sts4(xd + off, tf32_lo4(v));
           }
