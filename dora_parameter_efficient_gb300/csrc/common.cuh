@@ -118,9 +118,18 @@ struct PairParams {
   int* tile_done;        // [pair_tiles][2] segments finished per 128-row group (zero at launch)
   float* wnorm;          // [rows]
   float* g;              // [rows]
-  int* work_ctr;         // next unclaimed work item; zero at launch
+  int* work_ctr;         // next unclaimed work item (or range slot); zero at launch
   int* status;
   unsigned long long timeout_ns;
+  // static ranges (single-module launch, ranges != 0): the i-th CTA pair to
+  // start owns iterations [S(i), S(i + 1)) of the (pair tile, K tile) space,
+  // iteration = tile * ktot + K tile, S(i) = min(iters, i * len_early) for
+  // i <= n_early and len_late per slot after that; a piece is the part of a
+  // range inside one pair tile, and splits/seg_k are unused
+  int ranges;            // CTA pairs launched (0: K segments handed out one by one)
+  int ktot;              // K tiles per pair tile: kt_w + 2 * kt_b
+  int iters;             // pair_tiles * ktot
+  int n_early, len_early, len_late;
   // grouped launch: the per-module fields above are unused, these are
   const PairModule* mods;
   int n_mods;

@@ -229,6 +229,62 @@ void plan_pair_segments(PairParams& pp, int clusters) {
   pp.splits = nseg;
 }
 
+// Static ranges of the single-module main pass: pair slot i (its place in
+// the start order) owns a contiguous range of the (pair tile, K tile)
+// iterations and drains its accumulator only where the range crosses a tile
+// boundary, so every pair finishes at about the same time.  The pairs that
+// start after the Gram kernel (one per two of its CTAs; they take the last
+// slots) get `lag` fewer K tiles: about 1 us + 0.7 us per Gram K tile of
+// one CTA, against 0.47 us per main-pass K tile at r = 384 (tensor-bound;
+// bound by W's HBM stream below r ~ 288).  Used with at least as many pair
+// tiles as pairs, every range at least kMinRange K tiles long and no pair
+// tile meeting more than kMaxMainSplits ranges; otherwise the K segments.
+// Measured per call on one GB300 (static ranges against K segments):
+// 28672 x 8192, r = 384: 131.7 against 140.9 us; with fewer tiles than
+// pairs the segments won at 8192 x 8192, r = 384 (49.3 against 54.8-57.3 us
+// over lags of 19 to 60 K tiles) and static ranges were within 5 % either
+// way at 8192 x 8192, r = 128 and 11008 x 4096, r = 64.
+#ifndef DORA_STATIC_RANGES
+#define DORA_STATIC_RANGES 1
+#endif
+#ifndef DORA_RANGE_LATE_US0
+#define DORA_RANGE_LATE_US0 1.0
+#endif
+#ifndef DORA_RANGE_LATE_US_PER_KT
+#define DORA_RANGE_LATE_US_PER_KT 0.7
+#endif
+constexpr int64_t kMinRange = 8;
+
+bool plan_pair_ranges(PairParams& pp, int clusters, int gram_ctas, int gram_kt) {
+  pp.ranges = 0;
+  if (!DORA_STATIC_RANGES || clusters <= 0 || pp.pair_tiles < clusters) return false;
+  const int64_t ktot = pp.kt_w + 2 * static_cast<int64_t>(pp.kt_b);
+  const int64_t iters = static_cast<int64_t>(pp.pair_tiles) * ktot;
+  if (ktot <= 0 || iters >= (int64_t(1) << 30)) return false;
+  const int64_t n = clusters;
+  int64_t late = gram_ctas > 0 ? (gram_ctas + 1) / 2 : 0;
+  if (late >= n) late = 0;
+  const int rp = pp.n0 + pp.n1;
+  const double tau_us = 0.47 * (rp > 288 ? rp : 288) / 384.0;
+  const int64_t lag =
+      late > 0 ? std::llround((DORA_RANGE_LATE_US0 + DORA_RANGE_LATE_US_PER_KT * gram_kt) / tau_us) : 0;
+  const int64_t le = ceil_div(iters + late * lag, n);
+  const int64_t ll = late > 0 ? (le - lag > 1 ? le - lag : 1) : le;
+  const int64_t lmin = ll < le ? ll : le;
+  if (lmin < kMinRange) return false;
+  // a tile of ktot iterations meets at most ktot / lmin whole ranges, two
+  // partial ones and the shortened last range
+  if (ktot / lmin + 3 > kMaxMainSplits) return false;
+  if ((n - late) * le + late * ll < iters) return false;     // the ranges cover every iteration
+  pp.ranges = static_cast<int>(n);
+  pp.ktot = static_cast<int>(ktot);
+  pp.iters = static_cast<int>(iters);
+  pp.n_early = static_cast<int>(n - late);
+  pp.len_early = static_cast<int>(le);
+  pp.len_late = static_cast<int>(ll);
+  return true;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -376,8 +432,12 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     pp.work_ctr = status + kCtlWork;
     pp.status = status;
     pp.timeout_ns = kDefaultTimeoutNs;
+    const int gram_ctas = pg.nb * (pg.nb + 1) / 2 * pg.cluster;
+    const int gram_kt = static_cast<int>(ceil_div(k_tiles, pg.cluster));
     const int items = pp.pair_tiles * pp.splits;
-    const int clusters = items < clusters_max ? items : clusters_max;
+    const int clusters = plan_pair_ranges(pp, clusters_max, gram_ctas, gram_kt)
+                             ? pp.ranges
+                             : (items < clusters_max ? items : clusters_max);
     if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
     DORA_TRY(launch_gemm_pair(mW, mA_y2, mB_x, mGhi, mGlo, pp, clusters, stream));
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));

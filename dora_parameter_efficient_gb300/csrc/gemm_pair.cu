@@ -47,6 +47,13 @@
 //     fewer items.  Items are ordered segment-major with the K segments
 //     shrinking along K, so long items go first, short ones fill in at the
 //     end, and the last segment -- the one with the G' tiles -- goes last;
+//   * with more pair tiles than pairs, a single-module launch uses static
+//     ranges instead: the (pair tile, K tile) iterations are cut into one
+//     contiguous range per pair (shorter ones for the pairs that start after
+//     the Gram kernel), a pair's one atomic claim is its place in the start
+//     order, and it drains its accumulator only where its range crosses a
+//     tile boundary.  The ranges, so every partial sum, do not depend on
+//     which pair runs which; a tile's partials are numbered in K order;
 //   * the TMA producer runs ahead into the next item while the epilogue
 //     drains the accumulator;
 //   * W tiles are not prefetched into L2 ahead of their loads: with every
@@ -167,17 +174,51 @@ __device__ __forceinline__ ModView view_of(const PairParams& p, const ModView& s
   else return single;
 }
 
-// Work item -> (pair tile, K segment, its K tile range) inside its module.
-// Items are handed out segment by segment and the segments shrink along K,
-// so the long pieces of work go first and the short ones fill in at the end
-// (fewer idle pairs at the finish); the last segment also holds the G' tiles.
-__device__ __forceinline__ void item_range(const ModView& mv, int item, int& tile, int& split,
-                                           int& kb, int& ke) {
+// First iteration of range slot i (static ranges), and the slot whose range
+// holds iteration x < iters.
+__device__ __forceinline__ int64_t range_start(const PairParams& p, int i) {
+  const int64_t e = p.n_early;
+  const int64_t v = i <= e ? i * static_cast<int64_t>(p.len_early)
+                           : e * p.len_early + (i - e) * static_cast<int64_t>(p.len_late);
+  return v < p.iters ? v : p.iters;
+}
+
+__device__ __forceinline__ int range_of(const PairParams& p, int64_t x) {
+  const int64_t head = static_cast<int64_t>(p.n_early) * p.len_early;
+  return x < head ? static_cast<int>(x / p.len_early)
+                  : p.n_early + static_cast<int>((x - head) / p.len_late);
+}
+
+// Work item -> (pair tile, its K split, the split's K tile range, the number
+// of splits of that tile) inside its module.
+//   K segments: items are handed out segment by segment and the segments
+//   shrink along K, so the long pieces of work go first and the short ones
+//   fill in at the end (fewer idle pairs at the finish); the last segment
+//   also holds the G' tiles.
+//   Static ranges: the item is the first iteration of a piece; the pieces of
+//   a tile are the ranges that meet it, numbered in K order.
+template <bool kGrouped>
+__device__ __forceinline__ void item_range(const PairParams& p, const ModView& mv, int item,
+                                           int& tile, int& split, int& kb, int& ke, int& nsplit) {
+  if (!kGrouped && p.ranges > 0) {
+    const int64_t x = item;
+    tile = static_cast<int>(x / p.ktot);
+    const int64_t t0 = static_cast<int64_t>(tile) * p.ktot;
+    const int c = range_of(p, x);
+    const int64_t end = range_start(p, c + 1);
+    const int c0 = range_of(p, t0);
+    kb = static_cast<int>(x - t0);
+    ke = end < t0 + p.ktot ? static_cast<int>(end - t0) : p.ktot;
+    split = c - c0;
+    nsplit = range_of(p, t0 + p.ktot - 1) - c0 + 1;
+    return;
+  }
   item -= mv.item_begin;
   split = item / mv.pair_tiles;
   tile = item - split * mv.pair_tiles;
   kb = mv.seg_k[split];
   ke = mv.seg_k[split + 1];
+  nsplit = mv.splits;
 }
 
 // global fp32 load that bypasses L1 (data written by other CTAs of this grid)
@@ -296,6 +337,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint32_t slot1 = map_to_rank(smem_u32(const_cast<int*>(item_slot)), 1);
       const uint32_t full1 = map_to_rank(smem_u32(item_full), 1);
       int claimed = rank == 0 ? atomicAdd(p.work_ctr, 1) : 0;
+      // static ranges: this pair's slot is its place in the start order; its
+      // pieces are issued from the last to the first, so a pair's first piece
+      // begins with W tiles and no pair meets a G' tile early
+      int64_t range_lo = 0, range_cur = 0;
+      if (!kGrouped && p.ranges > 0 && rank == 0 && claimed < p.ranges) {
+        range_lo = range_start(p, claimed);
+        range_cur = range_start(p, claimed + 1);
+      }
       for (uint32_t n = 0; !stop; ++n) {
         int item;
         if (rank == 0) {
@@ -307,7 +356,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             *abort_flag = 1;
             break;
           }
-          item = claimed < n_items ? claimed : -1;
+          if (!kGrouped && p.ranges > 0) {
+            item = -1;
+            if (range_cur > range_lo) {
+              const int64_t t0 = (range_cur - 1) / p.ktot * p.ktot;
+              range_cur = t0 > range_lo ? t0 : range_lo;
+              item = static_cast<int>(range_cur);
+            }
+          } else {
+            item = claimed < n_items ? claimed : -1;
+          }
           item_slot[slot] = item;
           st_cluster_u32(slot1 + slot * 4u, static_cast<uint32_t>(item));
           mbar_arrive(&item_full[slot]);
@@ -321,8 +379,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           tma_prefetch_desc(mv.tW);
           tma_prefetch_desc(mv.tA);
         }
-        int tile, split, kb, ke;
-        item_range(mv, item, tile, split, kb, ke);
+        int tile, split, kb, ke, nsplit;
+        item_range<kGrouped>(p, mv, item, tile, split, kb, ke, nsplit);
         const int row0 = tile * 256 + static_cast<int>(rank) * 128;
         for (int kt = kb; kt < ke; ++kt, ++it) {
           // the slot's previous use (parity phase ^ 1) must have been consumed
@@ -367,7 +425,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             phase ^= 1u;
           }
         }
-        if (rank == 0) claimed = atomicAdd(p.work_ctr, 1);
+        if (rank == 0 && (kGrouped || p.ranges == 0)) claimed = atomicAdd(p.work_ctr, 1);
       }
       // The even CTA's `full` barriers count the loads of both CTAs: once the
       // last use of every stage has completed, no copy is still in flight.
@@ -399,8 +457,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (uint32_t n = 0; !stop; ++n, ++icount) {
         const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
         if (item < 0) break;
-        int tile, split, kb, ke;
-        item_range(view_of<kGrouped>(p, single, mod_begin, item), item, tile, split, kb, ke);
+        int tile, split, kb, ke, nsplit;
+        item_range<kGrouped>(p, view_of<kGrouped>(p, single, mod_begin, item), item, tile, split, kb, ke,
+                   nsplit);
         // accumulator buffer of this item, and how often it was used before
         const uint32_t buf = static_cast<uint32_t>(icount) % nbuf;
         const uint32_t use = static_cast<uint32_t>(icount) / nbuf;
@@ -492,8 +551,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         if (!all_ok) break;
       }
       const ModView mv = view_of<kGrouped>(p, single, mod_begin, item);
-      int tile, split, kb, ke;
-      item_range(mv, item, tile, split, kb, ke);
+      int tile, split, kb, ke, nsplit;
+      item_range<kGrouped>(p, mv, item, tile, split, kb, ke, nsplit);
       const int rowbase = tile * 256 + static_cast<int>(rank) * 128 + q * 32;
       const int grow = rowbase + lane;      // the row whose dot this lane computes
       const bool valid = grow < mv.rows;
@@ -637,7 +696,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (warp == 2 && lane == 0) {
         const int prev = atomicAdd(mv.tile_done + tile * 2 + static_cast<int>(rank), 1);
-        *last_flag = prev == mv.splits - 1 ? 1 : 0;
+        *last_flag = prev == nsplit - 1 ? 1 : 0;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (*last_flag && h == 0 && valid) {
@@ -645,7 +704,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // segment partials added in segment order, carried as double-floats
         df base{0.f, 0.f}, cross{0.f, 0.f};
 #pragma unroll 1
-        for (int i = 0; i < mv.splits; ++i) {
+        for (int i = 0; i < nsplit; ++i) {
           float e;
           two_sum(base.hi, ld_cg_f(mv.out_sumsq + static_cast<size_t>(i) * mv.rows + grow), base.hi, e);
           base.lo = __fadd_rn(base.lo, e);

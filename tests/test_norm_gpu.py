@@ -96,6 +96,13 @@ def test_config4_stack_layer0_sampled_rows(module):
     (configs.BF16, 256, 512, 264, 1.0),      # N = 272: two MMAs (256 + 16)
     (configs.BF16, 128, 1024, 512, 0.25),    # the largest rank
     (configs.BF16, 640, 4096, 384, 1.0),     # several K splits
+    # more pair tiles than CTA pairs: static ranges (each pair owns a run of
+    # (tile, K tile) iterations; a tile is cut where a range ends)
+    (configs.BF16, 19500, 4104, 40, 1.0),    # ragged rows, K tail, N padded 40 -> 48
+    (configs.BF16, 19500, 4104, 296, -1.25), # two MMAs (160 + 144), ragged everywhere
+    # fewer pair tiles than pairs: K segments
+    (configs.BF16, 8100, 4104, 40, 1.0),
+    (configs.BF16, 9000, 4104, 296, -1.25),
     (configs.F32, 200, 136, 24, 1.5),
     (configs.F32, 65, 36, 4, 2.0),
     (configs.F32, 70, 100, 512, 0.5),        # two N passes of 256
@@ -249,3 +256,15 @@ def test_deterministic_across_calls():
     b = _run(x, cfg)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_deterministic_with_static_ranges():
+    """20000 x 4096, r = 384 (static ranges): which CTA pair takes which
+    range depends on the order in which the pairs start, which varies from
+    call to call; the ranges, and so every sum, do not."""
+    cfg = _custom("det-ranges", configs.BF16, 20000, 4096, 384, 1.0)
+    x = gen.norm_inputs(cfg)
+    runs = [_run(x, cfg) for _ in range(3)]
+    for wn, g in runs[1:]:
+        np.testing.assert_array_equal(wn, runs[0][0])
+        np.testing.assert_array_equal(g, runs[0][1])
