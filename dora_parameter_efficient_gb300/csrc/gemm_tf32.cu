@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     }
   }
 
+  __syncwarp();              // whole warps at the aligned barriers below (roles ran on single lanes)
   tc_fence_before_sync();
   __syncthreads();
   cluster_sync();            // the peer may still read this CTA's shared memory until here

@@ -247,6 +247,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   // this CTA's partial block is in shared memory; the bulk copies read it
   fence_proxy_async_smem();
   if (threadIdx.x == 0) mbar_arrive_expect_tx(recv_full, slice_bytes * C);
+  __syncwarp();            // whole warps at the aligned barriers below
   tc_fence_before_sync();
   cluster_sync();          // every partial written, every receive area free and armed
 
@@ -260,8 +261,13 @@ __global__ void __launch_bounds__(kGramThreads, 1)
                         part_local + d * slice_bytes, slice_bytes,
                         map_to_rank(smem_u32(recv_full), d));
   }
+  __syncwarp();
   // one decision for the whole CTA (named barriers follow)
   const bool got = __syncthreads_and(mbar_wait(recv_full, 0, deadline) ? 1 : 0) != 0;
+  // every slice sent to this CTA has landed (or its wait gave up): once every
+  // CTA of the cluster has arrived here, no bulk copy between them is in
+  // flight and each may leave without waiting for the others' stores below
+  cluster_arrive();
   if (!got) {
     if (threadIdx.x == 0) atomicExch(p.status, kStatusTimeout);
   } else {
@@ -328,9 +334,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     }
   }
 
-  // every bulk copy has landed (each owner waited for its slices) before any
-  // CTA of the cluster leaves
-  cluster_sync();
+  __syncwarp();
+  cluster_wait();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, p.tmem_cols);

@@ -299,6 +299,15 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// the two halves of cluster_sync, for work that fits between them (every
+// thread of the cluster arrives once and waits once per phase)
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
