@@ -71,6 +71,10 @@ SIGNATURES = {
                                              ctypes.c_size_t, _P]),
     "dora_check_status": (ctypes.c_int, [_P, _P]),
     "dora_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
+    "dora_selftest_schedule": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(ctypes.c_int64)]),
     "dora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dora_version": (ctypes.c_int, []),
     "dora_launch_count": (ctypes.c_uint64, []),

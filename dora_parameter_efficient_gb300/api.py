@@ -340,6 +340,19 @@ def dora_selftest_timeout(workspace: torch.Tensor, timeout_us: int,
     check(st, "dora_selftest_timeout")
 
 
+def dora_selftest_schedule(d_out: int, d_in: int, r: int, clusters: int):
+    """Host-only check of the main pass's work decomposition for a bf16
+    d_out x d_in module at rank r on `clusters` CTA pairs: returns
+    (uses_static_ranges, most_pieces_of_one_tile, defects); defects is 0 when
+    every pair tile's K range is covered once, in order, by at most 16
+    numbered pieces."""
+    ur, mp, df = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    st = _lib.load().dora_selftest_schedule(int(d_out), int(d_in), int(r), int(clusters),
+                                            ctypes.byref(ur), ctypes.byref(mp), ctypes.byref(df))
+    check(st, "dora_selftest_schedule")
+    return bool(ur.value), int(mp.value), int(df.value)
+
+
 def dora_factored_norm_noalloc(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
                                m: torch.Tensor, eps: float, wnorm: torch.Tensor,
                                g: torch.Tensor,

@@ -136,6 +136,61 @@ struct PairParams {
   int n_items;
 };
 
+// ---- work decomposition of a single-module main pass, shared by the kernel
+// and the host-side schedule self-test.  One piece of work is a pair tile's
+// K tiles [kb, ke); `split` numbers it among the pieces of its tile in K
+// order (the plane its partial sums go to) and nsplit counts those pieces.
+
+// Static ranges: first iteration of range slot i, and the slot whose range
+// holds iteration x < iters.
+__host__ __device__ inline int64_t range_start(const PairParams& p, int i) {
+  const int64_t e = p.n_early;
+  const int64_t v = i <= e ? i * static_cast<int64_t>(p.len_early)
+                           : e * p.len_early + (i - e) * static_cast<int64_t>(p.len_late);
+  return v < p.iters ? v : p.iters;
+}
+
+__host__ __device__ inline int range_of(const PairParams& p, int64_t x) {
+  const int64_t head = static_cast<int64_t>(p.n_early) * p.len_early;
+  return x < head ? static_cast<int>(x / p.len_early)
+                  : p.n_early + static_cast<int>((x - head) / p.len_late);
+}
+
+// Static ranges: the piece that starts at iteration x.
+__host__ __device__ inline void range_piece(const PairParams& p, int64_t x, int& tile, int& split,
+                                            int& kb, int& ke, int& nsplit) {
+  tile = static_cast<int>(x / p.ktot);
+  const int64_t t0 = static_cast<int64_t>(tile) * p.ktot;
+  const int c = range_of(p, x);
+  const int64_t end = range_start(p, c + 1);
+  const int c0 = range_of(p, t0);
+  kb = static_cast<int>(x - t0);
+  ke = end < t0 + p.ktot ? static_cast<int>(end - t0) : p.ktot;
+  split = c - c0;
+  nsplit = range_of(p, t0 + p.ktot - 1) - c0 + 1;
+}
+
+// Static ranges: the first iteration of the next piece a pair issues from
+// its range [lo, cur), the last piece first (cur moves down to it), or -1.
+__host__ __device__ inline int64_t range_next(const PairParams& p, int64_t lo, int64_t& cur) {
+  if (cur <= lo) return -1;
+  const int64_t t0 = (cur - 1) / p.ktot * p.ktot;
+  cur = t0 > lo ? t0 : lo;
+  return cur;
+}
+
+// K segments: work item -> its piece (items segment-major: every tile's
+// first segment, then every tile's second, ...).
+__host__ __device__ inline void segment_piece(const int* seg_k, int splits, int pair_tiles,
+                                              int item, int& tile, int& split, int& kb, int& ke,
+                                              int& nsplit) {
+  split = item / pair_tiles;
+  tile = item - split * pair_tiles;
+  kb = seg_k[split];
+  ke = seg_k[split + 1];
+  nsplit = splits;
+}
+
 // modules of a grouped launch whose first item is kept in shared memory
 constexpr int kPairModCache = 2048;
 size_t pair_smem_bytes(int n_pad, int stages, bool grouped);

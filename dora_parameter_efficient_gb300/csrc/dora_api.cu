@@ -285,6 +285,33 @@ bool plan_pair_ranges(PairParams& pp, int clusters, int gram_ctas, int gram_kt) 
   return true;
 }
 
+// CTAs (K splits) of the single-module Gram kernel per 128 x 128 block: a
+// power of two (the 128 block rows split evenly), at most one K tile per CTA
+int gram_cluster_for(int k_tiles) {
+  int c = kGramCluster;
+  while (c > 1 && c > k_tiles) c >>= 1;
+  return c;
+}
+
+// The work decomposition of a single-module bf16 main pass: N split, K tiles,
+// pair tiles, K segments or static ranges.  Returns the CTA pairs to launch.
+// The norm and the schedule self-test both plan through here.
+int plan_main_pass(PairParams& pp, int64_t d_out, int64_t d_in, int64_t r, int clusters_max) {
+  const int rp = static_cast<int>(ceil_div(r, 16) * 16);
+  pp.n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
+  pp.n1 = rp - pp.n0;
+  pp.kt_w = static_cast<int>(ceil_div(d_in, kTcBlockK));
+  pp.kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+  pp.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
+  plan_pair_segments(pp, clusters_max);
+  const int gnb = gram_nb(rp), gcl = gram_cluster_for(pp.kt_w);
+  if (plan_pair_ranges(pp, clusters_max, gnb * (gnb + 1) / 2 * gcl,
+                       static_cast<int>(ceil_div(pp.kt_w, gcl))))
+    return pp.ranges;
+  const int items = pp.pair_tiles * pp.splits;
+  return items < clusters_max ? items : clusters_max;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -389,9 +416,7 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     pg.rp = rp;
     pg.k_tiles = k_tiles;
     pg.stages = kGramStages;
-    // a power of two (the 128 block rows split evenly), at most one K tile per CTA
-    pg.cluster = kGramCluster;
-    while (pg.cluster > 1 && pg.cluster > k_tiles) pg.cluster >>= 1;
+    pg.cluster = gram_cluster_for(k_tiles);
     pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
     pg.scale = 0.5f * s;
     pg.G_hi = Ghi;
@@ -402,16 +427,12 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
 
     PairParams pp{};
     pp.rows = static_cast<int>(d_out);
-    pp.n0 = n0;
-    pp.n1 = n1;
     pp.y_box_rows = y_box2;
-    pp.kt_w = k_tiles;
-    pp.kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
-    pp.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
     pp.stages = pair_pick_stages(rp, false);
     const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, false));
     if (clusters_max <= 0) return DORA_ERR_CUDA;
-    plan_pair_segments(pp, clusters_max);
+    const int clusters = plan_main_pass(pp, d_out, d_in, r, clusters_max);
+    if (pp.n0 != n0 || pp.n1 != n1 || pp.kt_w != k_tiles) return DORA_ERR_UNSUPPORTED;
     pp.r = static_cast<int>(r);
     // two accumulators when they fit in the 512 tensor-memory columns
     pp.acc_stride = tmem_cols;
@@ -432,12 +453,6 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     pp.work_ctr = status + kCtlWork;
     pp.status = status;
     pp.timeout_ns = kDefaultTimeoutNs;
-    const int gram_ctas = pg.nb * (pg.nb + 1) / 2 * pg.cluster;
-    const int gram_kt = static_cast<int>(ceil_div(k_tiles, pg.cluster));
-    const int items = pp.pair_tiles * pp.splits;
-    const int clusters = plan_pair_ranges(pp, clusters_max, gram_ctas, gram_kt)
-                             ? pp.ranges
-                             : (items < clusters_max ? items : clusters_max);
     if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
     DORA_TRY(launch_gemm_pair(mW, mA_y2, mB_x, mGhi, mGlo, pp, clusters, stream));
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
@@ -1147,6 +1162,63 @@ int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned time
   int* status = static_cast<int*>(workspace);
   DORA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
   return cuda_status(launch_selftest_timeout(status, 1000ull * timeout_us, st));
+}
+
+int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
+                           int* uses_ranges, int* max_pieces, int64_t* defects) {
+  if (d_out < 1 || d_in < 1 || r < 1 || r > DORA_MAX_RANK || clusters < 1 || clusters > 65535 ||
+      d_out >= (int64_t(1) << 31) || d_in >= (int64_t(1) << 31) || !uses_ranges || !max_pieces ||
+      !defects)
+    return DORA_ERR_INVALID_ARG;
+  PairParams pp{};
+  const int launch = plan_main_pass(pp, d_out, d_in, r, clusters);
+  const int ktot = pp.kt_w + 2 * pp.kt_b;
+  // every piece the launched pairs would run, as (kb, ke, split, nsplit) per tile
+  struct Piece { int kb, ke, split, nsplit; };
+  std::vector<std::vector<Piece>> tiles(static_cast<size_t>(pp.pair_tiles));
+  int64_t bad = 0;
+  auto add = [&](int tile, int split, int kb, int ke, int nsplit) {
+    if (tile < 0 || tile >= pp.pair_tiles) { ++bad; return; }
+    tiles[static_cast<size_t>(tile)].push_back(Piece{kb, ke, split, nsplit});
+  };
+  int tile, split, kb, ke, nsplit;
+  if (pp.ranges > 0) {
+    if (launch != pp.ranges) ++bad;
+    for (int slot = 0; slot < pp.ranges; ++slot) {
+      const int64_t lo = range_start(pp, slot);
+      int64_t cur = range_start(pp, slot + 1);
+      for (int64_t x; (x = range_next(pp, lo, cur)) >= 0;) {
+        range_piece(pp, x, tile, split, kb, ke, nsplit);
+        add(tile, split, kb, ke, nsplit);
+      }
+    }
+  } else {
+    if (launch < 1 || launch > clusters) ++bad;
+    for (int item = 0; item < pp.pair_tiles * pp.splits; ++item) {
+      segment_piece(pp.seg_k, pp.splits, pp.pair_tiles, item, tile, split, kb, ke, nsplit);
+      add(tile, split, kb, ke, nsplit);
+    }
+  }
+  // each tile: pieces that tile [0, ktot) in K order, numbered 0 .. nsplit - 1,
+  // at most as many as the workspace has partial planes, every piece non-empty
+  int most = 0;
+  for (auto& ps : tiles) {
+    std::sort(ps.begin(), ps.end(), [](const Piece& a, const Piece& b) { return a.kb < b.kb; });
+    const int n = static_cast<int>(ps.size());
+    most = n > most ? n : most;
+    if (n == 0 || n > kMaxMainSplits) { ++bad; continue; }
+    int at = 0;
+    for (int i = 0; i < n; ++i) {
+      const Piece& q = ps[static_cast<size_t>(i)];
+      if (q.kb != at || q.ke <= q.kb || q.split != i || q.nsplit != n) ++bad;
+      at = q.ke;
+    }
+    if (at != ktot) ++bad;
+  }
+  *uses_ranges = pp.ranges > 0 ? 1 : 0;
+  *max_pieces = most;
+  *defects = bad;
+  return DORA_OK;
 }
 
 int dora_check_status(const void* workspace, void* stream) {

@@ -174,21 +174,6 @@ __device__ __forceinline__ ModView view_of(const PairParams& p, const ModView& s
   else return single;
 }
 
-// First iteration of range slot i (static ranges), and the slot whose range
-// holds iteration x < iters.
-__device__ __forceinline__ int64_t range_start(const PairParams& p, int i) {
-  const int64_t e = p.n_early;
-  const int64_t v = i <= e ? i * static_cast<int64_t>(p.len_early)
-                           : e * p.len_early + (i - e) * static_cast<int64_t>(p.len_late);
-  return v < p.iters ? v : p.iters;
-}
-
-__device__ __forceinline__ int range_of(const PairParams& p, int64_t x) {
-  const int64_t head = static_cast<int64_t>(p.n_early) * p.len_early;
-  return x < head ? static_cast<int>(x / p.len_early)
-                  : p.n_early + static_cast<int>((x - head) / p.len_late);
-}
-
 // Work item -> (pair tile, its K split, the split's K tile range, the number
 // of splits of that tile) inside its module.
 //   K segments: items are handed out segment by segment and the segments
@@ -201,24 +186,11 @@ template <bool kGrouped>
 __device__ __forceinline__ void item_range(const PairParams& p, const ModView& mv, int item,
                                            int& tile, int& split, int& kb, int& ke, int& nsplit) {
   if (!kGrouped && p.ranges > 0) {
-    const int64_t x = item;
-    tile = static_cast<int>(x / p.ktot);
-    const int64_t t0 = static_cast<int64_t>(tile) * p.ktot;
-    const int c = range_of(p, x);
-    const int64_t end = range_start(p, c + 1);
-    const int c0 = range_of(p, t0);
-    kb = static_cast<int>(x - t0);
-    ke = end < t0 + p.ktot ? static_cast<int>(end - t0) : p.ktot;
-    split = c - c0;
-    nsplit = range_of(p, t0 + p.ktot - 1) - c0 + 1;
+    range_piece(p, item, tile, split, kb, ke, nsplit);
     return;
   }
-  item -= mv.item_begin;
-  split = item / mv.pair_tiles;
-  tile = item - split * mv.pair_tiles;
-  kb = mv.seg_k[split];
-  ke = mv.seg_k[split + 1];
-  nsplit = mv.splits;
+  segment_piece(mv.seg_k, mv.splits, mv.pair_tiles, item - mv.item_begin, tile, split, kb, ke,
+                nsplit);
 }
 
 // global fp32 load that bypasses L1 (data written by other CTAs of this grid)
@@ -357,12 +329,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             break;
           }
           if (!kGrouped && p.ranges > 0) {
-            item = -1;
-            if (range_cur > range_lo) {
-              const int64_t t0 = (range_cur - 1) / p.ktot * p.ktot;
-              range_cur = t0 > range_lo ? t0 : range_lo;
-              item = static_cast<int>(range_cur);
-            }
+            item = static_cast<int>(range_next(p, range_lo, range_cur));
           } else {
             item = claimed < n_items ? claimed : -1;
           }

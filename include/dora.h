@@ -350,6 +350,22 @@ int dora_check_status(const void* workspace, void* stream);
 int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned timeout_us,
                           void* stream);
 
+/*
+ * Self-test of the main pass's work decomposition (host only, no GPU): plans
+ * a bf16 single-module norm of d_out x d_in at rank r (1 .. DORA_MAX_RANK)
+ * exactly as dora_factored_norm does on a device with `clusters` co-resident
+ * CTA pairs (1 .. 65535; 76 on a GB300), enumerates every piece of work the
+ * launched pairs would run -- K segments handed out in item order, or the
+ * static ranges of each pair, issued from the last piece to the first -- and
+ * checks that the pieces of every 256-row pair tile cover its K tiles once,
+ * in K order, numbered 0 .. n - 1 with n <= 16 (the partial planes of the
+ * workspace).  Writes whether static ranges were chosen, the largest number
+ * of pieces of one tile, and the number of defects found (0 when the plan is
+ * sound).  Returns DORA_ERR_INVALID_ARG for bad arguments, else DORA_OK.
+ */
+int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
+                           int* uses_ranges, int* max_pieces, int64_t* defects);
+
 /* Number of CUDA kernels this library has launched in this process so far
  * (all devices, all entry points); a diagnostic counter. */
 uint64_t dora_launch_count(void);

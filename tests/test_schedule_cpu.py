@@ -1,0 +1,74 @@
+"""The main pass's work decomposition, checked on the host (no GPU).
+
+dora_selftest_schedule plans a bf16 single-module norm exactly as
+dora_factored_norm does and enumerates every piece of work the launched CTA
+pairs would run, through the same functions the kernel uses: K segments
+handed out in item order, or static ranges (one contiguous run of
+(pair tile, K tile) iterations per pair, issued from the last piece to the
+first).  A sound plan covers every pair tile's K tiles once, in K order,
+with pieces numbered 0 .. n - 1 and n at most the 16 partial planes of the
+workspace; a mistake in that arithmetic would drop or double-count part of
+a row's sums."""
+from __future__ import annotations
+
+import random
+
+import pytest
+
+from dora_parameter_efficient_gb300 import api
+from dora_parameter_efficient_gb300._lib import DoraError
+
+GB300_PAIRS = 76
+
+
+@pytest.mark.parametrize("d_out,d_in,r,ranges", [
+    (8192, 8192, 384, False),     # fewer pair tiles (32) than pairs: K segments 7:4:2
+    (8100, 4104, 40, False),
+    (9000, 4104, 296, False),
+    (19500, 4104, 40, True),      # 77 pair tiles: static ranges
+    (19500, 4104, 296, True),
+    (20000, 4096, 384, True),
+    (28672, 8192, 384, True),
+])
+def test_known_shapes(d_out, d_in, r, ranges):
+    uses_ranges, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
+    assert defects == 0
+    assert uses_ranges == ranges
+    assert 1 <= most <= 16
+
+
+def test_seeded_sweep_of_shapes_and_grids():
+    rng = random.Random(2026)
+    seen_ranges = seen_segments = 0
+    for _ in range(4000):
+        d_out = rng.choice([rng.randint(1, 300), rng.randint(1, 5000), rng.randint(1, 200000)])
+        d_in = rng.choice([rng.randint(1, 64), rng.randint(1, 20000), rng.randint(1, 100000)])
+        r = rng.choice([rng.randint(1, 16), rng.randint(1, 512)])
+        pairs = rng.choice([1, 2, 3, 7, 16, 60, 74, GB300_PAIRS, 148, 1000])
+        uses_ranges, most, defects = api.dora_selftest_schedule(d_out, d_in, r, pairs)
+        assert defects == 0, (d_out, d_in, r, pairs)
+        assert 1 <= most <= 16, (d_out, d_in, r, pairs)
+        seen_ranges += uses_ranges
+        seen_segments += not uses_ranges
+    assert seen_ranges > 100 and seen_segments > 100      # both schedules exercised
+
+
+@pytest.mark.parametrize("d_out", [1, 255, 256, 257, 76 * 256 - 1, 76 * 256, 76 * 256 + 1])
+@pytest.mark.parametrize("d_in", [1, 64, 65, 8192])
+def test_boundaries_of_tiles_and_of_the_range_rule(d_out, d_in):
+    """Row counts around one tile and around as many pair tiles as pairs
+    (where the plan switches to static ranges), K around one tile."""
+    for r in (8, 128, 384, 512):
+        uses_ranges, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
+        assert defects == 0 and most <= 16
+        if (d_out + 255) // 256 < GB300_PAIRS:
+            assert not uses_ranges
+
+
+@pytest.mark.parametrize("args", [
+    (0, 64, 8, 76), (64, 0, 8, 76), (64, 64, 0, 76), (64, 64, 513, 76), (64, 64, 8, 0),
+    (1 << 31, 64, 8, 76),
+])
+def test_rejects_bad_arguments(args):
+    with pytest.raises(DoraError):
+        api.dora_selftest_schedule(*args)
