@@ -71,6 +71,9 @@ SIGNATURES = {
                                              ctypes.c_size_t, _P]),
     "dora_check_status": (ctypes.c_int, [_P, _P]),
     "dora_selftest_timeout": (ctypes.c_int, [_P, ctypes.c_size_t, ctypes.c_uint, _P]),
+    "dora_selftest_grouped_schedule": (ctypes.c_int, [_P, _P, ctypes.c_int, _I64, ctypes.c_int,
+                                                      ctypes.POINTER(ctypes.c_int),
+                                                      ctypes.POINTER(ctypes.c_int64)]),
     "dora_selftest_schedule": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int,
                                               ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int),

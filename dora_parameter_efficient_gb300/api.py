@@ -353,6 +353,23 @@ def dora_selftest_schedule(d_out: int, d_in: int, r: int, clusters: int):
     return bool(ur.value), int(mp.value), int(df.value)
 
 
+def dora_selftest_grouped_schedule(shapes, r: int, clusters: int):
+    """Host-only check of a grouped main pass's work items for bf16 modules
+    of the given (d_out, d_in) shapes at rank r on `clusters` CTA pairs:
+    returns (most_pieces_of_one_tile, defects); defects is 0 when the
+    module order is longest-K first and every pair tile of every module is
+    covered once, in order, by at most 16 numbered pieces."""
+    n = len(shapes)
+    d_out = (ctypes.c_int64 * max(n, 1))(*[int(a) for a, _ in shapes])
+    d_in = (ctypes.c_int64 * max(n, 1))(*[int(b) for _, b in shapes])
+    mp, df = ctypes.c_int(), ctypes.c_int64()
+    st = _lib.load().dora_selftest_grouped_schedule(ctypes.addressof(d_out), ctypes.addressof(d_in),
+                                                    n, int(r), int(clusters), ctypes.byref(mp),
+                                                    ctypes.byref(df))
+    check(st, "dora_selftest_grouped_schedule")
+    return int(mp.value), int(df.value)
+
+
 def dora_factored_norm_noalloc(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
                                m: torch.Tensor, eps: float, wnorm: torch.Tensor,
                                g: torch.Tensor,

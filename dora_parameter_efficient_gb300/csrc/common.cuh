@@ -191,6 +191,19 @@ __host__ __device__ inline void segment_piece(const int* seg_k, int splits, int 
   nsplit = splits;
 }
 
+// Grouped launch: the module whose items hold `item`, by binary search over
+// the modules' first items (begin(i), non-decreasing, begin(0) = 0).
+template <class Begin>
+__host__ __device__ inline int find_module(Begin begin, int n, int item) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (begin(mid) <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
 // modules of a grouped launch whose first item is kept in shared memory
 constexpr int kPairModCache = 2048;
 size_t pair_smem_bytes(int n_pad, int stages, bool grouped);

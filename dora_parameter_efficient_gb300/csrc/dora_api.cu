@@ -670,6 +670,47 @@ bool modules_fusable(const dora_norm_module* mods, int n, int64_t r, int dtype) 
 
 // Host checks, layouts and (with write_tables) the one-launch tables, encoded
 // and copied to the workspace on `stream`.
+// The work items of a grouped main pass, independent of buffers: modules in
+// item order (longest K first, so that the last items the persistent grid
+// takes are short ones), each with its K tiles, pair tiles, K segments and
+// first item.  K segments only when the pair tiles of all modules are too
+// few to fill the persistent grid a few times over; a stack of many modules
+// fills it with whole-K items, each one accumulator drain.  Returns the
+// number of items.
+struct GroupedItems {
+  int kt_w, pair_tiles, splits, item_begin;
+  int seg_k[17];
+};
+
+int plan_grouped_items(int n, const int64_t* d_out, const int64_t* d_in, int64_t r,
+                       int clusters_max, std::vector<int>& order, std::vector<GroupedItems>& out) {
+  const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+  int64_t total_pairs = 0;
+  for (int i = 0; i < n; ++i) total_pairs += ceil_div(d_out[i], 2 * kTcBlockM);
+  const bool split_k = total_pairs < 4 * static_cast<int64_t>(clusters_max);
+  order.resize(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) order[static_cast<size_t>(i)] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return d_in[a] > d_in[b]; });
+  out.assign(static_cast<size_t>(n), GroupedItems{});
+  int item = 0;
+  for (int j = 0; j < n; ++j) {
+    const int i = order[static_cast<size_t>(j)];
+    GroupedItems& g = out[static_cast<size_t>(j)];
+    g.kt_w = static_cast<int>(ceil_div(d_in[i], kTcBlockK));
+    g.pair_tiles = static_cast<int>(ceil_div(d_out[i], 2 * kTcBlockM));
+    if (split_k) {
+      plan_module_segments(g.kt_w + 2 * kt_b, g.seg_k, &g.splits);
+    } else {
+      g.seg_k[0] = 0;
+      g.seg_k[1] = g.kt_w + 2 * kt_b;
+      g.splits = 1;
+    }
+    g.item_begin = item;
+    item += g.pair_tiles * g.splits;
+  }
+  return item;
+}
+
 int grouped_prepare(const dora_norm_module* mods, int n, int dtype, int64_t r, void* workspace,
                     size_t workspace_bytes, bool write_tables, cudaStream_t stream,
                     NormGroupedPlan* P) {
@@ -701,28 +742,22 @@ int grouped_prepare(const dora_norm_module* mods, int n, int dtype, int64_t r, v
   const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
   const int n1 = rp - n0;
   const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
-  const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
 
-  // K segments only when the pair tiles of all modules are too few to fill
-  // the persistent grid a few times over; a stack of many modules fills it
-  // with whole-K items, each one accumulator drain.
   const int clusters_max =
       pair_max_clusters(pair_smem_bytes(rp, pair_pick_stages(rp, true), true));
   if (clusters_max <= 0) return DORA_ERR_CUDA;
-  int64_t total_pairs = 0;
-  for (int i = 0; i < n; ++i) total_pairs += ceil_div(mods[i].d_out, 2 * kTcBlockM);
-  const bool split_k = total_pairs < 4 * static_cast<int64_t>(clusters_max);
-  // Items are numbered module by module in this order: longest K first, so
-  // that the last items the persistent grid takes are short ones.
-  std::vector<int> order(n);
-  for (int i = 0; i < n; ++i) order[i] = i;
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int a, int b) { return mods[a].d_in > mods[b].d_in; });
+  std::vector<int64_t> d_out(static_cast<size_t>(n)), d_in(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) {
+    d_out[static_cast<size_t>(i)] = mods[i].d_out;
+    d_in[static_cast<size_t>(i)] = mods[i].d_in;
+  }
+  std::vector<int> order;
+  std::vector<GroupedItems> items;
+  const int n_items = plan_grouped_items(n, d_out.data(), d_in.data(), r, clusters_max, order, items);
 
   std::vector<PairModule> pm(n);
   std::vector<GramModule> gm(n);
   int min_kt = 1 << 30;
-  int item = 0;
   for (int j = 0; j < n; ++j) {
     const int i = order[j];
     const dora_norm_module& md = mods[i];
@@ -742,18 +777,13 @@ int grouped_prepare(const dora_norm_module* mods, int n, int dtype, int64_t r, v
     p.out_sumsq = reinterpret_cast<float*>(ws + gp.off_pbase[i]);
     p.out_dot = reinterpret_cast<float*>(ws + gp.off_pcross[i]);
     p.tile_done = status + gp.tile_done_word[i];
+    const GroupedItems& it = items[static_cast<size_t>(j)];
     p.rows = static_cast<int>(md.d_out);
-    p.kt_w = static_cast<int>(ceil_div(md.d_in, kTcBlockK));
-    p.pair_tiles = static_cast<int>(ceil_div(md.d_out, 2 * kTcBlockM));
-    if (split_k) {
-      plan_module_segments(p.kt_w + 2 * kt_b, p.seg_k, &p.splits);
-    } else {
-      p.seg_k[0] = 0;
-      p.seg_k[1] = p.kt_w + 2 * kt_b;
-      p.splits = 1;
-    }
-    p.item_begin = item;
-    item += p.pair_tiles * p.splits;
+    p.kt_w = it.kt_w;
+    p.pair_tiles = it.pair_tiles;
+    p.splits = it.splits;
+    std::memcpy(p.seg_k, it.seg_k, sizeof(p.seg_k));
+    p.item_begin = it.item_begin;
     GramModule& q = gm[i];
     std::memset(&q, 0, sizeof(q));
     if (!make_map_bf16(&q.tAx, md.A, md.d_in, r, kTcBlockM) ||
@@ -770,7 +800,7 @@ int grouped_prepare(const dora_norm_module* mods, int n, int dtype, int64_t r, v
   DORA_TRY(cudaMemcpyAsync(ws + gp.off_gmods, gm.data(), sizeof(GramModule) * n,
                            cudaMemcpyHostToDevice, stream));
   P->tables = true;
-  P->n_items = item;
+  P->n_items = n_items;
   P->min_kt = min_kt;
   return DORA_OK;
 }
@@ -1216,6 +1246,69 @@ int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
     if (at != ktot) ++bad;
   }
   *uses_ranges = pp.ranges > 0 ? 1 : 0;
+  *max_pieces = most;
+  *defects = bad;
+  return DORA_OK;
+}
+
+int dora_selftest_grouped_schedule(const int64_t* d_out, const int64_t* d_in, int n_modules,
+                                   int64_t r, int clusters, int* max_pieces, int64_t* defects) {
+  if (!d_out || !d_in || n_modules < 1 || n_modules > (1 << 20) || r < 1 || r > DORA_MAX_RANK ||
+      clusters < 1 || clusters > 65535 || !max_pieces || !defects)
+    return DORA_ERR_INVALID_ARG;
+  int64_t total_tiles = 0;
+  for (int i = 0; i < n_modules; ++i) {
+    if (d_out[i] < 1 || d_in[i] < 1 || d_out[i] >= (int64_t(1) << 31) ||
+        d_in[i] >= (int64_t(1) << 31))
+      return DORA_ERR_INVALID_ARG;
+    total_tiles += ceil_div(d_out[i], 2 * kTcBlockM);
+  }
+  if (total_tiles > (int64_t(1) << 22)) return DORA_ERR_INVALID_ARG;
+  std::vector<int> order;
+  std::vector<GroupedItems> items;
+  const int n_items = plan_grouped_items(n_modules, d_out, d_in, r, clusters, order, items);
+  const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+  int64_t bad = 0;
+  // the item order: a permutation of the modules, longest K first
+  std::vector<int> seen(static_cast<size_t>(n_modules), 0);
+  for (int j = 0; j < n_modules; ++j) {
+    const int i = order[static_cast<size_t>(j)];
+    if (i < 0 || i >= n_modules || seen[static_cast<size_t>(i)]++) ++bad;
+    if (j > 0 && items[static_cast<size_t>(j)].kt_w > items[static_cast<size_t>(j - 1)].kt_w) ++bad;
+  }
+  // every item through the kernel's own module search and segment decode
+  struct Piece { int kb, ke, split, nsplit; };
+  std::vector<int64_t> tile_base(static_cast<size_t>(n_modules) + 1, 0);
+  for (int j = 0; j < n_modules; ++j)
+    tile_base[static_cast<size_t>(j) + 1] = tile_base[static_cast<size_t>(j)] + items[static_cast<size_t>(j)].pair_tiles;
+  std::vector<std::vector<Piece>> tiles(static_cast<size_t>(tile_base.back()));
+  for (int item = 0; item < n_items; ++item) {
+    const int j = find_module([&](int m) { return items[static_cast<size_t>(m)].item_begin; },
+                              n_modules, item);
+    const GroupedItems& g = items[static_cast<size_t>(j)];
+    int tile, split, kb, ke, nsplit;
+    segment_piece(g.seg_k, g.splits, g.pair_tiles, item - g.item_begin, tile, split, kb, ke, nsplit);
+    if (tile < 0 || tile >= g.pair_tiles) { ++bad; continue; }
+    tiles[static_cast<size_t>(tile_base[static_cast<size_t>(j)] + tile)].push_back(Piece{kb, ke, split, nsplit});
+  }
+  int most = 0;
+  for (int j = 0; j < n_modules; ++j) {
+    const int ktot = items[static_cast<size_t>(j)].kt_w + 2 * kt_b;
+    for (int64_t t = tile_base[static_cast<size_t>(j)]; t < tile_base[static_cast<size_t>(j) + 1]; ++t) {
+      auto& ps = tiles[static_cast<size_t>(t)];
+      std::sort(ps.begin(), ps.end(), [](const Piece& a, const Piece& b) { return a.kb < b.kb; });
+      const int np = static_cast<int>(ps.size());
+      most = np > most ? np : most;
+      if (np == 0 || np > kMaxMainSplits) { ++bad; continue; }
+      int at = 0;
+      for (int k = 0; k < np; ++k) {
+        const Piece& q = ps[static_cast<size_t>(k)];
+        if (q.kb != at || q.ke <= q.kb || q.split != k || q.nsplit != np) ++bad;
+        at = q.ke;
+      }
+      if (at != ktot) ++bad;
+    }
+  }
   *max_pieces = most;
   *defects = bad;
   return DORA_OK;

@@ -154,13 +154,8 @@ __device__ __forceinline__ ModView single_view(const PairParams& p, const CUtens
 // load and first MMA by a few microseconds
 __device__ __forceinline__ ModView module_view(const PairParams& p, const int* begins, int item) {
   const bool cached = p.n_mods <= kPairModCache;
-  int lo = 0, hi = p.n_mods - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    const int b = cached ? begins[mid] : p.mods[mid].item_begin;
-    if (b <= item) lo = mid;
-    else hi = mid - 1;
-  }
+  const int lo = find_module(
+      [&](int i) { return cached ? begins[i] : p.mods[i].item_begin; }, p.n_mods, item);
   const PairModule& md = p.mods[lo];
   return ModView{&md.tW, &md.tA, &md.tB, &md.tGhi, &md.tGlo, md.B, md.m, md.wnorm, md.g,
                  md.out_sumsq, md.out_dot, md.tile_done, md.rows, md.kt_w, md.pair_tiles,

@@ -366,6 +366,21 @@ int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned time
 int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
                            int* uses_ranges, int* max_pieces, int64_t* defects);
 
+/*
+ * The same check for a grouped launch (host only, no GPU): plans the work
+ * items of one grouped main pass over n_modules bf16 modules (d_out[i] x
+ * d_in[i], all at rank r) as dora_factored_norm_grouped and the grouped plan
+ * do on a device with `clusters` co-resident CTA pairs, then maps every item
+ * to its module and piece through the kernel's own search and decode, and
+ * checks the module order (longest K first) and that every pair tile of
+ * every module is covered once, in K order, by at most 16 numbered pieces.
+ * Writes the largest number of pieces of one tile and the number of defects
+ * (0 when sound).  Returns DORA_ERR_INVALID_ARG for bad arguments (including
+ * more than 2^22 pair tiles in all), else DORA_OK.
+ */
+int dora_selftest_grouped_schedule(const int64_t* d_out, const int64_t* d_in, int n_modules,
+                                   int64_t r, int clusters, int* max_pieces, int64_t* defects);
+
 /* Number of CUDA kernels this library has launched in this process so far
  * (all devices, all entry points); a diagnostic counter. */
 uint64_t dora_launch_count(void);

@@ -8,7 +8,9 @@ handed out in item order, or static ranges (one contiguous run of
 first).  A sound plan covers every pair tile's K tiles once, in K order,
 with pieces numbered 0 .. n - 1 and n at most the 16 partial planes of the
 workspace; a mistake in that arithmetic would drop or double-count part of
-a row's sums."""
+a row's sums.  dora_selftest_grouped_schedule does the same for a grouped
+launch: the module order, each module's K segments or whole-K items, and
+the item -> module search the kernel runs."""
 from __future__ import annotations
 
 import random
@@ -72,3 +74,43 @@ def test_boundaries_of_tiles_and_of_the_range_rule(d_out, d_in):
 def test_rejects_bad_arguments(args):
     with pytest.raises(DoraError):
         api.dora_selftest_schedule(*args)
+
+
+# ------------------------------------------------------------------ grouped launches
+def test_grouped_stack_of_the_7b_like_model():
+    """196 modules of seven shapes: enough pair tiles for whole-K items."""
+    from synthetic import configs
+    cfg = configs.get(4)
+    most, defects = api.dora_selftest_grouped_schedule(
+        [(m.d_out, m.d_in) for m in cfg.modules], cfg.r, GB300_PAIRS)
+    assert defects == 0
+    assert most == 1
+
+
+def test_grouped_few_modules_take_k_segments():
+    most, defects = api.dora_selftest_grouped_schedule([(300, 256), (64, 512), (520, 136)], 24,
+                                                       GB300_PAIRS)
+    assert defects == 0
+    assert most == 3
+
+
+def test_grouped_seeded_sweep():
+    rng = random.Random(77)
+    for _ in range(400):
+        n = rng.choice([1, 2, 3, 7, 50, 300])
+        shapes = [(rng.choice([rng.randint(1, 600), rng.randint(1, 20000)]),
+                   rng.choice([rng.randint(1, 200), rng.randint(1, 20000)])) for _ in range(n)]
+        r = rng.choice([8, 64, 128, 384, 512, rng.randint(1, 512)])
+        pairs = rng.choice([1, 16, GB300_PAIRS, 148])
+        most, defects = api.dora_selftest_grouped_schedule(shapes, r, pairs)
+        assert defects == 0, (n, r, pairs)
+        assert 1 <= most <= 16
+
+
+@pytest.mark.parametrize("shapes,r,pairs", [
+    ([], 8, 76), ([(0, 64)], 8, 76), ([(64, 0)], 8, 76), ([(64, 64)], 0, 76),
+    ([(64, 64)], 8, 0),
+])
+def test_grouped_rejects_bad_arguments(shapes, r, pairs):
+    with pytest.raises(DoraError):
+        api.dora_selftest_grouped_schedule(shapes, r, pairs)
