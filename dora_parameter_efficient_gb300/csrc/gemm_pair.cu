@@ -36,8 +36,9 @@
 //     its B row per tile into registers, so no burst of global loads
 //     competes with the TMA and MMA instructions;
 //   * at the end of an item two warps per TMEM lane quadrant read the halves
-//     of the D rows (tcgen05.ld), dot them with B and add the halves in a
-//     fixed order;
+//     of the D rows (tcgen05.ld, 16 columns at a time, the next load in
+//     flight while the current columns are multiplied), dot them with B and
+//     add the halves in a fixed order;
 //   * the grid is persistent and the work is handed out dynamically: the
 //     even CTA's TMA producer claims the next work item -- a (256-row tile,
 //     K split) pair -- from a global counter when it has issued the loads of
@@ -606,25 +607,39 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // chunks c_lo .. c_lo + 5, B held in bb; pieces at or past the padded
         // rank were never written by an MMA
         const int rp = p.n0 + p.n1;
+        // 16-column pieces of this warp's half, the next one loading while
+        // the current one is multiplied (columns in the same order as one
+        // piece at a time, so the same sums)
+        const int hc0 = 2 * c_lo;
+        int nh = 2 * c_hi - hc0;
+        if (nh > rp / 16 - hc0) nh = rp / 16 - hc0;
+        if (nh > 12) nh = 12;
+        uint32_t ra[16], rb[16];
+        if (nh > 0) {
+          tmem_load_16cols_async(acc_row + static_cast<uint32_t>(hc0 * 16), ra);
+          tmem_wait_ld(ra);
+        }
 #pragma unroll
-        for (int j = 0; j < 6; ++j) {
-          const int c = c_lo + j;
-          if (c < c_hi && c * 32 < rp) {
-            float v[32];
-            if (c * 32 + 32 <= rp) {
-              tmem_load_32cols(acc_row + static_cast<uint32_t>(c * 32), v);
-            } else {          // only the first 16 columns of this chunk exist
-              uint32_t rv[16];
-              tmem_load_16cols_async(acc_row + static_cast<uint32_t>(c * 32), rv);
-              tmem_wait_ld(rv);
+        for (int k = 0; k < 12; k += 2) {
+          if (k < nh) {
+            if (k + 1 < nh)
+              tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k + 1) * 16), rb);
+            float v[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                v[i] = __uint_as_float(rv[i]);
-                v[16 + i] = 0.f;
-              }
-            }
-            const uint4 part[4] = {bb[4 * j], bb[4 * j + 1], bb[4 * j + 2], bb[4 * j + 3]};
-            acc = dot_b<4>(part, v, acc);
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(ra[i]);
+            const uint4 part[2] = {bb[2 * k], bb[2 * k + 1]};
+            acc = dot_b<2>(part, v, acc);
+            if (k + 1 < nh) tmem_wait_ld(rb);
+          }
+          if (k + 1 < nh) {
+            if (k + 2 < nh)
+              tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k + 2) * 16), ra);
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rb[i]);
+            const uint4 part[2] = {bb[2 * k + 2], bb[2 * k + 3]};
+            acc = dot_b<2>(part, v, acc);
+            if (k + 2 < nh) tmem_wait_ld(ra);
           }
         }
         // ranks above 384: the rest of the half, B loaded now
