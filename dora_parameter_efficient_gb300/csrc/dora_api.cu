@@ -1337,7 +1337,7 @@ const char* dora_status_string(int status) {
   }
 }
 
-int dora_version(void) { return (1 << 16) | 0; }
+int dora_version(void) { return (1 << 16) | 1; }
 
 uint64_t dora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -388,7 +388,8 @@ uint64_t dora_launch_count(void);
 /* Static, human-readable name of a dora_status value. */
 const char* dora_status_string(int status);
 
-/* Library ABI version: (major << 16) | minor. */
+/* Library ABI version: (major << 16) | minor.  1.1 added the two schedule
+ * self-tests; nothing was removed or changed. */
 int dora_version(void);
 
 #ifdef __cplusplus

@@ -45,6 +45,7 @@ def test_status_strings(lib):
         assert s.startswith("DORA_")
     assert "unknown" in _lib.status_string(99)
     assert lib.dora_version() >> 16 == 1
+    assert lib.dora_version() & 0xFFFF >= 1      # the schedule self-tests
 
 
 def test_workspace_size(lib):
