@@ -302,6 +302,80 @@ def test_naive_form_is_worse_near_one():
     assert err_stable < err_naive / 2
 
 
+def _read_naive_golden(golden_dir):
+    rows = []
+    with open(os.path.join(golden_dir, "naive_compose_f32.txt")) as f:
+        for ln in f:
+            if not ln.strip() or ln.startswith("#"):
+                continue
+            p = ln.split()
+            rows.append((float.fromhex(p[0]), float.fromhex(p[1]), float.fromhex(p[2]),
+                         float.fromhex(p[3]), int(p[4], 16)))
+    return rows
+
+
+def _naive_pins_hold(naive, golden_dir):
+    """Every pin of the naive comparator, for the function `naive`:
+
+    * the hand-worked binary32 rows of tests/golden/naive_compose_f32.txt, bit
+      for bit (cancellation near g = 1, a rounding tie, the sign of the final
+      subtraction, the scale s);
+    * small dyadic inputs where every binary32 step of g*(s*lora+base)-base is
+      exact, so the result must equal the float64 compose of the oracle bit
+      for bit, on a [T x d] block with T != d (g per output feature)."""
+    for base, lora, g, s, bits in _read_naive_golden(golden_dir):
+        got = naive(np.array([[base]], np.float32), np.array([[lora]], np.float32),
+                    np.array([g], np.float32), s)
+        if np.asarray(got, np.float32).reshape(()).view(np.uint32) != bits:
+            return False
+    rng = np.random.default_rng(77)
+    T, d = 24, 40
+    base = rng.integers(-8, 9, (T, d)).astype(np.float32)
+    lora = rng.integers(-8, 9, (T, d)).astype(np.float32)
+    g = rng.choice([0.0, 0.5, 1.0, 1.5, 2.0, 3.0], d).astype(np.float32)
+    for s in (0.5, 1.0, 2.0):
+        want = oracle.compose(base, lora, g, s)        # exact: every value is a small dyadic
+        got = np.asarray(naive(base, lora, g, s))
+        if got.shape != want.shape or got.dtype != np.float32:
+            return False
+        if not np.array_equal(got.astype(np.float64), want):
+            return False
+    return True
+
+
+def test_naive_comparator_pinned(golden_dir):
+    """The naive comparator (Chinese write-up section 2.1.1) against hand-worked
+    binary32 results and against exact small-dyadic cases."""
+    assert _naive_pins_hold(oracle.naive_compose_f32, golden_dir)
+
+
+def test_naive_pins_catch_planted_mistakes(golden_dir):
+    """Mistakes planted in copies of the naive comparator (on the CPU) fail the
+    pins: the final subtraction flipped, s dropped, g broadcast over tokens
+    instead of features, the stable form in its place, float64 intermediates."""
+    f32 = np.float32
+
+    def plus_base(b, l, g, s):
+        return f32(g)[None, :] * (f32(s) * l + b) + b
+
+    def no_scale(b, l, g, s):
+        return g.astype(f32)[None, :] * (l.astype(f32) + b) - b
+
+    def by_token(b, l, g, s):
+        gg = np.resize(g.astype(f32), b.shape[0])[:, None]
+        return gg * (f32(s) * l + b) - b
+
+    def stable_form(b, l, g, s):
+        g = g.astype(f32)[None, :]
+        return (g - f32(1)) * b + g * (f32(s) * l)
+
+    def in_float64(b, l, g, s):
+        return oracle.compose(b, l, g, s).astype(f32)
+
+    for mutant in (plus_base, no_scale, by_token, stable_form, in_float64):
+        assert not _naive_pins_hold(mutant, golden_dir), mutant.__name__
+
+
 # ------------------------------------------------------------ rounding
 def test_bf16_rounding_golden(golden_dir):
     with open(os.path.join(golden_dir, "bf16_rne.txt")) as f:
