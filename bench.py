@@ -12,11 +12,14 @@ Printed (rank 0, one JSON line):
              by the norm part of the step (CUDA events on the launching stream,
              averaged over the K timed steps, max over ranks)
   compose    compose GB/s over the compose part of the same steps
+  back_to_back  the norm alone, the compose alone and the whole step in loops
+             with one event pair around each loop (no events between launches)
   roofline   the dominant kernel (the U = W A^T main pass) against the measured
-             bf16 peak; roofline_compose the compose kernel against HBM copy BW
+             burst bf16 peak; roofline_compose the compose kernel against HBM copy BW
   e2e        the same metrics through the public API from pinned host buffers,
              host<->device copies inside the timed region
-  cpu_baseline  the float64 CPU oracle on the host cores, bounded sample
+  cpu_baseline  the float64 CPU oracle on the host cores, bounded sample, with the
+             BLAS thread count it ran on and a single-thread sample
   compose_training  the training forward (out, inner) and backward (d_base,
              d_lora, dmag) at the same shape, GB/s
   stack      the 196-module 7B-like stack at r = 128: grouped norm through a
@@ -184,11 +187,85 @@ def oracle_sample(cfg, norm_x, comp_x, g32, rows, tokens):
     return t1 - t0, t2 - t1
 
 
-def cpu_threads():
+def blas_threads():
+    """(threads, how): the thread count of the BLAS library numpy loaded, as
+    that library reports it (threadpoolctl where installed, else the
+    library's exported get_num_threads function found in this process's
+    memory map), else the environment or the core count, saying which."""
+    try:
+        import threadpoolctl
+        info = [d for d in threadpoolctl.threadpool_info() if d.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"]), f"reported by {info[0].get('internal_api', 'blas')}"
+    except Exception:
+        pass
+    try:
+        import ctypes
+        libs = set()
+        with open("/proc/self/maps") as f:
+            for line in f:
+                path = line.split()[-1] if len(line.split()) >= 6 else ""
+                if "openblas" in os.path.basename(path).lower():
+                    libs.add(path)
+        for path in sorted(libs):
+            lib = ctypes.CDLL(path)
+            for name in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                         "openblas_get_num_threads64_", "openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    return int(fn()), "reported by OpenBLAS"
+    except Exception:
+        pass
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
         if os.environ.get(var, "").isdigit():
-            return int(os.environ[var])
-    return os.cpu_count() or 1
+            return int(os.environ[var]), f"from {var}"
+    return os.cpu_count() or 1, "assumed: os.cpu_count()"
+
+
+def cpu_threads():
+    return blas_threads()[0]
+
+
+SINGLE_THREAD_PROBE = r"""
+import json, sys, time
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from synthetic import configs, gen
+import oracle
+cfg = configs.get(int(sys.argv[2]))
+mod = cfg.module
+rows = np.arange(int(sys.argv[3]))
+toks = np.arange(int(sys.argv[4]))
+x = gen.norm_inputs(cfg, rows=rows)
+c = gen.compose_inputs(cfg, tokens=len(toks))
+g32 = np.full(mod.d_out, 1.0, np.float32)
+tn = tc = 0.0
+reps = 0
+while reps < 1 or tn + tc < float(sys.argv[5]):
+    t0 = time.perf_counter()
+    oracle.norm_and_scale(x["W"], x["A"], x["B"], x["m"], cfg.s, float(np.float32(cfg.eps)), cfg.dtype)
+    t1 = time.perf_counter()
+    oracle.compose_stored(c["base"], c["lora"], g32, cfg.s, cfg.dtype)
+    t2 = time.perf_counter()
+    tn += t1 - t0
+    tc += t2 - t1
+    reps += 1
+print(json.dumps({"norm_s": tn, "compose_s": tc, "reps": reps}))
+"""
+
+
+def single_thread_oracle(rows, toks, seconds=4.0):
+    """The oracle on one host thread (BLAS and OpenMP limited to one thread in
+    a fresh interpreter), on the first `rows` norm rows and `toks` compose
+    token rows of the metric workload, repeated for about `seconds`."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    proc = subprocess.run([sys.executable, "-c", SINGLE_THREAD_PROBE, ROOT, str(CFG_INDEX),
+                           str(rows), str(toks), str(seconds)],
+                          env=env, capture_output=True, text=True, timeout=600)
+    if proc.returncode != 0:
+        return None
+    return json.loads(proc.stdout.strip().splitlines()[-1])
 
 
 # ---------------------------------------------------------------- reference arm
@@ -233,7 +310,7 @@ def run_reference(args):
                    "tokens": cfg.tokens, "dtype_inputs": cfg.dtype},
         "compose": {"value": comp_gbs, "unit": "GB/s"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "cores_how": blas_threads()[1], "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -493,6 +570,36 @@ def run_ours(args):
         step(i, kevs[i], main=True)
     torch.cuda.synchronize()
     main_ms = [e[1].elapsed_time(e[2]) for e in kevs]
+
+    # ---- back to back: the norm alone, the compose alone and the whole step,
+    # each in a loop over the rotating sets with one event pair around the
+    # loop and none between launches
+    def norm_only(i):
+        k = i % N_SETS
+        s = sets[k]
+        api.dora_factored_norm(s["W"], s["A"], s["B"], cfg.s, s["m"], cfg.eps, wnorm=wn[k],
+                               g=gg[k], workspace=ws[k])
+
+    def comp_only(i):
+        k = i % N_SETS
+        api.dora_compose(sets[k]["base"], sets[k]["lora"], gg[k], cfg.s, out=outs[k])
+
+    def loop_ms(fn, n):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(n):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    b2b_n = max(3, min(args.steps, 2000))
+    b2b = {"norm_ms": loop_ms(norm_only, b2b_n), "compose_ms": loop_ms(comp_only, b2b_n),
+           "step_ms": loop_ms(step, b2b_n), "calls_per_loop": b2b_n}
     sampler.stop()
     clocks = sampler.summary()
 
@@ -513,9 +620,13 @@ def run_ours(args):
     roofline = {"kernel": "k_gemm_pair main pass (U = W A^T, the folded B G' tiles, sum W^2, "
                           "rowsum(B o D), the fused finalize) on tcgen05 CTA pairs",
                 "bound": "tensor", "achieved": main_tflops,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": main_tflops / peaks["bf16_tflops_sustained"],
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step loop)",
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": main_tflops / peaks["bf16_tflops"],
+                "peak_source": f"{peak_src} bf16 burst: the kernel runs about 50 us at a time "
+                               f"inside a loop of about a second, at the clock sampled in "
+                               f"`clocks` (the sustained figure was taken under the power cap "
+                               f"at a lower clock)",
+                "frac_of_measured_sustained": main_tflops / peaks["bf16_tflops_sustained"],
                 "frac_of_nominal": main_tflops / NOMINAL["bf16_tflops"],
                 "flops_per_launch": mflops, "ms_per_launch": main_ms_m,
                 "timing": f"CUDA events on the launching stream right around the main-pass "
@@ -659,14 +770,31 @@ def run_ours(args):
             tc += b
             passes += 1
         cpu_value = nflops * passes / tn / 1e12
-        cpu_baseline = {"value": cpu_value, "unit": "TFLOP/s", "cores": cpu_threads(),
+        threads, threads_how = blas_threads()
+        st_rows, st_toks = 1024, 256
+        st = single_thread_oracle(st_rows, st_toks)
+        single = None
+        if st is not None:
+            single = {"value": nflops / d_out * st_rows * st["reps"] / st["norm_s"] / 1e12,
+                      "unit": "TFLOP/s", "threads": 1,
+                      "compose": {"value": configs.compose_bytes(st_toks, d_out, cfg.dtype)
+                                  * st["reps"] / st["compose_s"] / 1e9, "unit": "GB/s"},
+                      "sample": f"the first {st_rows} norm rows and {st_toks} compose token rows, "
+                                f"{st['reps']} repetitions ({st['norm_s']:.1f} s norm, "
+                                f"{st['compose_s']:.1f} s compose) in a fresh interpreter with "
+                                f"OPENBLAS_NUM_THREADS = OMP_NUM_THREADS = 1"}
+        cpu_baseline = {"value": cpu_value, "unit": "TFLOP/s", "cores": threads,
+                        "cores_how": f"{threads_how}: the threads of the dense B A product; the "
+                                     f"elementwise numpy steps run on one thread",
+                        "host_cpus": os.cpu_count(),
                         "kind": "oracle",
                         "sample": f"float64 oracle (dense W+sBA row norms via numpy/OpenBLAS, "
                                   f"compose elementwise) on the whole workload, {passes} passes: "
                                   f"norm of all {d_out} rows ({tn:.1f} s in total), compose of all "
                                   f"{T} token rows ({tc:.1f} s in total); TFLOP/s uses the "
                                   f"method's algorithmic FLOPs",
-                        "compose": {"value": cbytes * passes / tc / 1e9, "unit": "GB/s"}}
+                        "compose": {"value": cbytes * passes / tc / 1e9, "unit": "GB/s"},
+                        "single_thread": single}
 
     if rank == 0:
         line = {
@@ -684,6 +812,15 @@ def run_ours(args):
             "norm": {"tflops": value, "ms": norm_ms_m, "modules_per_s": world / (norm_ms_m * 1e-3),
                      "frac_of_measured_bf16": value / peaks["bf16_tflops"],
                      "frac_of_nominal_bf16": value / NOMINAL["bf16_tflops"]},
+            "back_to_back": {
+                **b2b,
+                "norm_tflops": nflops / (b2b["norm_ms"] * 1e-3) / 1e12,
+                "norm_frac_of_measured_bf16": nflops / (b2b["norm_ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                "compose_GB/s": cbytes / (b2b["compose_ms"] * 1e-3) / 1e9,
+                "compose_frac_of_measured_hbm": cbytes / (b2b["compose_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "compose_frac_of_nominal_hbm": cbytes / (b2b["compose_ms"] * 1e-3) / 1e9 / NOMINAL["hbm_gbs"],
+                "timing": "one CUDA event pair around a loop of calls over the rotating sets "
+                          "(no event between launches); per call = loop time / calls"},
             "compose": {"value": comp_gbs, "unit": "GB/s", "ms": comp_ms_m,
                         "elements_per_s": T * d_out * world / (comp_ms_m * 1e-3),
                         "frac_of_measured_hbm": comp_gbs / world / peaks["hbm_gbs"],

@@ -915,22 +915,17 @@ int factored_norm_grouped_impl(const dora_norm_module* mods, int n, int dtype, i
 // that cannot allocate device memory still get a workspace.  Every device
 // that loads this library holds it until the process exits.  In host code the
 // name is only a stand-in for the symbol; its device address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress with the caller's device current.  The address is
+// looked up on every call (a host-side table lookup once the module is
+// loaded), so a context torn down and created again (cudaDeviceReset) never
+// leaves a stale address behind.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-void* g_noalloc_ptr[kMaxDevices] = {nullptr};
-
 int noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DORA_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DORA_ERR_CUDA;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DORA_ERR_CUDA;
+  *out = p;
   return DORA_OK;
 }
 

@@ -145,9 +145,10 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
  * inputs; a shape whose
  * dora_norm_workspace_size exceeds 32 MiB is refused with DORA_ERR_WORKSPACE
  * before anything is enqueued.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *     with the caller's device current), so the address stays right after a
+ *     cudaDeviceReset.  The first call on each device may load the library's
+ *     device code there; make that first call before any stream capture.
  *   - All calls on a device share the one array and it keeps the last call's
  *     contents (every value a call reads from it, the call itself writes
  *     first).  Calls that overlap on the GPU race: issue them on one stream,

@@ -152,3 +152,30 @@ def grad_inputs(cfg: Config, module: int = 0, seed: int = 0,
     mod = cfg.modules[module]
     T = cfg.tokens if tokens is None else tokens
     return normal((seed, cfg.index, T_DOUT, module), T, mod.d_out, cfg.std_grad, cfg.dtype)
+
+
+def stack_inputs_shared_w(cfg: Config, module: int, W: np.ndarray, w_row_len: np.ndarray,
+                          seed: int = 0) -> Dict[str, np.ndarray]:
+    """W, A, B, m of stack module ``module`` when its frozen weight is the
+    stored W of another module of the same shape (drawn once, passed in with
+    its float64 row lengths ``w_row_len``).  A, B and the magnitude noise z
+    come from ``module``'s own Philox keys, and m is built as in
+    :func:`norm_inputs` (``||W_j|| * (1 + 0.0015 z_j)`` in W's dtype), so
+    modules that share W still differ in every adapter tensor.  This keeps a
+    whole 196-module stack cheap to draw for a parity test."""
+    mod = cfg.modules[module]
+    assert W.shape == (mod.d_out, mod.d_in) and w_row_len.shape == (mod.d_out,)
+    base_key = (seed, cfg.index)
+    A = normal(base_key + (T_A, module), cfg.r, mod.d_in, cfg.std_a(mod.d_in), cfg.dtype)
+    B = normal(base_key + (T_B, module), mod.d_out, cfg.r, cfg.std_b, cfg.dtype)
+    z = normal(base_key + (T_M, module), mod.d_out, 1, 1.0, F32).reshape(-1)
+    m32 = (w_row_len * (1.0 + cfg.std_m_rel * z.astype(np.float64))).astype(np.float32)
+    m = f32_to_bf16_bits(m32) if cfg.dtype == BF16 else m32
+    return {"W": W, "A": A, "B": B, "m": m}
+
+
+def row_lengths(W: np.ndarray, dtype: str) -> np.ndarray:
+    """float64 Euclidean length of every row of a stored matrix (input
+    construction of m)."""
+    w64 = to_f64(W, dtype)
+    return np.sqrt(np.einsum("ij,ij->i", w64, w64))

@@ -48,6 +48,46 @@ def test_stack_layer_grouped_norm():
         assert rel_err(wns[k].cpu().numpy(), wn1.cpu().numpy()).max() <= 2e-6
 
 
+def test_full_stack_plan_every_module_sampled_rows():
+    """All 196 modules of the 7B-like stack (r = 128) in one grouped plan run,
+    four seeded rows of every module against the oracle.  The 28 layers share
+    the seven layer-0 weights W (read-only, the same buffers), while A, B and
+    m are drawn per module, so a work item mapped to the wrong module of its
+    shape class, or a wrong per-module table entry, still changes the result
+    (Chinese write-up sections 2.2 and 4.2: the stack of small projections)."""
+    cfg = configs.get(4)
+    n = len(cfg.modules)
+    assert n == 196
+    shared = {}
+    for k in range(7):
+        W = gen.norm_inputs(cfg, module=k)["W"]
+        shared[k] = (W, gen.row_lengths(W, cfg.dtype), to_dev(W, cfg.dtype))
+    xs, mods, rows = [], [], []
+    rng = np.random.default_rng(196)
+    for k in range(n):
+        W, row_len, W_dev = shared[k % 7]
+        x = gen.stack_inputs_shared_w(cfg, k, W, row_len)
+        d_out = cfg.modules[k].d_out
+        xs.append(x)
+        mods.append((W_dev, to_dev(x["A"], cfg.dtype), to_dev(x["B"], cfg.dtype),
+                     to_dev(x["m"], cfg.dtype)))
+        rows.append(np.unique(np.concatenate([[0, d_out - 1], rng.choice(d_out, 2, replace=False)])))
+    ws = torch.empty(api.norm_grouped_workspace_size(mods, torch.bfloat16), dtype=torch.uint8,
+                     device="cuda")
+    plan = api.dora_norm_grouped_plan_create(mods, workspace=ws)
+    try:
+        for _ in range(2):          # two runs of the same plan: the second starts from the first's state
+            plan.run(cfg.s, cfg.eps)
+        torch.cuda.synchronize()
+        assert api.dora_check_status(ws) == 0
+        for k in range(n):
+            wn = plan.wnorms[k].cpu().numpy()
+            g = plan.gs[k].cpu().numpy()
+            _check_norm(cfg, xs[k], wn, g, rows[k])
+    finally:
+        plan.destroy()
+
+
 def _mixed(dtype, r, s, shapes, seed=0):
     out = []
     for i, (d_out, d_in) in enumerate(shapes):

@@ -10,8 +10,8 @@ This file is named to be collected last, so a run that stops at the first
 failure has already run every other test; it also passes alone in a fresh
 process.  The GPU test calls the new entry point through the C ABI twice in a
 row, on two different modules, and compares each result with the existing
-entry point (dora_factored_norm with a caller workspace) within the parity
-tolerances of the other tests.
+entry point (dora_factored_norm with a caller workspace) and with the float64
+CPU oracle, within the parity tolerances of the other tests.
 """
 from __future__ import annotations
 
@@ -48,6 +48,7 @@ def test_oversized_shape_is_refused_before_any_launch():
 def test_noalloc_matches_workspace_entry_point_twice():
     import torch
 
+    import oracle
     from dora_parameter_efficient_gb300 import api
     from tests.parity_util import NORM_RTOL, rel_err, to_dev
 
@@ -71,3 +72,8 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert rel_err(wn.cpu().numpy(), wn_ref.cpu().numpy()).max() <= tol, cfg.name
         assert rel_err(g.cpu().numpy(), g_ref.cpu().numpy()).max() <= tol, cfg.name
         assert np.all(np.isfinite(wn.cpu().numpy()))
+        # and against the float64 oracle on the same stored inputs
+        wn_o, g_o = oracle.norm_and_scale(x["W"], x["A"], x["B"], x["m"], cfg.s,
+                                          float(np.float32(cfg.eps)), cfg.dtype)
+        assert rel_err(wn.cpu().numpy(), wn_o).max() <= tol, cfg.name
+        assert rel_err(g.cpu().numpy(), g_o).max() <= tol, cfg.name
