@@ -50,6 +50,13 @@ SIGNATURES = {
     "dora_factored_norm_noalloc": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64,
                                                   ctypes.c_float, _P, ctypes.c_float, _P, _P,
                                                   _P]),
+    "dora_norm_partials_floats": (ctypes.c_size_t, [_I64, _I64]),
+    "dora_norm_partials": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _P, _P,
+                                          ctypes.c_size_t, _P]),
+    "dora_norm_finalize_workspace_size": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int]),
+    "dora_norm_finalize_partials": (ctypes.c_int, [_P, _P, ctypes.c_int, _I64, _I64,
+                                                   ctypes.c_float, _P, ctypes.c_float, _P, _P, _P,
+                                                   ctypes.c_size_t, _P]),
     "dora_compose": (ctypes.c_int, [_P, _P, _P, ctypes.c_float, ctypes.c_int, _I64, _I64, _P, _P]),
     "dora_norm_grouped_workspace_size": (ctypes.c_size_t, [_P, ctypes.c_int, _I64, ctypes.c_int]),
     "dora_factored_norm_grouped": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int, _I64,

@@ -88,6 +88,124 @@ def dora_factored_norm(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: flo
     return wnorm, g
 
 
+# ---------------------------------------------------------------- d_in-sharded norm
+def norm_partials_floats(d_out: int, r: int) -> int:
+    """Length of the partials buffer: 2 d_out + r^2 float32 values."""
+    return 2 * int(d_out) + int(r) * int(r)
+
+
+def partials_views(partials: torch.Tensor, d_out: int, r: int):
+    """(base [d_out], cross [d_out], G [r, r]) views of a partials buffer."""
+    if partials.dim() != 1 or partials.numel() != norm_partials_floats(d_out, r):
+        raise ValueError(f"partials must be 1-D with {norm_partials_floats(d_out, r)} values")
+    return (partials[:d_out], partials[d_out:2 * d_out],
+            partials[2 * d_out:].view(int(r), int(r)))
+
+
+def slice_bounds(d_in: int, parts: int, index: int, dtype: torch.dtype) -> Tuple[int, int]:
+    """Columns [k0, k1) of d_in held by slice `index` of `parts` when W and A
+    are split along d_in: near-equal widths on a 64-column grid (the main
+    pass's K tile), so every slice's rows stay 16-byte multiples; the last
+    slice takes the remainder.  Host logic only."""
+    if parts < 1 or not 0 <= index < parts or d_in < 0:
+        raise ValueError("need parts >= 1, 0 <= index < parts and d_in >= 0")
+    eb = torch.tensor([], dtype=dtype).element_size()
+    if (d_in * eb) % 16 != 0:
+        raise ValueError("d_in * element size must be a multiple of 16 bytes")
+    tiles = -(-d_in // 64)
+    k0 = min(d_in, (tiles * index // parts) * 64)
+    k1 = d_in if index == parts - 1 else min(d_in, (tiles * (index + 1) // parts) * 64)
+    return k0, k1
+
+
+def dora_norm_partials(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                       partials: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """The partials of one d_in slice: base = sum W^2, cross = rowsum(B o (W A^T))
+    and G = A A^T over the slice's columns, as one float32 buffer
+    [2 d_out + r^2] (W [d_out, d_in_slice], A [r, d_in_slice], B [d_out, r])."""
+    code = _dtype_code(W)
+    for t, name in ((A, "A"), (B, "B")):
+        if t.dtype != W.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, W has {W.dtype}")
+    d_out, d_in = W.shape
+    r = A.shape[0]
+    if A.shape != (r, d_in) or B.shape != (d_out, r):
+        raise ValueError(f"shape mismatch: W{tuple(W.shape)} A{tuple(A.shape)} B{tuple(B.shape)}")
+    n = norm_partials_floats(d_out, r)
+    if partials is None:
+        partials = torch.empty(n, dtype=torch.float32, device=W.device)
+    elif partials.dtype != torch.float32 or partials.numel() != n:
+        raise ValueError(f"partials must be float32 with {n} values")
+    if workspace is None:
+        workspace = alloc_workspace(d_out, d_in, r, W.dtype, W.device)
+    st = _lib.load().dora_norm_partials(_dev(W, "W"), _dev(A, "A"), _dev(B, "B"), code, d_out,
+                                        d_in, r, _dev(partials, "partials"),
+                                        _dev(workspace, "workspace"), workspace.numel(),
+                                        _stream_handle(stream))
+    check(st, "dora_norm_partials")
+    return partials
+
+
+def finalize_workspace_size(d_out: int, r: int, dtype: torch.dtype) -> int:
+    return int(_lib.load().dora_norm_finalize_workspace_size(d_out, r, _DTYPES[dtype]))
+
+
+def dora_norm_finalize_partials(partials: torch.Tensor, B: torch.Tensor, s: float,
+                                m: torch.Tensor, eps: float,
+                                wnorm: Optional[torch.Tensor] = None,
+                                g: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream: Optional[torch.cuda.Stream] = None
+                                ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """wnorm and g from partials summed over every d_in slice (B [d_out, r],
+    m [d_out] in the inputs' dtype)."""
+    code = _dtype_code(B)
+    d_out, r = B.shape
+    if m.dtype != B.dtype or m.shape != (d_out,):
+        raise ValueError("m must match B's dtype and have d_out values")
+    if partials.dtype != torch.float32 or partials.numel() != norm_partials_floats(d_out, r):
+        raise ValueError("partials must be float32 [2 d_out + r^2]")
+    if wnorm is None:
+        wnorm = torch.empty(d_out, dtype=torch.float32, device=B.device)
+    if g is None:
+        g = torch.empty(d_out, dtype=torch.float32, device=B.device)
+    if workspace is None:
+        n = finalize_workspace_size(d_out, r, B.dtype)
+        if n == 0:
+            raise ValueError("invalid shape for dora_norm_finalize_partials")
+        workspace = torch.empty(n, dtype=torch.uint8, device=B.device)
+    st = _lib.load().dora_norm_finalize_partials(
+        _dev(partials, "partials"), _dev(B, "B"), code, d_out, r, float(s), _dev(m, "m"),
+        float(eps), _dev(wnorm, "wnorm"), _dev(g, "g"), _dev(workspace, "workspace"),
+        workspace.numel(), _stream_handle(stream))
+    check(st, "dora_norm_finalize_partials")
+    return wnorm, g
+
+
+def allreduce_partials(partials: torch.Tensor, group=None) -> torch.Tensor:
+    """The one exchange of the d_in-sharded norm: the partials of every rank
+    of `group` summed in place (torch.distributed all-reduce; NCCL between
+    GPUs).  The sum's order is the collective's, so results agree with the
+    single-device norm up to fp32 rounding of the partials."""
+    import torch.distributed as dist
+    dist.all_reduce(partials, op=dist.ReduceOp.SUM, group=group)
+    return partials
+
+
+def dora_factored_norm_sharded(W: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
+                               m: torch.Tensor, eps: float, group=None
+                               ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The norm of a module whose W and A are split along d_in over the ranks
+    of `group` (this rank holds W [d_out, d_in_slice], A [r, d_in_slice] and
+    all of B and m): the slice's partials, one all-reduce of 2 d_out + r^2
+    floats, then wnorm and g for every row on every rank."""
+    partials = dora_norm_partials(W, A, B)
+    allreduce_partials(partials, group)
+    return dora_norm_finalize_partials(partials, B, s, m, eps)
+
+
 def dora_compose(base: torch.Tensor, lora: torch.Tensor, g: torch.Tensor, s: float,
                  out: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:

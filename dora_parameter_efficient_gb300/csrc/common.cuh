@@ -53,6 +53,10 @@ struct GramParams {
   float scale;           // G' = scale * G, split into G_hi + G_lo
   uint16_t* G_hi;
   uint16_t* G_lo;
+  // partials mode: G itself (times scale) in fp32, [r_out x r_out] row-major,
+  // written instead of the split (G_hi / G_lo unused)
+  float* G_f32;
+  int r_out;
   int* status;
   unsigned long long timeout_ns;
 };
@@ -118,6 +122,16 @@ struct PairParams {
   int* tile_done;        // [pair_tiles][2] segments finished per 128-row group (zero at launch)
   float* wnorm;          // [rows]
   float* g;              // [rows]
+  // single-module launch only (null otherwise):
+  //   sums_base / sums_cross: the fused finalize writes the sums of the split
+  //   partials (base = sum W^2, cross = rowsum(B o D)) here, rounded to fp32,
+  //   instead of wnorm and g (the partials of a d_in slice);
+  //   ext_base / ext_cross: summed partials of the whole d_in range, added
+  //   ahead of the split partials before wnorm and g are assembled
+  float* sums_base;
+  float* sums_cross;
+  const float* ext_base;
+  const float* ext_cross;
   int* work_ctr;         // next unclaimed work item (or range slot); zero at launch
   int* status;
   unsigned long long timeout_ns;
@@ -264,7 +278,16 @@ cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t c
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
                             int n_cross, const float* pba, int n_ba, float s, const void* m,
                             int is_bf16, float eps, float* wnorm, float* g,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const float* ext_base = nullptr,
+                            const float* ext_cross = nullptr);
+// the sums of the split partials (base and cross, in split order) rounded to
+// fp32, written to sum_base / sum_cross: the partials of a d_in slice
+cudaError_t launch_sum_partials(int64_t d_out, const float* pbase, int n_base,
+                                const float* pcross, int n_cross, float* sum_base,
+                                float* sum_cross, cudaStream_t stream);
+// G' = scale * G [r x r] fp32 split into bf16 G'_hi + G'_lo [rp x rp], zero padded
+cudaError_t launch_gram_split(const float* G, int r, int rp, float scale, uint16_t* G_hi,
+                              uint16_t* G_lo, cudaStream_t stream);
 cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
                            int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,
                            cudaStream_t stream);

@@ -293,20 +293,36 @@ int gram_cluster_for(int k_tiles) {
   return c;
 }
 
+// What one main-pass launch covers: the whole norm (W tiles, then the (B, G')
+// tiles, fused finalize), the partials of a d_in slice (W tiles only, the
+// sums written out), or the finalize from summed partials ((B, G') tiles only).
+enum PassMode { kPassFull = 0, kPassSlice = 1, kPassFinal = 2 };
+
 // The work decomposition of a single-module bf16 main pass: N split, K tiles,
 // pair tiles, K segments or static ranges.  Returns the CTA pairs to launch.
 // The norm and the schedule self-test both plan through here.
-int plan_main_pass(PairParams& pp, int64_t d_out, int64_t d_in, int64_t r, int clusters_max) {
+int plan_main_pass(PairParams& pp, int64_t d_out, int64_t d_in, int64_t r, int clusters_max,
+                   int mode = kPassFull) {
   const int rp = static_cast<int>(ceil_div(r, 16) * 16);
   pp.n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
   pp.n1 = rp - pp.n0;
-  pp.kt_w = static_cast<int>(ceil_div(d_in, kTcBlockK));
-  pp.kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
+  pp.kt_w = mode == kPassFinal ? 0 : static_cast<int>(ceil_div(d_in, kTcBlockK));
+  pp.kt_b = mode == kPassSlice ? 0 : static_cast<int>(ceil_div(r, kTcBlockK));
   pp.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
+  if (mode == kPassFinal && pp.pair_tiles < clusters_max) {
+    // only the short (B, G') range: one item per pair tile, no K split
+    pp.splits = 1;
+    pp.seg_k[0] = 0;
+    pp.seg_k[1] = 2 * pp.kt_b;
+    pp.ranges = 0;
+    return pp.pair_tiles;
+  }
   plan_pair_segments(pp, clusters_max);
+  // the Gram kernel shares the SMs with the first pairs unless the pass
+  // starts from a finished G
   const int gnb = gram_nb(rp), gcl = gram_cluster_for(pp.kt_w);
-  if (plan_pair_ranges(pp, clusters_max, gnb * (gnb + 1) / 2 * gcl,
-                       static_cast<int>(ceil_div(pp.kt_w, gcl))))
+  const int gram_ctas = mode == kPassFinal ? 0 : gnb * (gnb + 1) / 2 * gcl;
+  if (plan_pair_ranges(pp, clusters_max, gram_ctas, static_cast<int>(ceil_div(pp.kt_w, gcl))))
     return pp.ranges;
   const int items = pp.pair_tiles * pp.splits;
   return items < clusters_max ? items : clusters_max;
@@ -326,6 +342,246 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? DORA_OK : DORA_ERR_CU
     const cudaError_t e_ = (expr);           \
     if (e_ != cudaSuccess) return DORA_ERR_CUDA; \
   } while (0)
+
+// The bf16 tensor-core path of the norm in one of three modes (PassMode).
+//   kPassFull: G = A A^T with G' = (s/2) G split into two bf16 terms (one
+//     cluster of CTAs per upper-triangular 128 x 128 block, K split across
+//     the cluster), then the CTA-pair main pass with the BA-norm tiles folded
+//     into its K loop, which also finalizes every 128-row group as its last K
+//     segment lands.
+//   kPassSlice: the partials of a d_in slice -- G = A A^T in fp32 into
+//     part_out + 2 d_out, and the main pass over the W tiles only, its fused
+//     finalize writing the sums of base and cross to part_out, part_out + d_out.
+//   kPassFinal: G' from the summed G of part_in + 2 d_out (split kernel), the
+//     main pass over the (B, G') tiles only, its finalize adding the summed
+//     base and cross of part_in ahead of its own partials.
+int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, int64_t d_in,
+                  int64_t r, float s, const void* m, float eps, float* wnorm, float* g,
+                  const Plan& plan, uint8_t* ws, int mode, float* part_out,
+                  const float* part_in, cudaStream_t stream, void* ev_begin, void* ev_end) {
+  int* status = reinterpret_cast<int*>(ws + plan.off_status);
+  uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + plan.off_Ghi);
+  uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + plan.off_Glo);
+  const int rp = plan.rp;
+  const int gnb = gram_nb(rp), gbw = gram_bw(rp);
+  const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
+  const uint32_t tmem_cols = [&] {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(rp)) c <<= 1;
+    return c;
+  }();
+  // N split of the pair MMAs: each CTA of the pair holds half of every chunk
+  const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
+  const int n1 = rp - n0;
+  const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
+  CUtensorMap mW, mA_x, mA_yg, mA_y2, mB_x, mGhi, mGlo;
+  // (a slice of a module without rows only has its Gram partial)
+  if (d_out > 0 && !make_map_bf16(&mB_x, B, r, d_out, kTcBlockM)) return DORA_ERR_CUDA;
+  if (mode != kPassFinal) {
+    if ((d_out > 0 && !make_map_bf16(&mW, W, d_in, d_out, kTcBlockM)) ||
+        !make_map_bf16(&mA_x, A, d_in, r, kTcBlockM) ||
+        !make_map_bf16(&mA_yg, A, d_in, r, gbw) || !make_map_bf16(&mA_y2, A, d_in, r, y_box2))
+      return DORA_ERR_CUDA;
+  } else {
+    // no W and A tiles: the kernel only prefetches these descriptors
+    mW = mB_x;
+  }
+  if (mode != kPassSlice) {
+    if (!make_map_bf16(&mGhi, Ghi, rp, rp, y_box2) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box2))
+      return DORA_ERR_CUDA;
+  } else {
+    mGhi = mA_y2;
+    mGlo = mA_y2;
+  }
+  if (mode == kPassFinal) mA_y2 = mGhi;
+
+  if (mode == kPassFinal) {
+    DORA_TRY(launch_gram_split(part_in + 2 * d_out, static_cast<int>(r), rp, 0.5f * s, Ghi, Glo,
+                               stream));
+  } else {
+    GramParams pg{};
+    pg.nb = gnb;
+    pg.bw = gbw;
+    pg.rp = rp;
+    pg.k_tiles = k_tiles;
+    pg.stages = kGramStages;
+    pg.cluster = gram_cluster_for(k_tiles);
+    pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
+    pg.scale = mode == kPassSlice ? 1.f : 0.5f * s;
+    pg.G_hi = Ghi;
+    pg.G_lo = Glo;
+    if (mode == kPassSlice) {
+      pg.G_f32 = part_out + 2 * d_out;
+      pg.r_out = static_cast<int>(r);
+    }
+    pg.status = status;
+    pg.timeout_ns = kDefaultTimeoutNs;
+    DORA_TRY(launch_gram(mA_x, mA_yg, pg, stream));
+  }
+  if (d_out == 0) return DORA_OK;
+
+  PairParams pp{};
+  pp.rows = static_cast<int>(d_out);
+  pp.y_box_rows = y_box2;
+  pp.stages = pair_pick_stages(rp, false);
+  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, false));
+  if (clusters_max <= 0) return DORA_ERR_CUDA;
+  const int clusters = plan_main_pass(pp, d_out, d_in, r, clusters_max, mode);
+  if (pp.n0 != n0 || pp.n1 != n1) return DORA_ERR_UNSUPPORTED;
+  pp.r = static_cast<int>(r);
+  // two accumulators when they fit in the 512 tensor-memory columns
+  pp.acc_stride = tmem_cols;
+  pp.acc_bufs = 2 * tmem_cols <= 512 ? 2 : 1;
+  pp.tmem_cols = tmem_cols * static_cast<uint32_t>(pp.acc_bufs);
+  pp.B = static_cast<const uint16_t*>(B);
+  pp.m = static_cast<const uint16_t*>(m);
+  // the sum over splits of rowsum(B o D) is cross + (s/2) ba, so the
+  // finalize's 2s * cross term carries the BA-norm term too
+  pp.two_s = 2.f * s;
+  pp.s_sq = s * s;
+  pp.eps = eps;
+  pp.out_sumsq = reinterpret_cast<float*>(ws + plan.off_pbase);
+  pp.out_dot = reinterpret_cast<float*>(ws + plan.off_pcross);
+  pp.tile_done = status + kCtlTileDone;
+  pp.wnorm = wnorm;
+  pp.g = g;
+  if (mode == kPassSlice) {
+    pp.sums_base = part_out;
+    pp.sums_cross = part_out + d_out;
+  } else if (mode == kPassFinal) {
+    pp.ext_base = part_in;
+    pp.ext_cross = part_in + d_out;
+  }
+  pp.work_ctr = status + kCtlWork;
+  pp.status = status;
+  pp.timeout_ns = kDefaultTimeoutNs;
+  if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
+  DORA_TRY(launch_gemm_pair(mW, mA_y2, mB_x, mGhi, mGlo, pp, clusters, stream));
+  if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
+  return DORA_OK;
+}
+
+// The fp32 (3xTF32) tensor-core path of the norm, in the modes of
+// run_bf16_pass.  kPassFull: G = A A^T in K segments, their sum scaled to
+// G' = (s/2) G, then the pair pass over (W, A) and (B, G') tiles in N passes
+// of up to 256 columns; the finalize kernel adds the partials.  kPassSlice:
+// the Gram's segments summed unscaled into part_out + 2 d_out, the pass over
+// the W tiles only, the sums of its partials written to part_out.
+// kPassFinal: G' = (s/2) G from part_in + 2 d_out, the pass over the (B, G')
+// tiles only, and the finalize adding part_in's base and cross first.
+int run_f32_pass(const void* W, const void* A, const void* B, int64_t d_out, int64_t d_in,
+                 int64_t r, float s, const void* m, float eps, float* wnorm, float* g,
+                 const Plan& plan, uint8_t* ws, int mode, float* part_out,
+                 const float* part_in, cudaStream_t stream, void* ev_begin, void* ev_end) {
+  int* status = reinterpret_cast<int*>(ws + plan.off_status);
+  float* G = reinterpret_cast<float*>(ws + plan.off_G);
+  float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
+  float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
+  float* Gpart = reinterpret_cast<float*>(ws + plan.off_Gpart);
+  const int rp = plan.rp;
+  const int passes = static_cast<int>(ceil_div(rp, 256));
+  const int n_pass = static_cast<int>(ceil_div(ceil_div(rp, passes), 16) * 16);
+  const int yr = n_pass / 2;
+  const int clusters_max = tf32_max_clusters();
+  if (clusters_max <= 0) return DORA_ERR_CUDA;
+  uint32_t acc_stride = 32;
+  while (acc_stride < static_cast<uint32_t>(n_pass)) acc_stride <<= 1;
+  const int kt_x = mode == kPassFinal ? 0 : static_cast<int>(ceil_div(d_in, kTf32BlockK));
+  CUtensorMap mW, mA_x, mA_y, mB_x, mG_y;
+  // (a slice of a module without rows only has its Gram partial)
+  if (d_out > 0 && !make_map_f32(&mB_x, B, r, d_out, kTcBlockM)) return DORA_ERR_CUDA;
+  if (mode != kPassFinal) {
+    if ((d_out > 0 && !make_map_f32(&mW, W, d_in, d_out, kTcBlockM)) ||
+        !make_map_f32(&mA_x, A, d_in, r, kTcBlockM) || !make_map_f32(&mA_y, A, d_in, r, yr))
+      return DORA_ERR_CUDA;
+  }
+  if (mode != kPassSlice) {
+    if (!make_map_f32(&mG_y, G, rp, rp, yr)) return DORA_ERR_CUDA;
+  } else {
+    mG_y = mA_y;
+  }
+  if (mode == kPassFinal) {
+    // no (W, A) tiles: the kernel only prefetches these descriptors
+    mW = mB_x;
+    mA_y = mG_y;
+  }
+
+  if (mode == kPassFinal) {
+    // one "segment": G' = (s/2) G, zero padded to rp x rp
+    DORA_TRY(launch_gram_tf32_reduce(part_in + 2 * d_out, 1, static_cast<int>(r), rp, 0.5f * s,
+                                     G, stream));
+  } else {
+    Tf32Params pg{};
+    pg.rows = static_cast<int>(r);
+    pg.n_pass = n_pass;
+    pg.passes = passes;
+    pg.kt_x = kt_x;
+    pg.kt_b = 0;
+    pg.pair_tiles = static_cast<int>(ceil_div(r, 2 * kTcBlockM));
+    {
+      const int units = pg.pair_tiles * passes;
+      int sp = static_cast<int>(ceil_div(clusters_max, units));
+      if (sp > kTf32MaxGramSplits) sp = kTf32MaxGramSplits;
+      if (sp > kt_x) sp = kt_x;
+      if (sp < 1) sp = 1;
+      pg.splits = sp;
+      for (int i = 0; i <= sp; ++i) pg.seg_k[i] = static_cast<int>((static_cast<int64_t>(kt_x) * i) / sp);
+    }
+    pg.n_items = pg.pair_tiles * passes * pg.splits;
+    pg.stages = tf32_pick_stages(n_pass);
+    pg.acc_stride = acc_stride;
+    pg.r = static_cast<int>(r);
+    pg.out_g = Gpart;
+    pg.status = status;
+    pg.timeout_ns = kDefaultTimeoutNs;
+    DORA_TRY(launch_gemm_tf32(mA_x, mA_y, mA_x, mA_y, pg, true,
+                              pg.n_items < clusters_max ? pg.n_items : clusters_max, stream));
+    if (mode == kPassSlice) {
+      // G of this slice, [r x r] unscaled and unpadded
+      DORA_TRY(launch_gram_tf32_reduce(Gpart, pg.splits, static_cast<int>(r), static_cast<int>(r),
+                                       1.f, part_out + 2 * d_out, stream));
+    } else {
+      DORA_TRY(launch_gram_tf32_reduce(Gpart, pg.splits, static_cast<int>(r), rp, 0.5f * s, G,
+                                       stream));
+    }
+  }
+  if (d_out == 0) return DORA_OK;
+
+  Tf32Params pm{};
+  pm.rows = static_cast<int>(d_out);
+  pm.n_pass = n_pass;
+  pm.passes = passes;
+  pm.kt_x = kt_x;
+  pm.kt_b = mode == kPassSlice ? 0 : static_cast<int>(ceil_div(rp, kTf32BlockK));
+  pm.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
+  {
+    const int ktot = pm.kt_x + pm.kt_b;
+    const int sp = pick_pair_splits(static_cast<int64_t>(pm.pair_tiles) * passes, ktot,
+                                    clusters_max, kMaxFinalParts / passes);
+    pm.splits = sp;
+    for (int i = 0; i <= sp; ++i) pm.seg_k[i] = static_cast<int>((static_cast<int64_t>(ktot) * i) / sp);
+  }
+  pm.n_items = pm.pair_tiles * passes * pm.splits;
+  pm.stages = tf32_pick_stages(n_pass);
+  pm.acc_stride = acc_stride;
+  pm.B = static_cast<const float*>(B);
+  pm.r = static_cast<int>(r);
+  pm.out_sumsq = pbase;
+  pm.out_dot = pcross;
+  pm.status = status;
+  pm.timeout_ns = kDefaultTimeoutNs;
+  if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
+  DORA_TRY(launch_gemm_tf32(mW, mA_y, mB_x, mG_y, pm, false,
+                            pm.n_items < clusters_max ? pm.n_items : clusters_max, stream));
+  if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
+  if (mode == kPassSlice)
+    return cuda_status(launch_sum_partials(d_out, pbase, pm.splits, pcross, passes * pm.splits,
+                                           part_out, part_out + d_out, stream));
+  return cuda_status(launch_finalize(d_out, pbase, pm.splits, pcross, passes * pm.splits, nullptr,
+                                     0, s, m, /*is_bf16=*/0, eps, wnorm, g, stream,
+                                     mode == kPassFinal ? part_in : nullptr,
+                                     mode == kPassFinal ? part_in + d_out : nullptr));
+}
 
 int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, int64_t d_out,
                        int64_t d_in, int64_t r, float s, const void* m, float eps, float* wnorm,
@@ -365,16 +621,12 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws + plan.off_status);
-  float* G = reinterpret_cast<float*>(ws + plan.off_G);
-  uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + plan.off_Ghi);
-  uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + plan.off_Glo);
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
-  float* Gpart = reinterpret_cast<float*>(ws + plan.off_Gpart);
 
   DORA_TRY(cudaMemsetAsync(status, 0, plan.zero_bytes, stream));
 
-  int n_base = 0, n_cross = 0;
+  int n_base = 0;
   if (d_in == 0) {
     // W has no columns: every term is zero.
   } else if (!adapter) {
@@ -384,159 +636,120 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
     n_base = 1;
   } else if (bf16) {
-    // G = A A^T with G' = (s/2) G split into two bf16 terms (one cluster of
-    // CTAs per upper-triangular 128 x 128 block, K split across the cluster),
-    // then the CTA-pair main pass with the BA-norm tiles folded into its K
-    // loop, which also finalizes every 128-row group as its last K segment
-    // lands.
-    const int rp = plan.rp;
-    const int gnb = gram_nb(rp), gbw = gram_bw(rp);
-    const int k_tiles = static_cast<int>(ceil_div(d_in, kTcBlockK));
-    const uint32_t tmem_cols = [&] {
-      uint32_t c = 32;
-      while (c < static_cast<uint32_t>(rp)) c <<= 1;
-      return c;
-    }();
-    // N split of the pair MMAs: each CTA of the pair holds half of every chunk
-    const int n0 = rp <= 256 ? rp : static_cast<int>(ceil_div(rp / 2, 16) * 16);
-    const int n1 = rp - n0;
-    const int y_box2 = n1 > 0 ? gcd_int(n0 / 2, n1 / 2) : n0 / 2;
-    CUtensorMap mW, mA_x, mA_yg, mA_y2, mB_x, mGhi, mGlo;
-    if (!make_map_bf16(&mW, W, d_in, d_out, kTcBlockM) ||
-        !make_map_bf16(&mA_x, A, d_in, r, kTcBlockM) ||
-        !make_map_bf16(&mA_yg, A, d_in, r, gbw) ||
-        !make_map_bf16(&mA_y2, A, d_in, r, y_box2) ||
-        !make_map_bf16(&mB_x, B, r, d_out, kTcBlockM) ||
-        !make_map_bf16(&mGhi, Ghi, rp, rp, y_box2) || !make_map_bf16(&mGlo, Glo, rp, rp, y_box2))
-      return DORA_ERR_CUDA;
-
-    GramParams pg{};
-    pg.nb = gnb;
-    pg.bw = gbw;
-    pg.rp = rp;
-    pg.k_tiles = k_tiles;
-    pg.stages = kGramStages;
-    pg.cluster = gram_cluster_for(k_tiles);
-    pg.tmem_cols = gbw <= 32 ? 32u : (gbw <= 64 ? 64u : 128u);
-    pg.scale = 0.5f * s;
-    pg.G_hi = Ghi;
-    pg.G_lo = Glo;
-    pg.status = status;
-    pg.timeout_ns = kDefaultTimeoutNs;
-    DORA_TRY(launch_gram(mA_x, mA_yg, pg, stream));
-
-    PairParams pp{};
-    pp.rows = static_cast<int>(d_out);
-    pp.y_box_rows = y_box2;
-    pp.stages = pair_pick_stages(rp, false);
-    const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, false));
-    if (clusters_max <= 0) return DORA_ERR_CUDA;
-    const int clusters = plan_main_pass(pp, d_out, d_in, r, clusters_max);
-    if (pp.n0 != n0 || pp.n1 != n1 || pp.kt_w != k_tiles) return DORA_ERR_UNSUPPORTED;
-    pp.r = static_cast<int>(r);
-    // two accumulators when they fit in the 512 tensor-memory columns
-    pp.acc_stride = tmem_cols;
-    pp.acc_bufs = 2 * tmem_cols <= 512 ? 2 : 1;
-    pp.tmem_cols = tmem_cols * static_cast<uint32_t>(pp.acc_bufs);
-    pp.B = static_cast<const uint16_t*>(B);
-    pp.m = static_cast<const uint16_t*>(m);
-    // the sum over splits of rowsum(B o D) is cross + (s/2) ba, so the
-    // finalize's 2s * cross term carries the BA-norm term too
-    pp.two_s = 2.f * s;
-    pp.s_sq = s * s;
-    pp.eps = eps;
-    pp.out_sumsq = pbase;
-    pp.out_dot = pcross;
-    pp.tile_done = status + kCtlTileDone;
-    pp.wnorm = wnorm;
-    pp.g = g;
-    pp.work_ctr = status + kCtlWork;
-    pp.status = status;
-    pp.timeout_ns = kDefaultTimeoutNs;
-    if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
-    DORA_TRY(launch_gemm_pair(mW, mA_y2, mB_x, mGhi, mGlo, pp, clusters, stream));
-    if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
-    return DORA_OK;
+    return run_bf16_pass(W, A, B, d_out, d_in, r, s, m, eps, wnorm, g, plan, ws, kPassFull,
+                         nullptr, nullptr, stream, ev_begin, ev_end);
   } else {
-    // fp32 inputs: the 3xTF32 tensor-core pass (gemm_tf32.cu).  G = A A^T in
-    // K segments, their sum scaled to G' = (s/2) G, then the pair pass over
-    // (W, A) and (B, G') tiles in N passes of up to 256 columns; the finalize
-    // kernel adds the partials.
-    const int rp = plan.rp;
-    const int passes = static_cast<int>(ceil_div(rp, 256));
-    const int n_pass = static_cast<int>(ceil_div(ceil_div(rp, passes), 16) * 16);
-    const int yr = n_pass / 2;
-    const int clusters_max = tf32_max_clusters();
-    if (clusters_max <= 0) return DORA_ERR_CUDA;
-    uint32_t acc_stride = 32;
-    while (acc_stride < static_cast<uint32_t>(n_pass)) acc_stride <<= 1;
-    const int kt_x = static_cast<int>(ceil_div(d_in, kTf32BlockK));
-    CUtensorMap mW, mA_x, mA_y, mB_x, mG_y;
-    if (!make_map_f32(&mW, W, d_in, d_out, kTcBlockM) ||
-        !make_map_f32(&mA_x, A, d_in, r, kTcBlockM) || !make_map_f32(&mA_y, A, d_in, r, yr) ||
-        !make_map_f32(&mB_x, B, r, d_out, kTcBlockM) || !make_map_f32(&mG_y, G, rp, rp, yr))
-      return DORA_ERR_CUDA;
-
-    Tf32Params pg{};
-    pg.rows = static_cast<int>(r);
-    pg.n_pass = n_pass;
-    pg.passes = passes;
-    pg.kt_x = kt_x;
-    pg.kt_b = 0;
-    pg.pair_tiles = static_cast<int>(ceil_div(r, 2 * kTcBlockM));
-    {
-      const int units = pg.pair_tiles * passes;
-      int sp = static_cast<int>(ceil_div(clusters_max, units));
-      if (sp > kTf32MaxGramSplits) sp = kTf32MaxGramSplits;
-      if (sp > kt_x) sp = kt_x;
-      if (sp < 1) sp = 1;
-      pg.splits = sp;
-      for (int i = 0; i <= sp; ++i) pg.seg_k[i] = static_cast<int>((static_cast<int64_t>(kt_x) * i) / sp);
-    }
-    pg.n_items = pg.pair_tiles * passes * pg.splits;
-    pg.stages = tf32_pick_stages(n_pass);
-    pg.acc_stride = acc_stride;
-    pg.r = static_cast<int>(r);
-    pg.out_g = Gpart;
-    pg.status = status;
-    pg.timeout_ns = kDefaultTimeoutNs;
-    DORA_TRY(launch_gemm_tf32(mA_x, mA_y, mA_x, mA_y, pg, true,
-                              pg.n_items < clusters_max ? pg.n_items : clusters_max, stream));
-    DORA_TRY(launch_gram_tf32_reduce(Gpart, pg.splits, static_cast<int>(r), rp, 0.5f * s, G, stream));
-
-    Tf32Params pm{};
-    pm.rows = static_cast<int>(d_out);
-    pm.n_pass = n_pass;
-    pm.passes = passes;
-    pm.kt_x = kt_x;
-    pm.kt_b = static_cast<int>(ceil_div(rp, kTf32BlockK));
-    pm.pair_tiles = static_cast<int>(ceil_div(d_out, 2 * kTcBlockM));
-    {
-      const int ktot = pm.kt_x + pm.kt_b;
-      const int sp = pick_pair_splits(static_cast<int64_t>(pm.pair_tiles) * passes, ktot,
-                                      clusters_max, kMaxFinalParts / passes);
-      pm.splits = sp;
-      for (int i = 0; i <= sp; ++i) pm.seg_k[i] = static_cast<int>((static_cast<int64_t>(ktot) * i) / sp);
-    }
-    pm.n_items = pm.pair_tiles * passes * pm.splits;
-    pm.stages = pg.stages;
-    pm.acc_stride = acc_stride;
-    pm.B = static_cast<const float*>(B);
-    pm.r = static_cast<int>(r);
-    pm.out_sumsq = pbase;
-    pm.out_dot = pcross;
-    pm.status = status;
-    pm.timeout_ns = kDefaultTimeoutNs;
-    if (ev_begin) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_begin), stream));
-    DORA_TRY(launch_gemm_tf32(mW, mA_y, mB_x, mG_y, pm, false,
-                              pm.n_items < clusters_max ? pm.n_items : clusters_max, stream));
-    if (ev_end) DORA_TRY(cudaEventRecord(static_cast<cudaEvent_t>(ev_end), stream));
-    n_base = pm.splits;
-    n_cross = passes * pm.splits;
+    return run_f32_pass(W, A, B, d_out, d_in, r, s, m, eps, wnorm, g, plan, ws, kPassFull,
+                        nullptr, nullptr, stream, ev_begin, ev_end);
   }
-  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, n_cross, nullptr, 0, s, m, bf16, eps,
-                           wnorm, g, stream));
+  DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, 0, nullptr, 0, s, m, bf16, eps, wnorm,
+                           g, stream));
   return DORA_OK;
+}
+
+// ---------------------------------------------------------------- d_in-sharded norm
+// Floats of the partials of one d_in slice: base [d_out], cross [d_out], G [r x r].
+size_t partials_floats(int64_t d_out, int64_t r) {
+  return 2 * static_cast<size_t>(d_out) + static_cast<size_t>(r) * static_cast<size_t>(r);
+}
+
+int norm_partials_impl(const void* W, const void* A, const void* B, int dtype, int64_t d_out,
+                       int64_t d_in, int64_t r, float* partials, void* workspace,
+                       size_t workspace_bytes, void* stream_v) {
+  if (!shape_ok(d_out, d_in, r, dtype)) {
+    if (r > DORA_MAX_RANK && d_out >= 0 && d_in >= 0) return DORA_ERR_UNSUPPORTED;
+    return DORA_ERR_INVALID_ARG;
+  }
+  const size_t nf = partials_floats(d_out, r);
+  if (nf == 0) return DORA_OK;
+  if (!partials || (reinterpret_cast<uintptr_t>(partials) & 3u) != 0) return DORA_ERR_INVALID_ARG;
+  const bool bf16 = dtype == DORA_BF16;
+  const size_t eb = bf16 ? 2 : 4;
+  const bool has_w = d_out > 0 && d_in > 0;
+  const bool has_a = r > 0 && d_in > 0;
+  if (has_w && !W) return DORA_ERR_INVALID_ARG;
+  if (has_a && !A) return DORA_ERR_INVALID_ARG;
+  if (has_w && r > 0 && !B) return DORA_ERR_INVALID_ARG;
+  const size_t pbytes = nf * 4;
+  if (has_w && overlap(partials, pbytes, W, d_out * d_in * eb)) return DORA_ERR_INVALID_ARG;
+  if (has_a && overlap(partials, pbytes, A, r * d_in * eb)) return DORA_ERR_INVALID_ARG;
+  if (has_w && r > 0 && overlap(partials, pbytes, B, d_out * r * eb)) return DORA_ERR_INVALID_ARG;
+  if (d_in > 0 && (d_in * eb) % 16 != 0) return DORA_ERR_UNSUPPORTED;
+  if (has_w && !aligned16(W)) return DORA_ERR_UNSUPPORTED;
+  if (has_a && ((r * eb) % 16 != 0 || !aligned16(A))) return DORA_ERR_UNSUPPORTED;
+  if (has_w && r > 0 && ((r * eb) % 16 != 0 || !aligned16(B))) return DORA_ERR_UNSUPPORTED;
+  const Plan plan = make_plan(d_out, d_in, r, dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < plan.total)
+    return DORA_ERR_WORKSPACE;
+
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DORA_TRY(cudaMemsetAsync(ws + plan.off_status, 0, plan.zero_bytes, stream));
+
+  if (!has_w && !has_a) {
+    // an empty slice: every partial is zero
+    return cuda_status(cudaMemsetAsync(partials, 0, pbytes, stream));
+  }
+  if (has_a) {
+    // the Gram kernel and (with rows) the main pass over the W tiles
+    if (bf16)
+      return run_bf16_pass(W, A, B, d_out, d_in, r, 0.f, nullptr, 1.f, nullptr, nullptr, plan, ws,
+                           kPassSlice, partials, nullptr, stream, nullptr, nullptr);
+    return run_f32_pass(W, A, B, d_out, d_in, r, 0.f, nullptr, 1.f, nullptr, nullptr, plan, ws,
+                        kPassSlice, partials, nullptr, stream, nullptr, nullptr);
+  }
+  // r = 0: base only, cross = 0
+  DORA_TRY(launch_row_sumsq(W, bf16, d_out, d_in, partials, stream));
+  return cuda_status(cudaMemsetAsync(partials + d_out, 0, static_cast<size_t>(d_out) * 4, stream));
+}
+
+int norm_finalize_impl(const float* partials, const void* B, int dtype, int64_t d_out, int64_t r,
+                       float s, const void* m, float eps, float* wnorm, float* g, void* workspace,
+                       size_t workspace_bytes, void* stream_v) {
+  if (!shape_ok(d_out, 0, r, dtype)) {
+    if (r > DORA_MAX_RANK && d_out >= 0) return DORA_ERR_UNSUPPORTED;
+    return DORA_ERR_INVALID_ARG;
+  }
+  if (!std::isfinite(s) || !(eps > 0.f) || !std::isfinite(eps)) return DORA_ERR_INVALID_ARG;
+  if (d_out == 0) return DORA_OK;
+  const bool bf16 = dtype == DORA_BF16;
+  const size_t eb = bf16 ? 2 : 4;
+  const bool adapter = r > 0 && s != 0.f;
+  if (!partials || !m || !wnorm || !g) return DORA_ERR_INVALID_ARG;
+  if (adapter && !B) return DORA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(partials) & 3u) != 0) return DORA_ERR_INVALID_ARG;
+  const size_t vec_bytes = static_cast<size_t>(d_out) * 4;
+  const size_t pbytes = partials_floats(d_out, r) * 4;
+  if (overlap(wnorm, vec_bytes, g, vec_bytes) || overlap(wnorm, vec_bytes, partials, pbytes) ||
+      overlap(g, vec_bytes, partials, pbytes) || overlap(wnorm, vec_bytes, m, d_out * eb) ||
+      overlap(g, vec_bytes, m, d_out * eb))
+    return DORA_ERR_INVALID_ARG;
+  if (adapter && ((r * eb) % 16 != 0 || !aligned16(B))) return DORA_ERR_UNSUPPORTED;
+  const Plan plan = make_plan(d_out, 0, r, dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < plan.total)
+    return DORA_ERR_WORKSPACE;
+
+  DeviceInfo dev;
+  const int dst = current_device_info(&dev);
+  if (dst != DORA_OK) return dst;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DORA_TRY(cudaMemsetAsync(ws + plan.off_status, 0, plan.zero_bytes, stream));
+  if (!adapter) {
+    // s = 0 or r = 0: wnorm^2 = base + 2 s cross (cross is 0 for r = 0)
+    return cuda_status(launch_finalize(d_out, partials, 1, partials + d_out, 1, nullptr, 0, s, m,
+                                       bf16, eps, wnorm, g, stream));
+  }
+  if (bf16)
+    return run_bf16_pass(nullptr, nullptr, B, d_out, 0, r, s, m, eps, wnorm, g, plan, ws,
+                         kPassFinal, nullptr, partials, stream, nullptr, nullptr);
+  return run_f32_pass(nullptr, nullptr, B, d_out, 0, r, s, m, eps, wnorm, g, plan, ws, kPassFinal,
+                      nullptr, partials, stream, nullptr, nullptr);
 }
 
 // ---------------------------------------------------------------- grouped norm
@@ -973,6 +1186,30 @@ int dora_factored_norm_noalloc(const void* W, const void* A, const void* B, int 
                             kNoAllocScratchBytes, stream, nullptr, nullptr);
 }
 
+size_t dora_norm_partials_floats(int64_t d_out, int64_t r) {
+  if (d_out < 0 || r < 0 || r > DORA_MAX_RANK || d_out >= (int64_t(1) << 31)) return 0;
+  return partials_floats(d_out, r);
+}
+
+int dora_norm_partials(const void* W, const void* A, const void* B, int dtype, int64_t d_out,
+                       int64_t d_in, int64_t r, float* partials, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return norm_partials_impl(W, A, B, dtype, d_out, d_in, r, partials, workspace, workspace_bytes,
+                            stream);
+}
+
+size_t dora_norm_finalize_workspace_size(int64_t d_out, int64_t r, int dtype) {
+  if (!shape_ok(d_out, 0, r, dtype)) return 0;
+  return make_plan(d_out, 0, r, dtype).total;
+}
+
+int dora_norm_finalize_partials(const float* partials, const void* B, int dtype, int64_t d_out,
+                                int64_t r, float s, const void* m, float eps, float* wnorm,
+                                float* g, void* workspace, size_t workspace_bytes, void* stream) {
+  return norm_finalize_impl(partials, B, dtype, d_out, r, s, m, eps, wnorm, g, workspace,
+                            workspace_bytes, stream);
+}
+
 int dora_compose(const void* base, const void* lora, const float* g, float s, int dtype,
                  int64_t T, int64_t d_out, void* out, void* stream) {
   if (T < 0 || d_out < 0 || (dtype != DORA_BF16 && dtype != DORA_F32) || !std::isfinite(s))
@@ -1332,7 +1569,7 @@ const char* dora_status_string(int status) {
   }
 }
 
-int dora_version(void) { return (1 << 16) | 1; }
+int dora_version(void) { return (1 << 16) | 2; }
 
 uint64_t dora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

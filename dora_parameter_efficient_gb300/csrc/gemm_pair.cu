@@ -390,6 +390,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         if (rank == 0 && (kGrouped || p.ranges == 0)) claimed = atomicAdd(p.work_ctr, 1);
       }
+      // Partials of a d_in slice read no G' tile, so nothing above waited for
+      // the Gram kernel this launch may overlap; hold the CTA until that grid
+      // has finished, so that this grid's completion implies the Gram's.
+      if (!kGrouped && p.sums_base && !g_ready) griddep_wait();
       // The even CTA's `full` barriers count the loads of both CTAs: once the
       // last use of every stage has completed, no copy is still in flight.
       if (rank == 0) {
@@ -678,8 +682,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (*last_flag && h == 0 && valid) {
         __threadfence();
-        // segment partials added in segment order, carried as double-floats
+        // segment partials added in segment order, carried as double-floats,
+        // after the caller's summed partials of the whole d_in range (if any)
         df base{0.f, 0.f}, cross{0.f, 0.f};
+        if (!kGrouped && p.ext_base) {
+          base.hi = p.ext_base[grow];
+          cross.hi = p.ext_cross[grow];
+        }
 #pragma unroll 1
         for (int i = 0; i < nsplit; ++i) {
           float e;
@@ -688,10 +697,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           two_sum(cross.hi, ld_cg_f(mv.out_dot + static_cast<size_t>(i) * mv.rows + grow), cross.hi, e);
           cross.lo = __fadd_rn(cross.lo, e);
         }
-        float wn, gv;
-        finalize_row(base, cross, nullptr, p.two_s, p.s_sq, bf16_to_f32(mv.m[grow]), p.eps, wn, gv);
-        mv.wnorm[grow] = wn;
-        mv.g[grow] = gv;
+        if (!kGrouped && p.sums_base) {
+          // the partials of this d_in slice, rounded once to fp32
+          p.sums_base[grow] = __fadd_rn(base.hi, base.lo);
+          p.sums_cross[grow] = __fadd_rn(cross.hi, cross.lo);
+        } else {
+          float wn, gv;
+          finalize_row(base, cross, nullptr, p.two_s, p.s_sq, bf16_to_f32(mv.m[grow]), p.eps, wn,
+                       gv);
+          mv.wnorm[grow] = wn;
+          mv.g[grow] = gv;
+        }
       }
     }
   }

@@ -21,7 +21,10 @@
 // The partial blocks never leave the cluster: no split-K buffer in global
 // memory and no second kernel.  G'_hi = bf16(G'), G'_lo = bf16(G' - G'_hi),
 // G' = (s/2) G rounded once to fp32: the two bf16 terms carry about 16
-// significant bits of G' into the tensor core.
+// significant bits of G' into the tensor core.  In partials mode (G_f32 set)
+// the kernel stores scale * G itself in fp32, [r x r] row-major, instead of
+// the split: the Gram partial of one d_in slice, which a caller adds across
+// slices.
 #include <cstring>
 
 #include "common.cuh"
@@ -292,6 +295,20 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         acc.w = __fadd_rn(acc.w, v.w);
       }
       const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+      const int gi = bi * 128 + static_cast<int>(q) * rows_per + li;
+      const int gj = bj * 128 + j;
+      if (p.G_f32) {
+        // fp32 G (scaled), staged for the mirror image in the hi/lo area
+        float* f_s = reinterpret_cast<float*>(hi_s);          // [rows_per][bw]
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float sc = __fmul_rn(p.scale, a[u]);
+          f_s[li * p.bw + j + u] = sc;
+          if (gi < p.r_out && gj + u < p.r_out)
+            p.G_f32[static_cast<size_t>(gi) * p.r_out + gj + u] = sc;
+        }
+        continue;
+      }
       uint16_t h4[4], l4[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -305,8 +322,6 @@ __global__ void __launch_bounds__(kGramThreads, 1)
                                   l4[2] | (static_cast<uint32_t>(l4[3]) << 16));
       *reinterpret_cast<uint2*>(hi_s + li * p.bw + j) = hv;
       *reinterpret_cast<uint2*>(lo_s + li * p.bw + j) = lv;
-      const int gi = bi * 128 + static_cast<int>(q) * rows_per + li;
-      const int gj = bj * 128 + j;
       // the block itself: four consecutive columns per thread (rp is a
       // multiple of 16, so a group of four is either inside or outside)
       if (gi < p.rp && gj < p.rp) {
@@ -325,7 +340,11 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         const int li = e % rows_per;
         const int gi = bi * 128 + static_cast<int>(q) * rows_per + li;
         const int gj = bj * 128 + j;
-        if (gi < p.rp && gj < p.rp) {
+        if (p.G_f32) {
+          if (gi < p.r_out && gj < p.r_out)
+            p.G_f32[static_cast<size_t>(gj) * p.r_out + gi] =
+                reinterpret_cast<const float*>(hi_s)[li * p.bw + j];
+        } else if (gi < p.rp && gj < p.rp) {
           const size_t t = static_cast<size_t>(gj) * p.rp + gi;
           p.G_hi[t] = hi_s[li * p.bw + j];
           p.G_lo[t] = lo_s[li * p.bw + j];

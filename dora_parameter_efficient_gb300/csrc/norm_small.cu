@@ -59,13 +59,21 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) out[row] = acc;
 }
 
-// sum of n fp32 partials in split order, as a double-float
+// sum of n fp32 partials in split order, as a double-float, after `first`
+// (0 when there is nothing ahead of the splits)
 __device__ __forceinline__ df sum_parts(const float* __restrict__ p, int n, int64_t stride,
-                                        int64_t j) {
+                                        int64_t j, float first = 0.f) {
   float v[kMaxFinalParts];
 #pragma unroll
   for (int i = 0; i < kMaxFinalParts; ++i) v[i] = i < n ? __ldg(p + i * stride + j) : 0.f;
-  return df_sum_in_order(v);
+  df acc{first, 0.f};
+#pragma unroll
+  for (int i = 0; i < kMaxFinalParts; ++i) {
+    float e;
+    two_sum(acc.hi, v[i], acc.hi, e);
+    acc.lo = __fadd_rn(acc.lo, e);
+  }
+  return acc;
 }
 
 // One thread per output row: the finalize step written out in finalize.cuh.
@@ -73,17 +81,55 @@ __global__ void __launch_bounds__(64)
     k_finalize(int64_t d_out, const float* __restrict__ pbase, int n_base,
                const float* __restrict__ pcross, int n_cross, const float* __restrict__ pba,
                int n_ba, float two_s, float s_sq, const void* __restrict__ m, int is_bf16,
-               float eps, float* __restrict__ wnorm, float* __restrict__ g) {
+               float eps, float* __restrict__ wnorm, float* __restrict__ g,
+               const float* __restrict__ ext_base, const float* __restrict__ ext_cross) {
   // launched as a programmatic dependent of the pass that wrote the partials
+  griddep_wait();
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j >= d_out) return;
+  // partials of the whole d_in range summed by the caller come first
+  const df base = sum_parts(pbase, n_base, d_out, j, ext_base ? ext_base[j] : 0.f);
+  const df cross = sum_parts(pcross, n_cross, d_out, j, ext_cross ? ext_cross[j] : 0.f);
+  const df ba = n_ba > 0 ? sum_parts(pba, n_ba, d_out, j) : df{0.f, 0.f};
+  const float mj = is_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(m)[j])
+                           : static_cast<const float*>(m)[j];
+  finalize_row(base, cross, n_ba > 0 ? &ba : nullptr, two_s, s_sq, mj, eps, wnorm[j], g[j]);
+}
+
+// One thread per row: the split partials of base and cross summed in split
+// order (double-float) and rounded once to fp32 -- the partials of one d_in
+// slice that a caller adds across slices.
+__global__ void __launch_bounds__(64)
+    k_sum_partials(int64_t d_out, const float* __restrict__ pbase, int n_base,
+                   const float* __restrict__ pcross, int n_cross, float* __restrict__ sum_base,
+                   float* __restrict__ sum_cross) {
   griddep_wait();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (j >= d_out) return;
   const df base = sum_parts(pbase, n_base, d_out, j);
   const df cross = sum_parts(pcross, n_cross, d_out, j);
-  const df ba = n_ba > 0 ? sum_parts(pba, n_ba, d_out, j) : df{0.f, 0.f};
-  const float mj = is_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(m)[j])
-                           : static_cast<const float*>(m)[j];
-  finalize_row(base, cross, n_ba > 0 ? &ba : nullptr, two_s, s_sq, mj, eps, wnorm[j], g[j]);
+  sum_base[j] = __fadd_rn(base.hi, base.lo);
+  sum_cross[j] = __fadd_rn(cross.hi, cross.lo);
+}
+
+// G' = scale * G for a fp32 G [r x r], split into bf16 G'_hi = bf16(G'),
+// G'_lo = bf16(G' - G'_hi), [rp x rp] with zeros outside [r x r] -- the two
+// terms the bf16 main pass folds into its K loop.
+__global__ void __launch_bounds__(256)
+    k_gram_split(const float* __restrict__ G, int r, int rp, float scale,
+                 uint16_t* __restrict__ G_hi, uint16_t* __restrict__ G_lo) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(rp) * rp) return;
+  const int i = static_cast<int>(idx / rp);
+  const int j = static_cast<int>(idx - static_cast<int64_t>(i) * rp);
+  uint16_t h = 0, l = 0;
+  if (i < r && j < r) {
+    const float v = __fmul_rn(scale, G[static_cast<int64_t>(i) * r + j]);
+    h = f32_to_bf16_rn(v);
+    l = f32_to_bf16_rn(__fsub_rn(v, bf16_to_f32(h)));
+  }
+  G_hi[idx] = h;
+  G_lo[idx] = l;
 }
 
 // One thread waits, with the pipelines' bounded wait, on an mbarrier that
@@ -120,7 +166,8 @@ cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t c
 cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const float* pcross,
                             int n_cross, const float* pba, int n_ba, float s, const void* m,
                             int is_bf16, float eps, float* wnorm, float* g,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const float* ext_base,
+                            const float* ext_cross) {
   if (n_base > kMaxFinalParts || n_cross > kMaxFinalParts || n_ba > kMaxFinalParts)
     return cudaErrorInvalidValue;
   const unsigned blocks = static_cast<unsigned>((d_out + 63) / 64);
@@ -139,9 +186,38 @@ cudaError_t launch_finalize(int64_t d_out, const float* pbase, int n_base, const
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k_finalize, d_out, pbase, n_base, pcross,
                                            n_cross, pba, n_ba, 2.f * s, s * s, m, is_bf16, eps,
-                                           wnorm, g);
+                                           wnorm, g, ext_base, ext_cross);
   note_launches(1);
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_partials(int64_t d_out, const float* pbase, int n_base,
+                                const float* pcross, int n_cross, float* sum_base,
+                                float* sum_cross, cudaStream_t stream) {
+  if (n_base > kMaxFinalParts || n_cross > kMaxFinalParts) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((d_out + 63) / 64), 1, 1);
+  cfg.blockDim = dim3(64, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_sum_partials, d_out, pbase, n_base, pcross,
+                                           n_cross, sum_base, sum_cross);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gram_split(const float* G, int r, int rp, float scale, uint16_t* G_hi,
+                              uint16_t* G_lo, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(rp) * rp;
+  k_gram_split<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(G, r, rp, scale, G_hi,
+                                                                           G_lo);
+  note_launches(1);
   return cudaGetLastError();
 }
 

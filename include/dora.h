@@ -163,6 +163,69 @@ int dora_factored_norm_noalloc(const void* W, const void* A, const void* B, int 
                                void* stream);
 
 /*
+ * The norm with d_in sharded across devices (row-parallel tensor
+ * parallelism: each device holds the columns [k0, k1) of W and of A, and all
+ * of B and m).  Every term of the factored norm is a sum over d_in: the base
+ * term ||W_j||^2, the cross term rowsum(B o U) with U = W A^T, and the Gram
+ * matrix G = A A^T that the BA-norm term rowsum((B G) o B) is built from
+ * (Chinese write-up, section 1.2.1 and Algorithm 1 of section 5.1, steps 4a-f
+ * and 6).  So each device computes the three for its slice, the devices add
+ * them with one all-reduce (sum) of 2 d_out + r^2 floats, and each device
+ * then finishes the norm from the sums.  The write-ups mention DoRA training
+ * beside tensor-parallel inference (section 4.1) but give no sharded norm;
+ * this split of the work is a reading of section 1.2.1's algebra.
+ *
+ * Partials layout (float32, contiguous, 2 * d_out + r * r values):
+ *   [0, d_out)                 base_j  = sum_k W_jk^2                over the slice
+ *   [d_out, 2 d_out)           cross_j = sum_l B_jl (W A^T)_jl      over the slice
+ *   [2 d_out, 2 d_out + r^2)   G       = A A^T, [r x r] row-major    over the slice
+ * The partials do not depend on s, eps or m.
+ */
+
+/* Floats of the partials buffer: 2 * d_out + r * r (0 for an invalid shape). */
+size_t dora_norm_partials_floats(int64_t d_out, int64_t r);
+
+/*
+ * The partials of one d_in slice.
+ *   W  [d_out x d_in]  this slice's columns of the frozen weight, dtype
+ *   A  [r x d_in]      this slice's columns of the down projection, dtype
+ *   B  [d_out x r]     the whole up projection, dtype
+ *   partials  [2 d_out + r^2] float32 output (4-byte aligned; must not
+ *          overlap an input)
+ *   workspace / workspace_bytes  at least dora_norm_workspace_size(d_out,
+ *          d_in, r, dtype) bytes, 256-byte aligned, no initialisation needed
+ * Requirements and errors as dora_factored_norm (d_in here is the slice
+ * width).  An empty slice (d_in = 0) writes zeros; r = 0 writes base and a
+ * zero cross; d_out = 0 writes G only.  Precision: as dora_factored_norm --
+ * fp32 sums of exact bf16 products, or 3xTF32 products for fp32 inputs --
+ * with each sum rounded once to fp32 when it is stored.
+ */
+int dora_norm_partials(const void* W, const void* A, const void* B, int dtype,
+                       int64_t d_out, int64_t d_in, int64_t r, float* partials,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace dora_norm_finalize_partials needs (0 for an invalid shape). */
+size_t dora_norm_finalize_workspace_size(int64_t d_out, int64_t r, int dtype);
+
+/*
+ * wnorm and g from partials summed over every slice of d_in (after the
+ * caller's all-reduce):
+ *   wnorm_j = sqrt(max(base_j + 2 s cross_j + s^2 rowsum((B G) o B)_j, 0)),
+ *   g_j = m_j / max(wnorm_j, eps)
+ * with the BA-norm term taken on the tensor cores from the summed G (bf16
+ * inputs: G' = (s/2) G split into two bf16 terms, as dora_factored_norm
+ * does).  partials: [2 d_out + r^2] float32 in the layout above; B [d_out x r],
+ * m [d_out] in dtype; wnorm, g [d_out] float32 outputs; workspace of
+ * dora_norm_finalize_workspace_size bytes, 256-byte aligned.  s == 0 or
+ * r == 0 skips the BA-norm term and B is not read.  Errors as
+ * dora_factored_norm.
+ */
+int dora_norm_finalize_partials(const float* partials, const void* B, int dtype,
+                                int64_t d_out, int64_t r, float s, const void* m, float eps,
+                                float* wnorm, float* g, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * Stable fused compose.
  *
  *   base, lora  [T x d_out]  dtype (base = the frozen layer's output, lora =
@@ -390,7 +453,8 @@ uint64_t dora_launch_count(void);
 const char* dora_status_string(int status);
 
 /* Library ABI version: (major << 16) | minor.  1.1 added the two schedule
- * self-tests; nothing was removed or changed. */
+ * self-tests, 1.2 the d_in-sharded norm (partials and finalize); nothing was
+ * removed or changed. */
 int dora_version(void);
 
 #ifdef __cplusplus

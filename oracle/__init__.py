@@ -7,5 +7,6 @@ from .dora_oracle import (  # noqa: F401
     BF16, F32, compose, compose_backward, compose_backward_stored, compose_inner,
     compose_inner_stored, compose_stored, decode, dense_ba_bytes, factored_intermediate_bytes,
     magnitude_grad, magnitude_grad_stored, magnitude_scale, naive_compose_f32, norm_and_scale,
+    norm_from_partials, norm_partials,
     round_to, round_to_bf16_bits, row_norm,
 )

@@ -27,6 +27,10 @@ Adaptation via Factored Norms and Fused Kernels" (Zelenin, Zhuravlyova):
 * rounding of a float64 result to the stored dtype: IEEE 754
   roundTiesToEven, done once, directly from float64.
 
+The d_in-sharded form of the norm (each term of the factored norm is a sum
+over d_in, so devices holding column slices add their shares; section 1.2.1)
+is given by ``norm_partials`` and ``norm_from_partials``.
+
 Each function names the passage it follows.  No function here is "parity
 unpinned": ``tests/test_oracle_pins.py`` checks every one against exact
 rational arithmetic, closed forms or hand-worked fixtures.
@@ -119,6 +123,41 @@ def norm_and_scale(W, A, B, m, s: float, eps: float, dtype: str
     module's rows: every row is independent."""
     wnorm = row_norm(decode(W, dtype), decode(A, dtype), decode(B, dtype), s)
     return wnorm, magnitude_scale(decode(m, dtype), wnorm, eps)
+
+
+# ---------------------------------------------------------------- d_in-sharded norm
+# Every term of the factored norm is a sum over the d_in columns (Chinese
+# write-up section 1.2.1; Algorithm 1 of section 5.1, steps 4a-f accumulate
+# them chunk by chunk over d_in): ||W_j||^2, rowsum(B o U)_j with U = W A^T,
+# and G = A A^T.  A device holding only the columns [k0, k1) of W and A can
+# form its share of each; the shares add up to the whole.  These functions
+# state the three sums by their definitions and apply the identity of
+# section 1.2.1 to summed shares; tests/test_oracle_pins.py pins them to the
+# dense norm above with exact rational arithmetic.
+def norm_partials(W: np.ndarray, A: np.ndarray, B: np.ndarray):
+    """(base, cross, G) of the columns of W [d_out x k] and A [r x k], float64:
+    base_j = sum_k W_jk^2;  cross_j = sum_l B_jl * sum_k W_jk A_lk;
+    G_lm = sum_k A_lk A_mk."""
+    W = np.asarray(W, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    base = np.sum(W * W, axis=1)
+    U = W @ A.T
+    cross = np.sum(B * U, axis=1)
+    G = A @ A.T
+    return base, cross, G
+
+
+def norm_from_partials(base: np.ndarray, cross: np.ndarray, G: np.ndarray, B: np.ndarray,
+                       s: float) -> np.ndarray:
+    """wnorm_j = sqrt(max(base_j + 2 s cross_j + s^2 B_j G B_j^T, 0)) from shares
+    summed over all of d_in (section 1.2.1's three terms; the clamp of section
+    1.2.2), float64."""
+    B = np.asarray(B, dtype=np.float64)
+    ba = np.sum((B @ np.asarray(G, dtype=np.float64)) * B, axis=1)
+    w2 = np.asarray(base, np.float64) + 2.0 * float(s) * np.asarray(cross, np.float64) \
+        + float(s) * float(s) * ba
+    return np.sqrt(np.maximum(w2, 0.0))
 
 
 # ---------------------------------------------------------------- the compose

@@ -199,3 +199,71 @@ def test_selftest_timeout_rejects_before_the_gpu(lib):
     assert lib.dora_selftest_timeout(8 * P, 128, 1000, None) == _lib.DORA_ERR_WORKSPACE
     assert lib.dora_selftest_timeout(8 * P, 1 << 20, 0, None) == _lib.DORA_ERR_INVALID_ARG
     assert lib.dora_selftest_timeout(8 * P, 1 << 20, 2_000_000, None) == _lib.DORA_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- d_in-sharded norm
+def _partials(lib, **kw):
+    a = dict(W=P, A=2 * P, B=3 * P, dtype=_lib.DORA_BF16, d_out=256, d_in=512, r=64,
+             partials=4 * P, ws=8 * P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.dora_norm_partials(a["W"], a["A"], a["B"], a["dtype"], a["d_out"], a["d_in"],
+                                  a["r"], a["partials"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=5), _lib.DORA_ERR_INVALID_ARG),
+    (dict(d_out=-1), _lib.DORA_ERR_INVALID_ARG),
+    (dict(r=513), _lib.DORA_ERR_UNSUPPORTED),
+    (dict(partials=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(partials=4 * P + 2), _lib.DORA_ERR_INVALID_ARG),   # not 4-byte aligned
+    (dict(partials=P + 64), _lib.DORA_ERR_INVALID_ARG),      # inside W
+    (dict(W=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(A=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(B=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(d_in=100), _lib.DORA_ERR_UNSUPPORTED),             # 200-byte rows
+    (dict(r=60), _lib.DORA_ERR_UNSUPPORTED),
+    (dict(A=2 * P + 8), _lib.DORA_ERR_UNSUPPORTED),          # misaligned
+    (dict(ws=None), _lib.DORA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), _lib.DORA_ERR_WORKSPACE),
+    (dict(d_out=0, r=0), _lib.DORA_OK),                      # no partials at all
+])
+def test_partials_argument_checks(lib, kw, status):
+    assert _partials(lib, **kw) == status
+
+
+def _finalize(lib, **kw):
+    a = dict(partials=4 * P, B=3 * P, dtype=_lib.DORA_BF16, d_out=256, r=64, s=1.0, m=5 * P,
+             eps=1e-6, wnorm=6 * P, g=7 * P, ws=8 * P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.dora_norm_finalize_partials(a["partials"], a["B"], a["dtype"], a["d_out"], a["r"],
+                                           a["s"], a["m"], a["eps"], a["wnorm"], a["g"], a["ws"],
+                                           a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=5), _lib.DORA_ERR_INVALID_ARG),
+    (dict(r=513), _lib.DORA_ERR_UNSUPPORTED),
+    (dict(eps=0.0), _lib.DORA_ERR_INVALID_ARG),
+    (dict(s=float("nan")), _lib.DORA_ERR_INVALID_ARG),
+    (dict(partials=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(B=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(m=None), _lib.DORA_ERR_INVALID_ARG),
+    (dict(g=6 * P), _lib.DORA_ERR_INVALID_ARG),              # wnorm == g
+    (dict(wnorm=4 * P + 512), _lib.DORA_ERR_INVALID_ARG),    # output inside the partials
+    (dict(r=60), _lib.DORA_ERR_UNSUPPORTED),                 # 120-byte B rows
+    (dict(ws=None), _lib.DORA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), _lib.DORA_ERR_WORKSPACE),
+    (dict(d_out=0), _lib.DORA_OK),
+])
+def test_finalize_partials_argument_checks(lib, kw, status):
+    assert _finalize(lib, **kw) == status
+
+
+def test_partials_sizes(lib):
+    assert lib.dora_norm_partials_floats(8192, 384) == 2 * 8192 + 384 * 384
+    assert lib.dora_norm_partials_floats(-1, 8) == 0
+    assert lib.dora_norm_partials_floats(8, 513) == 0
+    n = lib.dora_norm_finalize_workspace_size(8192, 384, _lib.DORA_BF16)
+    assert n == lib.dora_norm_workspace_size(8192, 64, 384, _lib.DORA_BF16)
+    assert lib.dora_norm_finalize_workspace_size(8, 513, _lib.DORA_BF16) == 0
+    assert lib.dora_version() & 0xFFFF >= 2      # the d_in-sharded norm

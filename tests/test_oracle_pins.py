@@ -429,3 +429,89 @@ def test_memory_figures_from_the_pages(golden_dir):
         elif kind == "gram_max_mb":
             r, want = int(row[1]), float(row[2])
             assert oracle.factored_intermediate_bytes(0, r, 4) / MB <= want
+
+
+# ------------------------------------------------------------ d_in-sharded norm
+def _exact_partials(W, A, B):
+    """base, cross, G by their definitions, in exact rationals."""
+    d_out, d_in = W.shape
+    r = A.shape[0]
+    base = [sum(Fraction(W[j, k]) ** 2 for k in range(d_in)) for j in range(d_out)]
+    cross = [sum(Fraction(B[j, l]) * sum(Fraction(W[j, k]) * Fraction(A[l, k]) for k in range(d_in))
+                 for l in range(r)) for j in range(d_out)]
+    G = [[sum(Fraction(A[a, k]) * Fraction(A[b, k]) for k in range(d_in)) for b in range(r)]
+         for a in range(r)]
+    return base, cross, G
+
+
+@pytest.mark.parametrize("cuts", [(), (5,), (0, 3), (2, 2, 7), (1, 4, 9)])
+def test_partials_are_the_definitions_and_add_up_exactly(cuts):
+    """Small integers: every float64 step is exact, so the shares of each
+    column slice equal the rational definitions, the shares of the slices
+    (empty ones included) add up to the whole module's, and the identity of
+    section 1.2.1 applied to the summed shares gives exactly the dense norm."""
+    rng = np.random.default_rng(len(cuts) + 17)
+    d_out, d_in, r, s = 5, 10, 3, 2.0
+    W = rng.integers(-3, 4, (d_out, d_in)).astype(np.float64)
+    A = rng.integers(-3, 4, (r, d_in)).astype(np.float64)
+    B = rng.integers(-3, 4, (d_out, r)).astype(np.float64)
+    bounds = [0, *cuts, d_in]
+    tot_b = np.zeros(d_out)
+    tot_c = np.zeros(d_out)
+    tot_g = np.zeros((r, r))
+    for k0, k1 in zip(bounds[:-1], bounds[1:]):
+        b, c, g = oracle.norm_partials(W[:, k0:k1], A[:, k0:k1], B)
+        eb, ec, eg = _exact_partials(W[:, k0:k1], A[:, k0:k1], B)
+        assert [Fraction(x) for x in b] == eb
+        assert [Fraction(x) for x in c] == ec
+        assert [[Fraction(x) for x in row] for row in g] == eg
+        tot_b += b
+        tot_c += c
+        tot_g += g
+    whole = oracle.norm_partials(W, A, B)
+    np.testing.assert_array_equal(tot_b, whole[0])
+    np.testing.assert_array_equal(tot_c, whole[1])
+    np.testing.assert_array_equal(tot_g, whole[2])
+    wn = oracle.norm_from_partials(tot_b, tot_c, tot_g, B, s)
+    exact_sq = _exact_dense_sq(W, A, B, s)
+    np.testing.assert_array_equal(wn, np.sqrt(np.array([float(x) for x in exact_sq])))
+
+
+def test_partials_norm_matches_dense_on_random_slices():
+    """Real-valued inputs split into four slices of unequal width: the norm from
+    the summed shares equals the dense definition to float64 rounding."""
+    rng = np.random.default_rng(5)
+    d_out, d_in, r, s = 40, 300, 12, -0.75
+    W = 0.02 * rng.standard_normal((d_out, d_in))
+    A = rng.standard_normal((r, d_in)) / np.sqrt(d_in)
+    B = 0.01 * rng.standard_normal((d_out, r))
+    parts = [oracle.norm_partials(W[:, a:b], A[:, a:b], B)
+             for a, b in ((0, 64), (64, 64), (64, 200), (200, 300))]
+    base = sum(p[0] for p in parts)
+    cross = sum(p[1] for p in parts)
+    G = sum(p[2] for p in parts)
+    wn = oracle.norm_from_partials(base, cross, G, B, s)
+    ref = oracle.row_norm(W, A, B, s)
+    assert np.max(np.abs(wn - ref) / ref) < 1e-13
+
+
+def test_partials_pins_catch_planted_mistakes():
+    """Mistakes planted in copies of norm_from_partials (on the CPU) break the
+    exact identity: 2s dropped to s, s^2 to s, the clamp removed on a
+    cancelling row."""
+    W = np.array([[2.0, -1.0, 0.0], [1.0, 1.0, 1.0]])
+    A = np.array([[1.0, 0.0, 1.0]])
+    B = np.array([[1.0], [-1.0]])
+    s = 2.0
+    base, cross, G = oracle.norm_partials(W, A, B)
+    exact = np.sqrt(np.array([float(x) for x in _exact_dense_sq(W, A, B, s)]))
+    np.testing.assert_array_equal(oracle.norm_from_partials(base, cross, G, B, s), exact)
+    ba = np.sum((B @ G) * B, axis=1)
+    for wrong in (base + s * cross + s * s * ba, base + 2 * s * cross + s * ba,
+                  base + 2 * s * cross):
+        assert not np.array_equal(np.sqrt(np.maximum(wrong, 0)), exact)
+    # a row with W = -s B A cancels to exactly zero; without the clamp a
+    # negative rounding residue would give NaN, with it the norm is 0
+    Wc = -s * (B @ A)
+    bc, cc, gc = oracle.norm_partials(Wc, A, B)
+    assert np.all(oracle.norm_from_partials(bc, cc, gc, B, s) == 0.0)
