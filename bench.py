@@ -14,6 +14,7 @@ Printed (rank 0, one JSON line):
   compose    compose GB/s over the compose part of the same steps
   back_to_back  the norm alone, the compose alone and the whole step in loops
              with one event pair around each loop (no events between launches)
+  cuda_graph the same three loops captured as CUDA graphs and replayed
   roofline   the dominant kernel (the U = W A^T main pass) against the measured
              burst bf16 peak; roofline_compose the compose kernel against HBM copy BW
   e2e        the same metrics through the public API from pinned host buffers,
@@ -600,6 +601,32 @@ def run_ours(args):
     b2b_n = max(3, min(args.steps, 2000))
     b2b = {"norm_ms": loop_ms(norm_only, b2b_n), "compose_ms": loop_ms(comp_only, b2b_n),
            "step_ms": loop_ms(step, b2b_n), "calls_per_loop": b2b_n}
+
+    # ---- the same three loops captured once as CUDA graphs of 30 calls (ten
+    # rounds of the rotating sets) and replayed: the launch chain without the
+    # host's per-call enqueue work
+    def graph_ms(fn, calls=30, replays=max(3, min(args.steps // 30, 100))):
+        gr = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gr):
+            for i in range(calls):
+                fn(i)
+        for _ in range(3):
+            gr.replay()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(replays):
+            gr.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / (replays * calls)
+        del gr
+        return ms
+
+    graphs = {"norm_ms": graph_ms(norm_only), "compose_ms": graph_ms(comp_only),
+              "step_ms": graph_ms(step), "calls_per_graph": 30}
     sampler.stop()
     clocks = sampler.summary()
 
@@ -821,6 +848,15 @@ def run_ours(args):
                 "compose_frac_of_nominal_hbm": cbytes / (b2b["compose_ms"] * 1e-3) / 1e9 / NOMINAL["hbm_gbs"],
                 "timing": "one CUDA event pair around a loop of calls over the rotating sets "
                           "(no event between launches); per call = loop time / calls"},
+            "cuda_graph": {
+                **graphs,
+                "norm_tflops": nflops / (graphs["norm_ms"] * 1e-3) / 1e12,
+                "norm_frac_of_measured_bf16": nflops / (graphs["norm_ms"] * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                "compose_GB/s": cbytes / (graphs["compose_ms"] * 1e-3) / 1e9,
+                "compose_frac_of_measured_hbm": cbytes / (graphs["compose_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "compose_frac_of_nominal_hbm": cbytes / (graphs["compose_ms"] * 1e-3) / 1e9 / NOMINAL["hbm_gbs"],
+                "timing": "each loop captured once as a CUDA graph of 30 calls over the rotating "
+                          "sets, one event pair around the replays; per call = time / calls"},
             "compose": {"value": comp_gbs, "unit": "GB/s", "ms": comp_ms_m,
                         "elements_per_s": T * d_out * world / (comp_ms_m * 1e-3),
                         "frac_of_measured_hbm": comp_gbs / world / peaks["hbm_gbs"],

@@ -271,6 +271,9 @@ cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int r
                                     float* Gp, cudaStream_t stream);
 
 // ------------------------------------------------------------------ small kernels
+// zeroes n ints at p (a norm workspace's control block); the next kernel may
+// be launched as its programmatic dependent
+cudaError_t launch_zero_words(int* p, int n, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(int* status, unsigned long long timeout_ns,
                                     cudaStream_t stream);
 cudaError_t launch_row_sumsq(const void* X, int is_bf16, int64_t rows, int64_t cols,

@@ -20,6 +20,7 @@
 // take a grid-stride loop, and anything unaligned the element-wise loop.
 // Grids are sized to a multiple of the SM count.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dora {
 
@@ -61,6 +62,9 @@ __global__ void __launch_bounds__(kColThreads, 4)
     k_compose_cols(const uint4* __restrict__ base, const uint4* __restrict__ lora,
                    const float* __restrict__ g, float s, int64_t T, int64_t dv,
                    uint4* __restrict__ out) {
+  // launched as a programmatic dependent of whatever precedes it: the blocks
+  // may be resident before that grid ends, but read nothing until it has
+  griddep_wait();
   constexpr int EPV = BF16 ? 8 : 4;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * kColThreads + threadIdx.x;
   float gv[EPV], gm[EPV];
@@ -111,6 +115,8 @@ __global__ void __launch_bounds__(kColThreads, 4)
       __stcs(out + r * dv + c, o);
     }
   }
+  // the next kernel of the stream may launch (it waits for this grid)
+  griddep_launch_dependents();
 }
 
 template <bool BF16>
@@ -118,6 +124,7 @@ __global__ void __launch_bounds__(256)
     k_compose(const void* __restrict__ base, const void* __restrict__ lora,
               const float* __restrict__ g, float s, int64_t T, int64_t d_out,
               void* __restrict__ out, int vec_ok) {
+  griddep_wait();
   const int64_t n = T * d_out;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -184,6 +191,7 @@ __global__ void __launch_bounds__(256)
       }
     }
   }
+  griddep_launch_dependents();
 }
 
 // Grouped compose over a module table: unit u = (module, 16-row block,
@@ -277,6 +285,31 @@ cudaError_t launch_compose_grouped(const ComposeModule* mods, int n_mods, int64_
   return cudaGetLastError();
 }
 
+namespace {
+
+// Launch as a programmatic dependent of the previous work in the stream: the
+// grid is set up while that work finishes; the kernels wait (griddep_wait)
+// before their first read.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_compose(const void* base, const void* lora, const float* g, float s,
                            int is_bf16, int64_t T, int64_t d_out, void* out, int num_sms,
                            cudaStream_t stream) {
@@ -296,30 +329,24 @@ cudaError_t launch_compose(const void* base, const void* lora, const float* g, f
     if (yblocks > 65535) yblocks = 65535;
     if (yblocks < 1) yblocks = 1;
     const dim3 grid(static_cast<unsigned>(xblocks), static_cast<unsigned>(yblocks));
-    if (is_bf16)
-      k_compose_cols<true><<<grid, kColThreads, 0, stream>>>(
-          static_cast<const uint4*>(base), static_cast<const uint4*>(lora), g, s, T, dv,
-          static_cast<uint4*>(out));
-    else
-      k_compose_cols<false><<<grid, kColThreads, 0, stream>>>(
-          static_cast<const uint4*>(base), static_cast<const uint4*>(lora), g, s, T, dv,
-          static_cast<uint4*>(out));
-    note_launches(1);
-    return cudaGetLastError();
+    const uint4* b4 = static_cast<const uint4*>(base);
+    const uint4* l4 = static_cast<const uint4*>(lora);
+    uint4* o4 = static_cast<uint4*>(out);
+    return is_bf16 ? launch_dependent(k_compose_cols<true>, grid, dim3(kColThreads), stream, b4,
+                                      l4, g, s, T, dv, o4)
+                   : launch_dependent(k_compose_cols<false>, grid, dim3(kColThreads), stream, b4,
+                                      l4, g, s, T, dv, o4);
   }
   const int64_t work = vec_ok ? (n / epv + kUnroll - 1) / kUnroll : n;
   int64_t blocks = (work + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (is_bf16)
-    k_compose<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(base, lora, g, s, T, d_out,
-                                                                       out, vec_ok);
-  else
-    k_compose<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(base, lora, g, s, T,
-                                                                        d_out, out, vec_ok);
-  note_launches(1);
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(blocks));
+  return is_bf16 ? launch_dependent(k_compose<true>, grid, dim3(256), stream, base, lora, g, s, T,
+                                    d_out, out, static_cast<int>(vec_ok))
+                 : launch_dependent(k_compose<false>, grid, dim3(256), stream, base, lora, g, s,
+                                    T, d_out, out, static_cast<int>(vec_ok));
 }
 
 }  // namespace dora

@@ -624,7 +624,7 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
 
-  DORA_TRY(cudaMemsetAsync(status, 0, plan.zero_bytes, stream));
+  DORA_TRY(launch_zero_words(status, static_cast<int>(plan.zero_bytes / 4), stream));
 
   int n_base = 0;
   if (d_in == 0) {
@@ -688,7 +688,8 @@ int norm_partials_impl(const void* W, const void* A, const void* B, int dtype, i
   if (dst != DORA_OK) return dst;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DORA_TRY(cudaMemsetAsync(ws + plan.off_status, 0, plan.zero_bytes, stream));
+  DORA_TRY(launch_zero_words(reinterpret_cast<int*>(ws + plan.off_status),
+                             static_cast<int>(plan.zero_bytes / 4), stream));
 
   if (!has_w && !has_a) {
     // an empty slice: every partial is zero
@@ -739,7 +740,8 @@ int norm_finalize_impl(const float* partials, const void* B, int dtype, int64_t 
   if (dst != DORA_OK) return dst;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DORA_TRY(cudaMemsetAsync(ws + plan.off_status, 0, plan.zero_bytes, stream));
+  DORA_TRY(launch_zero_words(reinterpret_cast<int*>(ws + plan.off_status),
+                             static_cast<int>(plan.zero_bytes / 4), stream));
   if (!adapter) {
     // s = 0 or r = 0: wnorm^2 = base + 2 s cross (cross is 0 for r = 0)
     return cuda_status(launch_finalize(d_out, partials, 1, partials + d_out, 1, nullptr, 0, s, m,
@@ -1060,7 +1062,7 @@ int grouped_run(const NormGroupedPlan& P, float s, float eps, cudaStream_t strea
   const int kt_b = static_cast<int>(ceil_div(r, kTcBlockK));
   const PairModule* pm_dev = reinterpret_cast<const PairModule*>(P.ws + gp.off_pmods);
   const GramModule* gm_dev = reinterpret_cast<const GramModule*>(P.ws + gp.off_gmods);
-  DORA_TRY(cudaMemsetAsync(status, 0, gp.zero_bytes, stream));
+  DORA_TRY(launch_zero_words(status, static_cast<int>(gp.zero_bytes / 4), stream));
 
   GramParams pg{};
   pg.nb = gnb;

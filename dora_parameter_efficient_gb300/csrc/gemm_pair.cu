@@ -390,10 +390,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         if (rank == 0 && (kGrouped || p.ranges == 0)) claimed = atomicAdd(p.work_ctr, 1);
       }
-      // Partials of a d_in slice read no G' tile, so nothing above waited for
-      // the Gram kernel this launch may overlap; hold the CTA until that grid
-      // has finished, so that this grid's completion implies the Gram's.
-      if (!kGrouped && p.sums_base && !g_ready) griddep_wait();
+      // A CTA that loaded no G' tile (every CTA for the partials of a d_in
+      // slice) never waited for the Gram kernel this launch may overlap:
+      // wait before exiting, so that this grid's completion covers the Gram's.
+      if (!g_ready) griddep_wait();
       // The even CTA's `full` barriers count the loads of both CTAs: once the
       // last use of every stage has completed, no copy is still in flight.
       if (rank == 0) {
@@ -715,6 +715,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __syncwarp();              // whole warps at the aligned barriers below (roles ran on single lanes)
   tc_fence_before_sync();
   __syncthreads();
+  // (No early trigger for the next kernel here: on one GB300 a compose
+  // launched as this grid's dependent from this point ran the norm + compose
+  // step 6 us slower than one launched when this grid completes.)
   cluster_sync();            // the peer may still read this CTA's shared memory until here
   if (warp == 1) {
     __syncwarp();

@@ -229,6 +229,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
           }
         }
       }
+      // A CTA that loaded no G' tile never waited for the kernels this one
+      // may overlap: wait before exiting, so that this grid's completion
+      // covers theirs (for the Gram itself, a plain launch, a no-op).
+      if (!g_ready) griddep_wait();
       // no copy may still be in flight when the CTA exits
       const uint64_t drain_deadline = global_timer_ns() + p.timeout_ns;
       const uint32_t first = it > nraw ? it - nraw : 0;
@@ -439,6 +443,9 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   __syncwarp();              // whole warps at the aligned barriers below (roles ran on single lanes)
   tc_fence_before_sync();
   __syncthreads();
+  // this CTA's work is done: the next kernel of the stream (a programmatic
+  // dependent that waits for this grid before it reads) may start
+  griddep_launch_dependents();
   cluster_sync();            // the peer may still read this CTA's shared memory until here
   if (warp == 1) {
     __syncwarp();
@@ -450,6 +457,11 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 // G' = scale * (sum of the K-segment partials in segment order), zero padded
 __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, int r, int rp,
                                    float scale, float* __restrict__ Gp) {
+  // a programmatic dependent of the Gram pass: the norm pass behind it may
+  // launch now (it waits for this grid before its first G' tile); the sums
+  // start once the Gram's partials are complete
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<int64_t>(rp) * rp) return;
   const int i = static_cast<int>(idx / rp);
@@ -551,9 +563,18 @@ cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const
 cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int rp, float scale,
                                     float* Gp, cudaStream_t stream) {
   const int64_t n = static_cast<int64_t>(rp) * rp;
-  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-  k_gram_tf32_reduce<<<blocks, 256, 0, stream>>>(parts, splits, r, rp, scale, Gp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce, parts, splits, r, rp, scale, Gp);
   note_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

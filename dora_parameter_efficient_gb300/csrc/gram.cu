@@ -84,8 +84,12 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   }
   const CUtensorMap& tAx = *tAxp;
   const CUtensorMap& tAy = *tAyp;
-  // the main pass queued behind this kernel may start launching; it waits
-  // for this grid to finish before it reads G'
+  // launched as a programmatic dependent of the kernel that zeroes the
+  // workspace's control words (or of whatever precedes it in the stream):
+  // nothing is read or written before that grid has finished.  Then the main
+  // pass queued behind this kernel may start launching; it waits for this
+  // grid to finish before it reads G'.
+  griddep_wait();
   griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -400,13 +404,15 @@ cudaError_t gram_launch(const CUtensorMap& tAx, const CUtensorMap& tAy, const Gr
   cfg.blockDim = dim3(kGramThreads, 1, 1);
   cfg.dynamicSmemBytes = gram_smem_bytes(p.bw, p.stages);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k_gram<kGrouped>, tAx, tAy, p, mods);
   note_launches(1);
   if (e != cudaSuccess) return e;

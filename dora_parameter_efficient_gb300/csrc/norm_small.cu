@@ -132,6 +132,24 @@ __global__ void __launch_bounds__(256)
   G_lo[idx] = l;
 }
 
+// Zeroes the control words at the head of a norm workspace (the status word,
+// the main pass's work counter and its completion counters).  It lets the
+// next kernel of the norm -- launched as its programmatic dependent -- start
+// at once; that kernel waits for this one (griddep_wait) before anything that
+// depends on the zeros.  A kernel, not cudaMemsetAsync: on one GB300 the
+// memset took about 3 us more per norm inside a CUDA graph and broke the
+// programmatic chain in a stream.
+__global__ void __launch_bounds__(256) k_zero_words(int* __restrict__ p, int n) {
+  // itself a programmatic dependent of the previous work in the stream, which
+  // may still use this workspace (the previous norm on it): zero afterwards
+  griddep_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
+  // only now may the Gram kernel's CTAs (most of an SM's shared memory
+  // each) become resident: launched earlier they sit on SMs that the
+  // previous kernel -- often a compose of one wave -- still needs
+  griddep_launch_dependents();
+}
+
 // One thread waits, with the pipelines' bounded wait, on an mbarrier that
 // nothing arrives on; when the limit passes it records the timeout in the
 // status word, as a pipeline role does, and the kernel returns.
@@ -145,6 +163,23 @@ __global__ void k_selftest_timeout(int* status, unsigned long long timeout_ns) {
 }
 
 }  // namespace
+
+cudaError_t launch_zero_words(int* p, int n, cudaStream_t stream) {
+  const int blocks = n <= 2048 ? 1 : (n + 2047) / 2048 < 64 ? (n + 2047) / 2048 : 64;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_zero_words, p, n);
+  note_launches(1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_selftest_timeout(int* status, unsigned long long timeout_ns,
                                     cudaStream_t stream) {
