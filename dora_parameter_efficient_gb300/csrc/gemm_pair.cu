@@ -189,6 +189,12 @@ __device__ __forceinline__ void item_range(const PairParams& p, const ModView& m
                 nsplit);
 }
 
+// acquire-release fence at GPU scope: orders this thread's partial stores
+// before the completion counter's update, and the last segment's reads of the
+// other segments' partials after it (lighter than the sequentially
+// consistent __threadfence)
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // global fp32 load that bypasses L1 (data written by other CTAs of this grid)
 __device__ __forceinline__ float ld_cg_f(const float* p) {
   float v;
@@ -673,7 +679,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (h == 0 && valid) mv.out_dot[static_cast<size_t>(split) * mv.rows + grow] = acc + dh[trow];
       // the last segment of this 128-row group to finish assembles wnorm and
       // g for its rows from the partials of every segment, in segment order
-      __threadfence();
+      fence_acq_rel_gpu();
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (warp == 2 && lane == 0) {
         const int prev = atomicAdd(mv.tile_done + tile * 2 + static_cast<int>(rank), 1);
@@ -681,16 +687,35 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (*last_flag && h == 0 && valid) {
-        __threadfence();
+        fence_acq_rel_gpu();
         // segment partials added in segment order, carried as double-floats,
-        // after the caller's summed partials of the whole d_in range (if any)
+        // after the caller's summed partials of the whole d_in range (if any);
+        // the first four segments' partials are loaded together (one L2
+        // round trip on this item's critical tail instead of one per segment)
         df base{0.f, 0.f}, cross{0.f, 0.f};
         if (!kGrouped && p.ext_base) {
           base.hi = p.ext_base[grow];
           cross.hi = p.ext_cross[grow];
         }
+        constexpr int kBatch = 4;
+        float vb[kBatch], vc[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          vb[i] = i < nsplit ? __ldcg(mv.out_sumsq + static_cast<size_t>(i) * mv.rows + grow) : 0.f;
+          vc[i] = i < nsplit ? __ldcg(mv.out_dot + static_cast<size_t>(i) * mv.rows + grow) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          if (i < nsplit) {
+            float e;
+            two_sum(base.hi, vb[i], base.hi, e);
+            base.lo = __fadd_rn(base.lo, e);
+            two_sum(cross.hi, vc[i], cross.hi, e);
+            cross.lo = __fadd_rn(cross.lo, e);
+          }
+        }
 #pragma unroll 1
-        for (int i = 0; i < nsplit; ++i) {
+        for (int i = kBatch; i < nsplit; ++i) {
           float e;
           two_sum(base.hi, ld_cg_f(mv.out_sumsq + static_cast<size_t>(i) * mv.rows + grow), base.hi, e);
           base.lo = __fadd_rn(base.lo, e);
