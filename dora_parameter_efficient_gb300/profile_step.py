@@ -9,6 +9,11 @@ backward with the magnitude gradient).
 With --grouped it runs every module of the config instead (the 196-module
 stack: --config 4) as one grouped norm per step through a plan created once,
 then one grouped compose, with inputs drawn on the device.
+
+With --compose-pairs each step runs a second compose right after the first,
+on a second set of activations (a copy) into a second output, so a profiler
+that captures the second one sees the first one's output written back from
+L2 to HBM during it, as it is in a running step.
 """
 from __future__ import annotations
 
@@ -73,6 +78,7 @@ def main() -> int:
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--training", action="store_true")
     ap.add_argument("--grouped", action="store_true")
+    ap.add_argument("--compose-pairs", action="store_true")
     args = ap.parse_args()
     cfg = configs.get(args.config)
     if args.grouped:
@@ -86,6 +92,8 @@ def main() -> int:
     wn = torch.empty(d_out, dtype=torch.float32, device="cuda")
     g = torch.empty(d_out, dtype=torch.float32, device="cuda")
     out = torch.empty_like(base)
+    if args.compose_pairs:
+        base2, lora2, out2 = base.clone(), lora.clone(), torch.empty_like(base)
     if args.training:
         grad = to_dev(gen.grad_inputs(cfg, module=args.module), cfg.dtype)
         inner = torch.empty_like(base)
@@ -100,6 +108,8 @@ def main() -> int:
         e[1].record()
         api.dora_compose(base, lora, g, cfg.s, out=out)
         e[2].record()
+        if args.compose_pairs:
+            api.dora_compose(base2, lora2, g, cfg.s, out=out2)
         if args.training:
             api.dora_compose_train(base, lora, g, cfg.s, out=out, inner=inner)
             api.dora_compose_backward(grad, g, cfg.s, inner=inner, wnorm=wn, eps=cfg.eps,
