@@ -145,8 +145,8 @@ __global__ void __launch_bounds__(256) k_zero_words(int* __restrict__ p, int n) 
   griddep_wait();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
   // only now may the Gram kernel's CTAs (most of an SM's shared memory
-  // each) become resident: launched earlier they sit on SMs that the
-  // previous kernel -- often a compose of one wave -- still needs
+  // each) become resident, so that they never hold SMs the previous kernel
+  // still has blocks waiting for
   griddep_launch_dependents();
 }
 
