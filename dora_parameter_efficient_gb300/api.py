@@ -461,14 +461,20 @@ def dora_selftest_timeout(workspace: torch.Tensor, timeout_us: int,
 def dora_selftest_schedule(d_out: int, d_in: int, r: int, clusters: int):
     """Host-only check of the main pass's work decomposition for a bf16
     d_out x d_in module at rank r on `clusters` CTA pairs: returns
-    (uses_static_ranges, most_pieces_of_one_tile, defects); defects is 0 when
+    (schedule, most_pieces_of_one_tile, defects) with schedule one of
+    SCHEDULE_SEGMENTS, SCHEDULE_RANGES, SCHEDULE_TABLE; defects is 0 when
     every pair tile's K range is covered once, in order, by at most 16
     numbered pieces."""
-    ur, mp, df = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    sc, mp, df = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
     st = _lib.load().dora_selftest_schedule(int(d_out), int(d_in), int(r), int(clusters),
-                                            ctypes.byref(ur), ctypes.byref(mp), ctypes.byref(df))
+                                            ctypes.byref(sc), ctypes.byref(mp), ctypes.byref(df))
     check(st, "dora_selftest_schedule")
-    return bool(ur.value), int(mp.value), int(df.value)
+    return int(sc.value), int(mp.value), int(df.value)
+
+
+SCHEDULE_SEGMENTS = 0   # K segments handed out one by one
+SCHEDULE_RANGES = 1     # one static range of (pair tile, K tile) iterations per pair
+SCHEDULE_TABLE = 2      # piece table: one K range of one pair tile per pair
 
 
 def dora_selftest_grouped_schedule(shapes, r: int, clusters: int):

@@ -41,6 +41,7 @@ constexpr int kTcBlockM = 128;
 constexpr int kTcBlockK = 64;                 // bf16 elements per 128-byte smem row
 constexpr uint32_t kTcXTileBytes = kTcBlockM * 128;
 constexpr int kTcMaxStages = 8;
+constexpr int kPairTabMax = 128;              // pieces of a piece-table main pass
 
 struct GramParams {
   int nb;                // 128-row blocks per side of G (upper triangle computed)
@@ -144,6 +145,11 @@ struct PairParams {
   int ktot;              // K tiles per pair tile: kt_w + 2 * kt_b
   int iters;             // pair_tiles * ktot
   int n_early, len_early, len_late;
+  // piece table (single-module launch, n_tab != 0): work item i is the piece
+  // tab[i] = {tile | split << 16 | nsplit << 24, kb, ke}; used with fewer
+  // pair tiles than pairs, one piece per pair, the long pieces first
+  int n_tab;
+  uint32_t tab[kPairTabMax][3];
   // grouped launch: the per-module fields above are unused, these are
   const PairModule* mods;
   int n_mods;
@@ -191,6 +197,17 @@ __host__ __device__ inline int64_t range_next(const PairParams& p, int64_t lo, i
   const int64_t t0 = (cur - 1) / p.ktot * p.ktot;
   cur = t0 > lo ? t0 : lo;
   return cur;
+}
+
+// Piece table: work item -> its piece.
+__host__ __device__ inline void table_piece(const PairParams& p, int item, int& tile, int& split,
+                                            int& kb, int& ke, int& nsplit) {
+  const uint32_t w = p.tab[item][0];
+  tile = static_cast<int>(w & 0xFFFFu);
+  split = static_cast<int>((w >> 16) & 0xFFu);
+  nsplit = static_cast<int>(w >> 24);
+  kb = static_cast<int>(p.tab[item][1]);
+  ke = static_cast<int>(p.tab[item][2]);
 }
 
 // K segments: work item -> its piece (items segment-major: every tile's

@@ -255,6 +255,15 @@ void plan_pair_segments(PairParams& pp, int clusters) {
 #endif
 constexpr int64_t kMinRange = 8;
 
+// K tiles a pair behind the Gram kernel starts after the others: about
+// 1 us + 0.7 us per Gram K tile of one CTA, against 0.47 us per main-pass K
+// tile at r = 384 (tensor-bound; bound by W's HBM stream below r ~ 288)
+int64_t gram_lag_tiles(const PairParams& pp, int gram_kt) {
+  const int rp = pp.n0 + pp.n1;
+  const double tau_us = 0.47 * (rp > 288 ? rp : 288) / 384.0;
+  return std::llround((DORA_RANGE_LATE_US0 + DORA_RANGE_LATE_US_PER_KT * gram_kt) / tau_us);
+}
+
 bool plan_pair_ranges(PairParams& pp, int clusters, int gram_ctas, int gram_kt) {
   pp.ranges = 0;
   if (!DORA_STATIC_RANGES || clusters <= 0 || pp.pair_tiles < clusters) return false;
@@ -264,10 +273,7 @@ bool plan_pair_ranges(PairParams& pp, int clusters, int gram_ctas, int gram_kt) 
   const int64_t n = clusters;
   int64_t late = gram_ctas > 0 ? (gram_ctas + 1) / 2 : 0;
   if (late >= n) late = 0;
-  const int rp = pp.n0 + pp.n1;
-  const double tau_us = 0.47 * (rp > 288 ? rp : 288) / 384.0;
-  const int64_t lag =
-      late > 0 ? std::llround((DORA_RANGE_LATE_US0 + DORA_RANGE_LATE_US_PER_KT * gram_kt) / tau_us) : 0;
+  const int64_t lag = late > 0 ? gram_lag_tiles(pp, gram_kt) : 0;
   const int64_t le = ceil_div(iters + late * lag, n);
   const int64_t ll = late > 0 ? (le - lag > 1 ? le - lag : 1) : le;
   const int64_t lmin = ll < le ? ll : le;
@@ -282,6 +288,179 @@ bool plan_pair_ranges(PairParams& pp, int clusters, int gram_ctas, int gram_kt) 
   pp.n_early = static_cast<int>(n - late);
   pp.len_early = static_cast<int>(le);
   pp.len_late = static_cast<int>(ll);
+  return true;
+}
+
+// Piece table of the single-module main pass with fewer pair tiles than
+// pairs: every pair runs exactly one piece (a K range of one pair tile), so
+// no pair pays for a second accumulator drain (about 2.4 us at r = 384),
+// and the pieces are sized for when their pairs start.  The `late` pairs
+// that share SMs with the Gram kernel start about `lag` K tiles after the
+// others and claim last, so they get pieces `lag` tiles shorter.  A tile is
+// cut into e pieces for early pairs and l for late ones; with F the longest
+// early piece, e F + l (F - lag) >= ktot must hold.  The smallest F for which
+// the tiles can be cut with at most n - late early and late late pieces is
+// found by a small dynamic program over the tiles (they are all alike, so
+// it only counts pieces).  Inside a tile the early pieces come first in K
+// and the late ones (which start after the Gram kernel has finished) hold
+// the (B, G') tiles at the end; the table lists the early pieces longest
+// first, then the late ones.  Returns false (K segments are used) when the
+// cut needs more than kMaxMainSplits pieces in a tile or kPairTabMax pieces.
+// Measured on one GB300 at 8192 x 8192, r = 384: see plan_main_pass.
+#ifndef DORA_PIECE_TABLE
+#define DORA_PIECE_TABLE 1
+#endif
+// The cut depends only on (pair tiles, K tiles, pairs, late, lag); it is
+// planned once per such key (a dynamic program of up to a few hundred
+// thousand steps) and kept in a small cache, so a call costs a table copy.
+struct PieceKey {
+  int64_t T, K, clusters, late, lag;
+  bool operator==(const PieceKey& o) const {
+    return T == o.T && K == o.K && clusters == o.clusters && late == o.late && lag == o.lag;
+  }
+};
+struct PieceEntry {
+  PieceKey key;
+  bool ok;
+  int n_tab;
+  uint32_t tab[kPairTabMax][3];
+};
+std::mutex g_piece_mu;
+PieceEntry g_piece_cache[16];
+int g_piece_used = 0, g_piece_next = 0;
+
+bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64_t lag);
+
+bool plan_pair_pieces(PairParams& pp, int clusters, int64_t late, int64_t lag) {
+  pp.n_tab = 0;
+  const int64_t T = pp.pair_tiles;
+  const int64_t K = pp.kt_w + 2 * static_cast<int64_t>(pp.kt_b);
+  if (!DORA_PIECE_TABLE || T <= 0 || K <= 0 || T >= clusters || clusters > kPairTabMax) return false;
+  if (late >= clusters || lag <= 0) late = 0;
+  if (late == 0) lag = 0;
+  const PieceKey key{T, K, clusters, late, lag};
+  std::lock_guard<std::mutex> lk(g_piece_mu);
+  for (int i = 0; i < g_piece_used; ++i) {
+    const PieceEntry& e = g_piece_cache[i];
+    if (e.key == key) {
+      if (!e.ok) return false;
+      pp.n_tab = e.n_tab;
+      std::memcpy(pp.tab, e.tab, sizeof(uint32_t) * 3 * static_cast<size_t>(e.n_tab));
+      return true;
+    }
+  }
+  const bool ok = plan_pair_pieces_uncached(pp, clusters, late, lag);
+  PieceEntry& e = g_piece_cache[g_piece_next];
+  g_piece_next = (g_piece_next + 1) % 16;
+  if (g_piece_used < 16) ++g_piece_used;
+  e.key = key;
+  e.ok = ok;
+  e.n_tab = ok ? pp.n_tab : 0;
+  if (ok) std::memcpy(e.tab, pp.tab, sizeof(uint32_t) * 3 * static_cast<size_t>(pp.n_tab));
+  return ok;
+}
+
+bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64_t lag) {
+  pp.n_tab = 0;
+  const int64_t T = pp.pair_tiles;
+  const int64_t K = pp.kt_w + 2 * static_cast<int64_t>(pp.kt_b);
+  const int64_t ne = clusters - late;
+  constexpr int64_t kNone = int64_t(1) << 40;
+  int64_t best_F = -1;
+  std::vector<int64_t> lmin(kMaxMainSplits + 1);
+  // dp[i][e]: fewest late pieces that cut i tiles with e early pieces
+  std::vector<std::vector<int64_t>> dp;
+  std::vector<std::vector<int>> pick;
+  // no cut has a longest early piece below the mean piece over all pairs
+  const int64_t f0 = (T * K + clusters - 1) / clusters;
+  for (int64_t F = f0 > 1 ? f0 : 1; F <= K && best_F < 0; ++F) {
+    const int64_t Fl = late > 0 ? F - lag : 0;
+    for (int e = 0; e <= kMaxMainSplits; ++e) {
+      const int64_t rest = K - e * F;
+      if (rest <= 0) lmin[e] = e >= 1 ? 0 : kNone;
+      else lmin[e] = Fl >= 1 ? (rest + Fl - 1) / Fl : kNone;
+      if (lmin[e] != kNone && e + lmin[e] > kMaxMainSplits) lmin[e] = kNone;
+    }
+    dp.assign(static_cast<size_t>(T + 1), std::vector<int64_t>(static_cast<size_t>(ne + 1), kNone));
+    pick.assign(static_cast<size_t>(T + 1), std::vector<int>(static_cast<size_t>(ne + 1), -1));
+    dp[0][0] = 0;
+    for (int64_t i = 0; i < T; ++i)
+      for (int64_t u = 0; u <= ne; ++u) {
+        if (dp[i][u] == kNone) continue;
+        for (int e = 0; e <= kMaxMainSplits && u + e <= ne; ++e) {
+          if (lmin[e] == kNone) continue;
+          const int64_t v = dp[i][u] + lmin[e];
+          if (v < dp[i + 1][u + e]) {
+            dp[i + 1][u + e] = v;
+            pick[i + 1][u + e] = e;
+          }
+        }
+      }
+    for (int64_t u = 0; u <= ne; ++u)
+      if (dp[T][u] <= late) {
+        best_F = F;
+        break;
+      }
+  }
+  if (best_F < 0) return false;
+  const int64_t F = best_F;
+  // among the cuts with that F, the one with the fewest pieces (each piece
+  // costs an accumulator drain and a set of partials), then the fewest late ones
+  int64_t u = -1;
+  for (int64_t v = ne; v >= 0; --v)
+    if (dp[T][v] <= late && (u < 0 || v + dp[T][v] < u + dp[T][u])) u = v;
+  std::vector<int> e_of(static_cast<size_t>(T));
+  for (int64_t i = T; i > 0; --i) {
+    const int e = pick[i][u];
+    e_of[static_cast<size_t>(i - 1)] = e;
+    u -= e;
+  }
+  struct Piece { int tile, split, nsplit, kb, ke; bool early; };
+  std::vector<Piece> early, latep;
+  for (int64_t t = 0; t < T; ++t) {
+    const int e = e_of[static_cast<size_t>(t)];
+    const int64_t rest = K - e * F;
+    const int l = rest <= 0 ? 0 : static_cast<int>(lmin[e]);
+    const int n = e + l;
+    // lengths: early x, late x - lag, summing to K (x <= F by the cut rule)
+    std::vector<int64_t> len(static_cast<size_t>(n));
+    const int64_t tot = K + static_cast<int64_t>(l) * (late > 0 ? lag : 0);
+    for (int i = 0; i < n; ++i) {
+      const int64_t x = tot / n + (i < tot % n ? 1 : 0);
+      len[static_cast<size_t>(i)] = i < e ? x : x - lag;
+    }
+    // the last late piece absorbs rounding; every piece at least one K tile
+    int64_t sum = 0;
+    for (int i = 0; i < n; ++i) {
+      if (len[static_cast<size_t>(i)] < 1) len[static_cast<size_t>(i)] = 1;
+      sum += len[static_cast<size_t>(i)];
+    }
+    len[static_cast<size_t>(n - 1)] += K - sum;
+    if (len[static_cast<size_t>(n - 1)] < 1) return false;
+    int64_t at = 0;
+    for (int i = 0; i < n; ++i) {
+      const int64_t ke = at + len[static_cast<size_t>(i)];
+      const Piece pc{static_cast<int>(t), i, n, static_cast<int>(at), static_cast<int>(ke), i < e};
+      (i < e ? early : latep).push_back(pc);
+      at = ke;
+    }
+    if (at != K) return false;
+  }
+  if (early.size() + latep.size() > static_cast<size_t>(kPairTabMax)) return false;
+  auto longer = [](const Piece& a, const Piece& b) {
+    return a.ke - a.kb != b.ke - b.kb ? a.ke - a.kb > b.ke - b.kb : a.tile < b.tile;
+  };
+  std::stable_sort(early.begin(), early.end(), longer);
+  std::stable_sort(latep.begin(), latep.end(), longer);
+  early.insert(early.end(), latep.begin(), latep.end());
+  for (size_t i = 0; i < early.size(); ++i) {
+    const Piece& q = early[i];
+    pp.tab[i][0] = static_cast<uint32_t>(q.tile) | static_cast<uint32_t>(q.split) << 16 |
+                   static_cast<uint32_t>(q.nsplit) << 24;
+    pp.tab[i][1] = static_cast<uint32_t>(q.kb);
+    pp.tab[i][2] = static_cast<uint32_t>(q.ke);
+  }
+  pp.n_tab = static_cast<int>(early.size());
   return true;
 }
 
@@ -322,8 +501,11 @@ int plan_main_pass(PairParams& pp, int64_t d_out, int64_t d_in, int64_t r, int c
   // starts from a finished G
   const int gnb = gram_nb(rp), gcl = gram_cluster_for(pp.kt_w);
   const int gram_ctas = mode == kPassFinal ? 0 : gnb * (gnb + 1) / 2 * gcl;
-  if (plan_pair_ranges(pp, clusters_max, gram_ctas, static_cast<int>(ceil_div(pp.kt_w, gcl))))
-    return pp.ranges;
+  const int gram_kt = static_cast<int>(ceil_div(pp.kt_w, gcl));
+  if (plan_pair_ranges(pp, clusters_max, gram_ctas, gram_kt)) return pp.ranges;
+  if (plan_pair_pieces(pp, clusters_max, gram_ctas > 0 ? (gram_ctas + 1) / 2 : 0,
+                       gram_ctas > 0 ? gram_lag_tiles(pp, gram_kt) : 0))
+    return pp.n_tab;
   const int items = pp.pair_tiles * pp.splits;
   return items < clusters_max ? items : clusters_max;
 }
@@ -1429,9 +1611,9 @@ int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned time
 }
 
 int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
-                           int* uses_ranges, int* max_pieces, int64_t* defects) {
+                           int* schedule, int* max_pieces, int64_t* defects) {
   if (d_out < 1 || d_in < 1 || r < 1 || r > DORA_MAX_RANK || clusters < 1 || clusters > 65535 ||
-      d_out >= (int64_t(1) << 31) || d_in >= (int64_t(1) << 31) || !uses_ranges || !max_pieces ||
+      d_out >= (int64_t(1) << 31) || d_in >= (int64_t(1) << 31) || !schedule || !max_pieces ||
       !defects)
     return DORA_ERR_INVALID_ARG;
   PairParams pp{};
@@ -1456,6 +1638,12 @@ int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
         add(tile, split, kb, ke, nsplit);
       }
     }
+  } else if (pp.n_tab > 0) {
+    if (launch != pp.n_tab || launch > clusters || pp.n_tab > kPairTabMax) ++bad;
+    for (int item = 0; item < pp.n_tab; ++item) {
+      table_piece(pp, item, tile, split, kb, ke, nsplit);
+      add(tile, split, kb, ke, nsplit);
+    }
   } else {
     if (launch < 1 || launch > clusters) ++bad;
     for (int item = 0; item < pp.pair_tiles * pp.splits; ++item) {
@@ -1479,7 +1667,7 @@ int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
     }
     if (at != ktot) ++bad;
   }
-  *uses_ranges = pp.ranges > 0 ? 1 : 0;
+  *schedule = pp.ranges > 0 ? 1 : (pp.n_tab > 0 ? 2 : 0);
   *max_pieces = most;
   *defects = bad;
   return DORA_OK;

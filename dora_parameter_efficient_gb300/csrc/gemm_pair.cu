@@ -178,11 +178,16 @@ __device__ __forceinline__ ModView view_of(const PairParams& p, const ModView& s
 //   also holds the G' tiles.
 //   Static ranges: the item is the first iteration of a piece; the pieces of
 //   a tile are the ranges that meet it, numbered in K order.
+//   Piece table: the item indexes a table of pieces planned on the host.
 template <bool kGrouped>
 __device__ __forceinline__ void item_range(const PairParams& p, const ModView& mv, int item,
                                            int& tile, int& split, int& kb, int& ke, int& nsplit) {
   if (!kGrouped && p.ranges > 0) {
     range_piece(p, item, tile, split, kb, ke, nsplit);
+    return;
+  }
+  if (!kGrouped && p.n_tab > 0) {
+    table_piece(p, item, tile, split, kb, ke, nsplit);
     return;
   }
   segment_piece(mv.seg_k, mv.splits, mv.pair_tiles, item - mv.item_begin, tile, split, kb, ke,
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs, 1: its peer
-  const int n_items = kGrouped ? p.n_items : p.pair_tiles * p.splits;
+  const int n_items = kGrouped ? p.n_items : (p.n_tab > 0 ? p.n_tab : p.pair_tiles * p.splits);
   const ModView single = single_view(p, &tW, &tA, &tB, &tGhi, &tGlo);
   const uint32_t item_empty0 = map_to_rank(smem_u32(item_empty), 0);
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;

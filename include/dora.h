@@ -419,16 +419,19 @@ int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned time
  * a bf16 single-module norm of d_out x d_in at rank r (1 .. DORA_MAX_RANK)
  * exactly as dora_factored_norm does on a device with `clusters` co-resident
  * CTA pairs (1 .. 65535; 76 on a GB300), enumerates every piece of work the
- * launched pairs would run -- K segments handed out in item order, or the
- * static ranges of each pair, issued from the last piece to the first -- and
+ * launched pairs would run -- K segments handed out in item order, the static
+ * ranges of each pair (issued from the last piece to the first), or the
+ * piece table (one piece per pair, with fewer pair tiles than pairs) -- and
  * checks that the pieces of every 256-row pair tile cover its K tiles once,
  * in K order, numbered 0 .. n - 1 with n <= 16 (the partial planes of the
- * workspace).  Writes whether static ranges were chosen, the largest number
- * of pieces of one tile, and the number of defects found (0 when the plan is
- * sound).  Returns DORA_ERR_INVALID_ARG for bad arguments, else DORA_OK.
+ * workspace), and that a piece table gives each launched pair one piece.
+ * Writes the schedule chosen (*schedule: 0 K segments, 1 static ranges,
+ * 2 piece table), the largest number of pieces of one tile, and the number
+ * of defects found (0 when the plan is sound).  Returns DORA_ERR_INVALID_ARG
+ * for bad arguments, else DORA_OK.
  */
 int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
-                           int* uses_ranges, int* max_pieces, int64_t* defects);
+                           int* schedule, int* max_pieces, int64_t* defects);
 
 /*
  * The same check for a grouped launch (host only, no GPU): plans the work

@@ -3,9 +3,10 @@
 dora_selftest_schedule plans a bf16 single-module norm exactly as
 dora_factored_norm does and enumerates every piece of work the launched CTA
 pairs would run, through the same functions the kernel uses: K segments
-handed out in item order, or static ranges (one contiguous run of
+handed out in item order, static ranges (one contiguous run of
 (pair tile, K tile) iterations per pair, issued from the last piece to the
-first).  A sound plan covers every pair tile's K tiles once, in K order,
+first), or a piece table (one K range of one pair tile per pair, with fewer
+pair tiles than pairs).  A sound plan covers every pair tile's K tiles once, in K order,
 with pieces numbered 0 .. n - 1 and n at most the 16 partial planes of the
 workspace; a mistake in that arithmetic would drop or double-count part of
 a row's sums.  dora_selftest_grouped_schedule does the same for a grouped
@@ -23,36 +24,49 @@ from dora_parameter_efficient_gb300._lib import DoraError
 GB300_PAIRS = 76
 
 
-@pytest.mark.parametrize("d_out,d_in,r,ranges", [
-    (8192, 8192, 384, False),     # fewer pair tiles (32) than pairs: K segments 7:4:2
-    (8100, 4104, 40, False),
-    (9000, 4104, 296, False),
-    (19500, 4104, 40, True),      # 77 pair tiles: static ranges
-    (19500, 4104, 296, True),
-    (20000, 4096, 384, True),
-    (28672, 8192, 384, True),
+TABLE, RANGES, SEGMENTS = api.SCHEDULE_TABLE, api.SCHEDULE_RANGES, api.SCHEDULE_SEGMENTS
+
+
+@pytest.mark.parametrize("d_out,d_in,r,schedule", [
+    (8192, 8192, 384, TABLE),     # fewer pair tiles (32) than pairs: one piece per pair
+    (8100, 4104, 40, TABLE),
+    (9000, 4104, 296, TABLE),
+    (2048, 8192, 384, TABLE),
+    (16384, 8192, 384, TABLE),
+    (19500, 4104, 40, RANGES),    # 77 pair tiles: static ranges
+    (19500, 4104, 296, RANGES),
+    (20000, 4096, 384, RANGES),
+    (28672, 8192, 384, RANGES),
 ])
-def test_known_shapes(d_out, d_in, r, ranges):
-    uses_ranges, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
+def test_known_shapes(d_out, d_in, r, schedule):
+    got, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
     assert defects == 0
-    assert uses_ranges == ranges
+    assert got == schedule
     assert 1 <= most <= 16
+
+
+def test_piece_table_of_the_metric_workload():
+    """8192 x 8192, r = 384 on 76 pairs: 32 pair tiles of 140 K tiles; the
+    24 pairs behind the Gram kernel start about 26 K tiles late.  One piece
+    per pair: 26 tiles in two early pieces of 70, 6 tiles in four late
+    pieces of 35 (the longest piece 70, against 75 for K segments 7:4:2)."""
+    got, most, defects = api.dora_selftest_schedule(8192, 8192, 384, GB300_PAIRS)
+    assert (got, most, defects) == (TABLE, 4, 0)
 
 
 def test_seeded_sweep_of_shapes_and_grids():
     rng = random.Random(2026)
-    seen_ranges = seen_segments = 0
+    seen = {TABLE: 0, RANGES: 0, SEGMENTS: 0}
     for _ in range(4000):
         d_out = rng.choice([rng.randint(1, 300), rng.randint(1, 5000), rng.randint(1, 200000)])
         d_in = rng.choice([rng.randint(1, 64), rng.randint(1, 20000), rng.randint(1, 100000)])
         r = rng.choice([rng.randint(1, 16), rng.randint(1, 512)])
         pairs = rng.choice([1, 2, 3, 7, 16, 60, 74, GB300_PAIRS, 148, 1000])
-        uses_ranges, most, defects = api.dora_selftest_schedule(d_out, d_in, r, pairs)
+        schedule, most, defects = api.dora_selftest_schedule(d_out, d_in, r, pairs)
         assert defects == 0, (d_out, d_in, r, pairs)
         assert 1 <= most <= 16, (d_out, d_in, r, pairs)
-        seen_ranges += uses_ranges
-        seen_segments += not uses_ranges
-    assert seen_ranges > 100 and seen_segments > 100      # both schedules exercised
+        seen[schedule] += 1
+    assert min(seen.values()) > 100, seen      # every schedule exercised
 
 
 @pytest.mark.parametrize("d_out", [1, 255, 256, 257, 76 * 256 - 1, 76 * 256, 76 * 256 + 1])
@@ -61,10 +75,10 @@ def test_boundaries_of_tiles_and_of_the_range_rule(d_out, d_in):
     """Row counts around one tile and around as many pair tiles as pairs
     (where the plan switches to static ranges), K around one tile."""
     for r in (8, 128, 384, 512):
-        uses_ranges, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
+        schedule, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
         assert defects == 0 and most <= 16
         if (d_out + 255) // 256 < GB300_PAIRS:
-            assert not uses_ranges
+            assert schedule != RANGES
 
 
 @pytest.mark.parametrize("args", [
