@@ -194,11 +194,17 @@ __device__ __forceinline__ void item_range(const PairParams& p, const ModView& m
                 nsplit);
 }
 
-// acquire-release fence at GPU scope: orders this thread's partial stores
-// before the completion counter's update, and the last segment's reads of the
-// other segments' partials after it (lighter than the sequentially
-// consistent __threadfence)
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// The completion counter of a 128-row group, incremented with acquire-release
+// semantics at GPU scope by one thread after a barrier of the epilogue warps:
+// the release publishes every epilogue thread's partial stores (they precede
+// the barrier), the acquire orders the last segment's reads of the other
+// segments' partials (after the next barrier) behind the other segments'
+// releases.  No thread needs a fence of its own.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 // global fp32 load that bypasses L1 (data written by other CTAs of this grid)
 __device__ __forceinline__ float ld_cg_f(const float* p) {
@@ -315,7 +321,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       bool g_ready = false;      // G'_hi / G'_lo written by the preceding kernel
       const uint32_t slot1 = map_to_rank(smem_u32(const_cast<int*>(item_slot)), 1);
       const uint32_t full1 = map_to_rank(smem_u32(item_full), 1);
-      int claimed = rank == 0 ? atomicAdd(p.work_ctr, 1) : 0;
+      // piece table: pair c runs piece c and nothing else (the table lists the
+      // long pieces first, and clusters start in index order, so the pairs
+      // behind the Gram kernel get the short ones); no claim on the counter
+      const bool by_index = !kGrouped && p.n_tab > 0;
+      int claimed = rank != 0 ? 0 : by_index ? static_cast<int>(blockIdx.x >> 1) : atomicAdd(p.work_ctr, 1);
       // static ranges: this pair's slot is its place in the start order; its
       // pieces are issued from the last to the first, so a pair's first piece
       // begins with W tiles and no pair meets a G' tile early
@@ -399,7 +409,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             phase ^= 1u;
           }
         }
-        if (rank == 0 && (kGrouped || p.ranges == 0)) claimed = atomicAdd(p.work_ctr, 1);
+        if (rank == 0 && (kGrouped || p.ranges == 0))
+          claimed = by_index ? n_items : atomicAdd(p.work_ctr, 1);
       }
       // A CTA that loaded no G' tile (every CTA for the partials of a d_in
       // slice) never waited for the Gram kernel this launch may overlap:
@@ -684,15 +695,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (h == 0 && valid) mv.out_dot[static_cast<size_t>(split) * mv.rows + grow] = acc + dh[trow];
       // the last segment of this 128-row group to finish assembles wnorm and
       // g for its rows from the partials of every segment, in segment order
-      fence_acq_rel_gpu();
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (warp == 2 && lane == 0) {
-        const int prev = atomicAdd(mv.tile_done + tile * 2 + static_cast<int>(rank), 1);
+        const int prev = atom_add_acq_rel_gpu(mv.tile_done + tile * 2 + static_cast<int>(rank), 1);
         *last_flag = prev == nsplit - 1 ? 1 : 0;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (*last_flag && h == 0 && valid) {
-        fence_acq_rel_gpu();
         // segment partials added in segment order, carried as double-floats,
         // after the caller's summed partials of the whole d_in range (if any);
         // the first four segments' partials are loaded together (one L2
