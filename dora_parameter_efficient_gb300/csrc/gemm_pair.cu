@@ -71,17 +71,26 @@ namespace dora {
 
 namespace {
 
+// acc + a^2 + b^2 for the two bf16 halves (a: low, b: high) of w, each step
+// one mixed-precision FMA (bf16 operands, fp32 addend and result, rounded
+// once): the bf16 product is exact in fp32, so each step equals
+// fmaf(float(a), float(a), acc) without the two unpacking instructions
+__device__ __forceinline__ float fma_sq_bf16x2(uint32_t w, float acc) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "fma.rn.f32.bf16 %0, lo, lo, %2;\n\t"
+      "fma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+      : "=f"(r)
+      : "r"(w), "f"(acc));
+  return r;
+}
+
 // Sum of squares of 8 bf16 values.
 __device__ __forceinline__ float sumsq8(const uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float acc = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float a = bf16_lo(w[i]), b = bf16_hi(w[i]);
-    acc = fmaf(a, a, acc);
-    acc = fmaf(b, b, acc);
-  }
-  return acc;
+  float acc = fma_sq_bf16x2(v.x, 0.f);
+  acc = fma_sq_bf16x2(v.y, acc);
+  acc = fma_sq_bf16x2(v.z, acc);
+  return fma_sq_bf16x2(v.w, acc);
 }
 
 // Columns [c0, c0 + 8 * N) of one row of B (bf16); columns past r read as 0.
