@@ -114,6 +114,8 @@ struct PairParams {
   uint32_t tmem_cols;    // acc_bufs * acc_stride
   int acc_bufs;          // accumulator buffers (2 when two fit in the 512 TMEM columns)
   uint32_t acc_stride;   // TMEM columns per accumulator buffer
+  uint32_t par_off;      // r <= 128: the odd K steps' accumulator, this many columns into
+                         // the buffer (0: one accumulator per buffer)
   // epilogue and the fused finalize
   const uint16_t* B;     // [rows x r] bf16
   const uint16_t* m;     // [rows] bf16

@@ -245,7 +245,13 @@ __device__ __forceinline__ int read_item(uint32_t n, uint64_t* item_full, const 
   return item;
 }
 
-template <bool kGrouped>
+// kPar (r <= 128, one N chunk): the K steps of a tile alternate between two
+// accumulators -- even K steps into the buffer's first, odd ones into its
+// second, p.par_off columns on -- and the epilogue adds the two.  MMAs that
+// accumulate into the same tensor memory wait for each other (about 110
+// cycles each at N <= 128, more than their math), so one chain of four per K
+// tile set the tile rate at small ranks; two chains halve that wait.
+template <bool kGrouped, bool kPar>
 __global__ void __launch_bounds__(kPairThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tW, const __grid_constant__ CUtensorMap tA,
                 const __grid_constant__ CUtensorMap tB, const __grid_constant__ CUtensorMap tGhi,
@@ -482,9 +488,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint32_t first = kt == kb ? 0u : 1u;
 #pragma unroll
           for (int ks = 0; ks < kTcBlockK / 16; ++ks) {
-            const uint32_t acc = ks > 0 ? 1u : first;
-            umma_bf16_pair(acc0, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
-            if (two) umma_bf16_pair(acc1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
+            if constexpr (kPar) {
+              // the first two K steps of an item start the two chains
+              const uint32_t acc = (kt == kb && ks < 2) ? 0u : 1u;
+              umma_bf16_pair(acc0 + ((ks & 1) ? p.par_off : 0u), dx + 2 * ks, dy + 2 * ks, idesc0,
+                             acc);
+            } else {
+              const uint32_t acc = ks > 0 ? 1u : first;
+              umma_bf16_pair(acc0, dx + 2 * ks, dy + 2 * ks, idesc0, acc);
+              if (two) umma_bf16_pair(acc1, dx + 2 * ks, dy + dy1_off + 2 * ks, idesc1, acc);
+            }
           }
           umma_commit_pair(&consumed[s], 0x3);
           if (++s == stages) {
@@ -584,11 +597,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           phase ^= 1u;
         }
       };
-      // up to 192 columns of this lane's B half-row, two 16-byte pieces per tile
-      uint4 bb[24];
+      // up to 192 columns of this lane's B half-row (64 with two accumulators,
+      // r <= 128), two 16-byte pieces per tile
+      constexpr int kBV = kPar ? 8 : 24;
+      uint4 bb[kBV];
       int kt = kb;
 #pragma unroll
-      for (int v = 0; v < 24; v += 2) {
+      for (int v = 0; v < kBV; v += 2) {
         if (kt < ke) epi_tile(kt++);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -649,46 +664,66 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         int nh = 2 * c_hi - hc0;
         if (nh > rp / 16 - hc0) nh = rp / 16 - hc0;
         if (nh > 12) nh = 12;
-        uint32_t ra[16], rb[16];
-        if (nh > 0) {
-          tmem_load_16cols_async(acc_row + static_cast<uint32_t>(hc0 * 16), ra);
-          tmem_wait_ld(ra);
-        }
+        if constexpr (kPar) {
+          // two accumulators: each column is the sum of its even-K and odd-K
+          // chains, added once in fp32 before the dot with B
 #pragma unroll
-        for (int k = 0; k < 12; k += 2) {
-          if (k < nh) {
-            if (k + 1 < nh)
-              tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k + 1) * 16), rb);
+          for (int k = 0; k < kBV / 2; ++k) {
+            if (k < nh) {
+              uint32_t ra[16], rb[16];
+              tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k) * 16), ra);
+              tmem_load_16cols_async(acc_row + p.par_off + static_cast<uint32_t>((hc0 + k) * 16), rb);
+              tmem_wait_ld(ra);
+              tmem_wait_ld(rb);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = __fadd_rn(__uint_as_float(ra[i]), __uint_as_float(rb[i]));
+              const uint4 part[2] = {bb[2 * k], bb[2 * k + 1]};
+              acc = dot_b<2>(part, v, acc);
+            }
+          }
+        } else {
+          uint32_t ra[16], rb[16];
+          if (nh > 0) {
+            tmem_load_16cols_async(acc_row + static_cast<uint32_t>(hc0 * 16), ra);
+            tmem_wait_ld(ra);
+          }
+#pragma unroll
+          for (int k = 0; k < 12; k += 2) {
+            if (k < nh) {
+              if (k + 1 < nh)
+                tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k + 1) * 16), rb);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(ra[i]);
+              const uint4 part[2] = {bb[2 * k], bb[2 * k + 1]};
+              acc = dot_b<2>(part, v, acc);
+              if (k + 1 < nh) tmem_wait_ld(rb);
+            }
+            if (k + 1 < nh) {
+              if (k + 2 < nh)
+                tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k + 2) * 16), ra);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rb[i]);
+              const uint4 part[2] = {bb[2 * k + 2], bb[2 * k + 3]};
+              acc = dot_b<2>(part, v, acc);
+              if (k + 2 < nh) tmem_wait_ld(ra);
+            }
+          }
+          // ranks above 384: the rest of the half, B loaded now
+          const int col_end = c_hi * 32 < rp ? c_hi * 32 : rp;
+          for (int col = (c_lo + 6) * 32; col < col_end; col += 16) {
+            uint4 part[2];
+            load_b_cols<2>(brow, col, p.r, valid, part);
+            uint32_t rv[16];
+            tmem_load_16cols_async(acc_row + static_cast<uint32_t>(col), rv);
+            tmem_wait_ld(rv);
             float v[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(ra[i]);
-            const uint4 part[2] = {bb[2 * k], bb[2 * k + 1]};
+            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rv[i]);
             acc = dot_b<2>(part, v, acc);
-            if (k + 1 < nh) tmem_wait_ld(rb);
           }
-          if (k + 1 < nh) {
-            if (k + 2 < nh)
-              tmem_load_16cols_async(acc_row + static_cast<uint32_t>((hc0 + k + 2) * 16), ra);
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rb[i]);
-            const uint4 part[2] = {bb[2 * k + 2], bb[2 * k + 3]};
-            acc = dot_b<2>(part, v, acc);
-            if (k + 2 < nh) tmem_wait_ld(ra);
-          }
-        }
-        // ranks above 384: the rest of the half, B loaded now
-        const int col_end = c_hi * 32 < rp ? c_hi * 32 : rp;
-        for (int col = (c_lo + 6) * 32; col < col_end; col += 16) {
-          uint4 part[2];
-          load_b_cols<2>(brow, col, p.r, valid, part);
-          uint32_t rv[16];
-          tmem_load_16cols_async(acc_row + static_cast<uint32_t>(col), rv);
-          tmem_wait_ld(rv);
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rv[i]);
-          acc = dot_b<2>(part, v, acc);
         }
       }
       // accumulator drained: let the even CTA start the next item's MMAs
@@ -811,11 +846,15 @@ int pair_max_clusters(size_t smem_bytes) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaFuncSetAttribute(k_gemm_pair<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(k_gemm_pair<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMaxSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(k_gemm_pair<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(k_gemm_pair<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMaxSmem) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<false>, &cfg) != cudaSuccess)
+      cudaFuncSetAttribute(k_gemm_pair<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_gemm_pair<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<false, false>, &cfg) != cudaSuccess)
     return 0;
   if (dev < 64) cached[dev] = n;
   return n;
@@ -840,7 +879,9 @@ cudaError_t launch_gemm_pair(const CUtensorMap& tW, const CUtensorMap& tA, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair<false>, tW, tA, tB, tGhi, tGlo, p);
+  cudaError_t e = p.par_off != 0
+                      ? cudaLaunchKernelEx(&cfg, k_gemm_pair<false, true>, tW, tA, tB, tGhi, tGlo, p)
+                      : cudaLaunchKernelEx(&cfg, k_gemm_pair<false, false>, tW, tA, tB, tGhi, tGlo, p);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -865,7 +906,9 @@ cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStre
   cfg.numAttrs = 2;
   CUtensorMap none;
   std::memset(&none, 0, sizeof(none));
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_pair<true>, none, none, none, none, none, p);
+  cudaError_t e = p.par_off != 0
+                      ? cudaLaunchKernelEx(&cfg, k_gemm_pair<true, true>, none, none, none, none, none, p)
+                      : cudaLaunchKernelEx(&cfg, k_gemm_pair<true, false>, none, none, none, none, none, p);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
