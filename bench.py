@@ -753,6 +753,19 @@ def run_ours(args):
         "timing": f"CUDA events around each call, mean over {train_steps} steps, "
                   f"{N_SETS} rotating input sets",
     }
+    # the same kernels back to back: forward alone, and forward + backward
+    # (one event pair around each loop, none between launches)
+    tf_b2b = loop_ms(lambda i: train_fwd(i % N_SETS), train_steps)
+    tfb_b2b = loop_ms(lambda i: (train_fwd(i % N_SETS), train_bwd(i % N_SETS)), train_steps)
+    tb_b2b = tfb_b2b - tf_b2b
+    compose_training["back_to_back"] = {
+        "forward_ms": tf_b2b, "forward_GB/s": tf_bytes / (tf_b2b * 1e-3) / 1e9,
+        "forward_frac_of_measured_hbm": tf_bytes / (tf_b2b * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "backward_ms": tb_b2b, "backward_GB/s": tb_bytes / (tb_b2b * 1e-3) / 1e9,
+        "backward_frac_of_measured_hbm": tb_bytes / (tb_b2b * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "timing": f"loops of {train_steps} forwards and of {train_steps} forward + backward "
+                  f"pairs over the rotating sets, one event pair around each loop; backward = "
+                  f"the pair's time minus the forward's"}
 
     # ---- the 7B-like stack (196 modules, r = 128): grouped norm + compose,
     # one launch sequence per step for all modules; inputs drawn on the

@@ -60,6 +60,11 @@ struct GramParams {
   int r_out;
   int* status;
   unsigned long long timeout_ns;
+  // single-module launch heading the norm's chain: the first CTA zeroes these
+  // control words of the workspace (status, work counter, completion
+  // counters) before the main pass may launch (zero_n = 0: none)
+  int* zero_p;
+  int zero_n;
 };
 
 // one module of a grouped Gram launch (same rank, so the same block grid)

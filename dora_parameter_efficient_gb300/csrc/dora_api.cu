@@ -560,10 +560,15 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? DORA_OK : DORA_ERR_CU
 //   kPassFinal: G' from the summed G of part_in + 2 d_out (split kernel), the
 //     main pass over the (B, G') tiles only, its finalize adding the summed
 //     base and cross of part_in ahead of its own partials.
+// zero_words: the pass also zeroes the workspace's control words -- in the
+// Gram kernel that heads the chain when the main pass runs a piece table
+// (it touches them only after waiting for that grid), else with the
+// zeroing kernel first.
 int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, int64_t d_in,
                   int64_t r, float s, const void* m, float eps, float* wnorm, float* g,
                   const Plan& plan, uint8_t* ws, int mode, float* part_out,
-                  const float* part_in, cudaStream_t stream, void* ev_begin, void* ev_end) {
+                  const float* part_in, cudaStream_t stream, void* ev_begin, void* ev_end,
+                  bool zero_words = false) {
   int* status = reinterpret_cast<int*>(ws + plan.off_status);
   uint16_t* Ghi = reinterpret_cast<uint16_t*>(ws + plan.off_Ghi);
   uint16_t* Glo = reinterpret_cast<uint16_t*>(ws + plan.off_Glo);
@@ -600,6 +605,24 @@ int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, in
   }
   if (mode == kPassFinal) mA_y2 = mGhi;
 
+  // the main pass's work decomposition (host only), planned first: with a
+  // piece table it never claims from the work counter, so the Gram kernel can
+  // zero the control words in place of a kernel of its own
+  PairParams pp{};
+  int clusters = 0;
+  if (d_out > 0) {
+    pp.rows = static_cast<int>(d_out);
+    pp.y_box_rows = y_box2;
+    pp.stages = pair_pick_stages(rp, false);
+    const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, false));
+    if (clusters_max <= 0) return DORA_ERR_CUDA;
+    clusters = plan_main_pass(pp, d_out, d_in, r, clusters_max, mode);
+    if (pp.n0 != n0 || pp.n1 != n1) return DORA_ERR_UNSUPPORTED;
+  }
+  const bool gram_zeroes = zero_words && mode != kPassFinal && d_out > 0 && pp.n_tab > 0;
+  if (zero_words && !gram_zeroes)
+    DORA_TRY(launch_zero_words(status, static_cast<int>(plan.zero_bytes / 4), stream));
+
   if (mode == kPassFinal) {
     DORA_TRY(launch_gram_split(part_in + 2 * d_out, static_cast<int>(r), rp, 0.5f * s, Ghi, Glo,
                                stream));
@@ -621,18 +644,14 @@ int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, in
     }
     pg.status = status;
     pg.timeout_ns = kDefaultTimeoutNs;
+    if (gram_zeroes) {
+      pg.zero_p = status;
+      pg.zero_n = static_cast<int>(plan.zero_bytes / 4);
+    }
     DORA_TRY(launch_gram(mA_x, mA_yg, pg, stream));
   }
   if (d_out == 0) return DORA_OK;
 
-  PairParams pp{};
-  pp.rows = static_cast<int>(d_out);
-  pp.y_box_rows = y_box2;
-  pp.stages = pair_pick_stages(rp, false);
-  const int clusters_max = pair_max_clusters(pair_smem_bytes(rp, pp.stages, false));
-  if (clusters_max <= 0) return DORA_ERR_CUDA;
-  const int clusters = plan_main_pass(pp, d_out, d_in, r, clusters_max, mode);
-  if (pp.n0 != n0 || pp.n1 != n1) return DORA_ERR_UNSUPPORTED;
   pp.r = static_cast<int>(r);
   set_accumulators(pp, tmem_cols);
   pp.B = static_cast<const uint16_t*>(B);
@@ -826,7 +845,10 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
 
-  DORA_TRY(launch_zero_words(status, static_cast<int>(plan.zero_bytes / 4), stream));
+  // the bf16 tensor-core pass zeroes the control words itself (in its Gram
+  // kernel when it can), every other path with the zeroing kernel here
+  if (!(adapter && bf16 && d_in > 0))
+    DORA_TRY(launch_zero_words(status, static_cast<int>(plan.zero_bytes / 4), stream));
 
   int n_base = 0;
   if (d_in == 0) {
@@ -839,7 +861,7 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
     n_base = 1;
   } else if (bf16) {
     return run_bf16_pass(W, A, B, d_out, d_in, r, s, m, eps, wnorm, g, plan, ws, kPassFull,
-                         nullptr, nullptr, stream, ev_begin, ev_end);
+                         nullptr, nullptr, stream, ev_begin, ev_end, /*zero_words=*/true);
   } else {
     return run_f32_pass(W, A, B, d_out, d_in, r, s, m, eps, wnorm, g, plan, ws, kPassFull,
                         nullptr, nullptr, stream, ev_begin, ev_end);

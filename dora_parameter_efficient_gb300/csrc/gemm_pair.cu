@@ -231,13 +231,21 @@ constexpr int kPairEpiWarps = kPairEpiThreads / 32;
 constexpr uint32_t kItemRing = 4;
 constexpr uint32_t kItemReaders = 2 + 2 * kPairEpiWarps;
 
+// The workspace's control words may be zeroed by the Gram kernel this grid
+// depends on: a timeout is recorded in the status word only after that grid
+// has finished (its own waits are bounded, so this wait ends too).
+__device__ __forceinline__ void record_timeout(int* status) {
+  griddep_wait();
+  atomicExch(status, kStatusTimeout);
+}
+
 // The n-th work item of this CTA pair (-1: no more work), as published in the
 // ring; the reader releases the slot on the even CTA's `item_empty`.
 __device__ __forceinline__ int read_item(uint32_t n, uint64_t* item_full, const volatile int* item_slot,
                                          uint32_t item_empty0, uint64_t deadline, int* status) {
   const uint32_t slot = n % kItemRing;
   if (!mbar_wait_cluster(&item_full[slot], (n / kItemRing) & 1u, deadline)) {
-    atomicExch(status, kStatusTimeout);
+    record_timeout(status);
     return -1;
   }
   const int item = item_slot[slot];
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint32_t slot = n % kItemRing;
           if (n >= kItemRing &&
               !mbar_wait_cluster(&item_empty[slot], (n / kItemRing - 1) & 1u, deadline)) {
-            atomicExch(p.status, kStatusTimeout);
+            record_timeout(p.status);
             *abort_flag = 1;
             break;
           }
@@ -385,7 +393,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           // the slot's previous use (parity phase ^ 1) must have been consumed
           // by the MMAs and read by the epilogue warps
           if (it >= stages && !mbar_wait(&empty[s], phase ^ 1u, deadline)) {
-            atomicExch(p.status, kStatusTimeout);
+            record_timeout(p.status);
             *abort_flag = 1;
             stop = true;
             break;
@@ -438,7 +446,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t first = it > stages ? it - stages : 0;
         for (uint32_t i = first; i < it; ++i)
           if (!mbar_wait(&full[i % stages], (i / stages) & 1u, drain_deadline))
-            atomicExch(p.status, kStatusTimeout);
+            record_timeout(p.status);
       }
     }
   } else if (warp == 1) {
@@ -471,14 +479,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         const uint32_t acc1 = acc0 + static_cast<uint32_t>(p.n0);
         if (use > 0 && !mbar_wait(&accum_empty[buf], (use - 1) & 1u, deadline)) {
           // the accumulator was never drained: issue nothing more
-          atomicExch(p.status, kStatusTimeout);
+          record_timeout(p.status);
           *abort_flag = 1;
           break;
         }
         tc_fence_after_sync();
         for (int kt = kb; kt < ke; ++kt) {
           if (!mbar_wait(&full[s], phase, deadline)) {
-            atomicExch(p.status, kStatusTimeout);
+            record_timeout(p.status);
             *abort_flag = 1;
             stop = true;
             break;
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       if (icount > 0) {
         const uint32_t last = static_cast<uint32_t>(icount - 1);
         if (!mbar_wait(&accum_full[last % nbuf], (last / nbuf) & 1u, global_timer_ns() + p.timeout_ns))
-          atomicExch(p.status, kStatusTimeout);
+          record_timeout(p.status);
       }
     }
   } else if (warp < 2 + kPairEpiWarps) {
@@ -575,7 +583,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // one tile of the item: wait for its MMAs, sum squares of the W tile, release it
       auto epi_tile = [&](int kt) {
         if (alive && !mbar_wait(&consumed[s], phase, deadline)) {
-          atomicExch(p.status, kStatusTimeout);
+          record_timeout(p.status);
           *abort_flag = 1;
           alive = false;
         }
@@ -635,7 +643,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint32_t acc_row = tmem_row + buf * p.acc_stride;   // this item's accumulator
       bool ok = alive && mbar_wait(&accum_full[buf], (static_cast<uint32_t>(icount) / nbuf) & 1u, deadline);
       if (alive && !ok) {
-        atomicExch(p.status, kStatusTimeout);
+        record_timeout(p.status);
         *abort_flag = 1;
       }
       tc_fence_after_sync();
@@ -741,6 +749,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       // g for its rows from the partials of every segment, in segment order
       asm volatile("bar.sync 1, %0;" ::"n"(kPairEpiThreads) : "memory");
       if (warp == 2 && lane == 0) {
+        // the completion counters may have been zeroed by the Gram kernel
+        // this grid depends on (immediate once that grid has finished)
+        griddep_wait();
         const int prev = atom_add_acq_rel_gpu(mv.tile_done + tile * 2 + static_cast<int>(rank), 1);
         *last_flag = prev == nsplit - 1 ? 1 : 0;
       }

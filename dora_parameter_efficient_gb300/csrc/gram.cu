@@ -84,12 +84,18 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   }
   const CUtensorMap& tAx = *tAxp;
   const CUtensorMap& tAy = *tAyp;
-  // launched as a programmatic dependent of the kernel that zeroes the
-  // workspace's control words (or of whatever precedes it in the stream):
-  // nothing is read or written before that grid has finished.  Then the main
-  // pass queued behind this kernel may start launching; it waits for this
-  // grid to finish before it reads G'.
+  // launched as a programmatic dependent of whatever precedes it in the
+  // stream (the previous norm on this workspace, or the kernel that zeroes
+  // the workspace's control words): nothing is read or written before that
+  // grid has finished.  When this kernel heads the norm's chain its first CTA
+  // zeroes the control words here; the main pass reads or writes them only
+  // after waiting for this grid (griddepcontrol.wait), and another CTA of
+  // this grid records a timeout only after its bounded wait (seconds) has
+  // run out.  Then the main pass queued behind this kernel may start
+  // launching; it waits for this grid to finish before it reads G'.
   griddep_wait();
+  if (!kGrouped && p_in.zero_n > 0 && blockIdx.x == 0)
+    for (int i = static_cast<int>(threadIdx.x); i < p_in.zero_n; i += kGramThreads) p_in.zero_p[i] = 0;
   griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
