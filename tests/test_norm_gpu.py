@@ -268,3 +268,42 @@ def test_deterministic_with_static_ranges():
     for wn, g in runs[1:]:
         np.testing.assert_array_equal(wn, runs[0][0])
         np.testing.assert_array_equal(g, runs[0][1])
+
+
+def test_one_workspace_across_schedules_and_leftover_words():
+    """One workspace, filled with random bytes first, serves norms that plan
+    their work differently -- a piece table (fewer pair tiles than pairs,
+    control words zeroed by the Gram kernel), static ranges (more pair tiles
+    than pairs, zeroing kernel), two accumulators per buffer (r <= 128) and
+    the s = 0 path -- in an order where every call finds the previous call's
+    control words (completion counters, work counter, status) left over.
+    Every result must match the oracle, and repeating the sequence must give
+    the same bits."""
+    shapes = [(2048, 1024, 384, 1.0), (20000, 1024, 384, 1.0), (4096, 2048, 128, 2.0),
+              (2048, 1024, 384, 0.0), (2048, 1024, 384, 1.0)]
+    cfgs = [_custom(f"ws-{i}", configs.BF16, d_out, d_in, r, s) for i, (d_out, d_in, r, s)
+            in enumerate(shapes)]
+    xs = [gen.norm_inputs(c) for c in cfgs]
+    size = max(api.workspace_size(d_out, d_in, r, torch.bfloat16) for d_out, d_in, r, _ in shapes)
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+    gen_t = torch.Generator(device="cuda")
+    gen_t.manual_seed(11)
+    ws.copy_(torch.randint(0, 256, (size,), dtype=torch.uint8, device="cuda", generator=gen_t))
+    first = []
+    for rep in range(2):
+        for i, (cfg, x) in enumerate(zip(cfgs, xs)):
+            dev = {k: to_dev(x[k], cfg.dtype) for k in ("W", "A", "B", "m")}
+            wn, g = api.dora_factored_norm(dev["W"], dev["A"], dev["B"], cfg.s, dev["m"],
+                                           cfg.eps, workspace=ws)
+            assert api.dora_check_status(ws) == 0
+            wn, g = wn.cpu().numpy(), g.cpu().numpy()
+            if rep == 0:
+                rows = np.arange(cfg.module.d_out)
+                if cfg.module.d_out > 4096:
+                    rows = np.sort(np.random.default_rng(i).choice(cfg.module.d_out, 512, False))
+                wn_ref, g_ref = _oracle(x, cfg, rows=rows)
+                _check(cfg, wn[rows], g[rows], wn_ref, g_ref)
+                first.append((wn, g))
+            else:
+                np.testing.assert_array_equal(wn, first[i][0])
+                np.testing.assert_array_equal(g, first[i][1])
