@@ -242,7 +242,12 @@ __device__ __forceinline__ void record_timeout(int* status) {
 // The n-th work item of this CTA pair (-1: no more work), as published in the
 // ring; the reader releases the slot on the even CTA's `item_empty`.
 __device__ __forceinline__ int read_item(uint32_t n, uint64_t* item_full, const volatile int* item_slot,
-                                         uint32_t item_empty0, uint64_t deadline, int* status) {
+                                         uint32_t item_empty0, uint64_t deadline, int* status,
+                                         bool by_index) {
+  // piece table: every role of both CTAs knows the pair's one piece (its
+  // cluster index) without the ring, so no role waits for a publication
+  // across the pair at the start
+  if (by_index) return n == 0 ? static_cast<int>(blockIdx.x >> 1) : -1;
   const uint32_t slot = n % kItemRing;
   if (!mbar_wait_cluster(&item_full[slot], (n / kItemRing) & 1u, deadline)) {
     record_timeout(status);
@@ -292,6 +297,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const ModView single = single_view(p, &tW, &tA, &tB, &tGhi, &tGlo);
   const uint32_t item_empty0 = map_to_rank(smem_u32(item_empty), 0);
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+  // piece table: pair c runs piece c and nothing else (the table lists the
+  // long pieces first, and clusters start in index order, so the pairs
+  // behind the Gram kernel get the short ones): no claim on the counter, and
+  // no item ring -- every role derives the item from the cluster index
+  const bool by_index = !kGrouped && p.n_tab > 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -344,10 +354,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       bool g_ready = false;      // G'_hi / G'_lo written by the preceding kernel
       const uint32_t slot1 = map_to_rank(smem_u32(const_cast<int*>(item_slot)), 1);
       const uint32_t full1 = map_to_rank(smem_u32(item_full), 1);
-      // piece table: pair c runs piece c and nothing else (the table lists the
-      // long pieces first, and clusters start in index order, so the pairs
-      // behind the Gram kernel get the short ones); no claim on the counter
-      const bool by_index = !kGrouped && p.n_tab > 0;
       int claimed = rank != 0 ? 0 : by_index ? static_cast<int>(blockIdx.x >> 1) : atomicAdd(p.work_ctr, 1);
       // static ranges: this pair's slot is its place in the start order; its
       // pieces are issued from the last to the first, so a pair's first piece
@@ -359,7 +365,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
       for (uint32_t n = 0; !stop; ++n) {
         int item;
-        if (rank == 0) {
+        if (by_index) {
+          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, true);
+        } else if (rank == 0) {
           // publish the claimed item (or the end) to both CTAs
           const uint32_t slot = n % kItemRing;
           if (n >= kItemRing &&
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           mbar_arrive(&item_full[slot]);
           mbar_arrive_cluster(full1 + slot * 8u);
         } else {
-          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
+          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, by_index);
         }
         if (item < 0) break;
         const ModView mv = view_of<kGrouped>(p, single, mod_begin, item);
@@ -467,7 +475,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       int icount = 0;
       bool stop = false;
       for (uint32_t n = 0; !stop; ++n, ++icount) {
-        const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
+        const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, by_index);
         if (item < 0) break;
         int tile, split, kb, ke, nsplit;
         item_range<kGrouped>(p, view_of<kGrouped>(p, single, mod_begin, item), item, tile, split, kb, ke,
@@ -553,7 +561,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     int icount = 0;
     for (uint32_t n = 0;; ++n, ++icount) {
       int item = -1;
-      if (alive && lane == 0) item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status);
+      if (alive && lane == 0) item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, by_index);
       item = __shfl_sync(0xFFFFFFFFu, item, 0);
       {
         // the 8 warps read the same item sequence; decide together anyway, as
