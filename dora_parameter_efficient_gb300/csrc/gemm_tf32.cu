@@ -454,7 +454,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   }
 }
 
-// G' = scale * (sum of the K-segment partials in segment order), zero padded
+// G' = scale * (sum of the K-segment partials in segment order), zero padded.
+// kVec: four neighbouring columns per thread with 16-byte loads and stores
+// (r and rp multiples of 4, both arrays 16-byte aligned); the same sums.
+template <bool kVec>
 __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, int r, int rp,
                                    float scale, float* __restrict__ Gp) {
   // a programmatic dependent of the Gram pass: the norm pass behind it may
@@ -462,28 +465,49 @@ __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, 
   // start once the Gram's partials are complete
   griddep_launch_dependents();
   griddep_wait();
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  constexpr int kW = kVec ? 4 : 1;
+  const int64_t idx = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kW;
   if (idx >= static_cast<int64_t>(rp) * rp) return;
   const int i = static_cast<int>(idx / rp);
   const int j = static_cast<int>(idx - static_cast<int64_t>(i) * rp);
-  float out = 0.f;
+  float out[kW];
+#pragma unroll
+  for (int c = 0; c < kW; ++c) out[c] = 0.f;
   if (i < r && j < r) {
-    // all loads first (they are independent), then the sum in segment order
-    float v[kTf32MaxGramSplits];
+    // all loads first (they are independent), then the sums in segment order
+    float v[kTf32MaxGramSplits][kW];
     const size_t plane = static_cast<size_t>(r) * r;
     const float* src = parts + static_cast<size_t>(i) * r + j;
 #pragma unroll
-    for (int sp = 0; sp < kTf32MaxGramSplits; ++sp) v[sp] = sp < splits ? __ldg(src + sp * plane) : 0.f;
-    df acc{0.f, 0.f};
-#pragma unroll
     for (int sp = 0; sp < kTf32MaxGramSplits; ++sp) {
-      float e;
-      two_sum(acc.hi, v[sp], acc.hi, e);
-      acc.lo = __fadd_rn(acc.lo, e);
+      if constexpr (kVec) {
+        const float4 t = sp < splits ? __ldg(reinterpret_cast<const float4*>(src + sp * plane))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[sp][0] = t.x;
+        v[sp][1] = t.y;
+        v[sp][2] = t.z;
+        v[sp][3] = t.w;
+      } else {
+        v[sp][0] = sp < splits ? __ldg(src + sp * plane) : 0.f;
+      }
     }
-    out = __fmul_rn(scale, __fadd_rn(acc.hi, acc.lo));
+#pragma unroll
+    for (int c = 0; c < kW; ++c) {
+      df acc{0.f, 0.f};
+#pragma unroll
+      for (int sp = 0; sp < kTf32MaxGramSplits; ++sp) {
+        float e;
+        two_sum(acc.hi, v[sp][c], acc.hi, e);
+        acc.lo = __fadd_rn(acc.lo, e);
+      }
+      out[c] = __fmul_rn(scale, __fadd_rn(acc.hi, acc.lo));
+    }
   }
-  Gp[idx] = out;
+  if constexpr (kVec) {
+    *reinterpret_cast<float4*>(Gp + idx) = make_float4(out[0], out[1], out[2], out[3]);
+  } else {
+    Gp[idx] = out[0];
+  }
 }
 
 }  // namespace
@@ -562,7 +586,9 @@ cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const
 
 cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int rp, float scale,
                                     float* Gp, cudaStream_t stream) {
-  const int64_t n = static_cast<int64_t>(rp) * rp;
+  const bool vec = r % 4 == 0 && rp % 4 == 0 && (reinterpret_cast<uintptr_t>(parts) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(Gp) & 15u) == 0;
+  const int64_t n = static_cast<int64_t>(rp) * rp / (vec ? 4 : 1);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
@@ -572,7 +598,9 @@ cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int r
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce, parts, splits, r, rp, scale, Gp);
+  const cudaError_t e =
+      vec ? cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce<true>, parts, splits, r, rp, scale, Gp)
+          : cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce<false>, parts, splits, r, rp, scale, Gp);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
