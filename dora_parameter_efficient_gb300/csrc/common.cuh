@@ -257,7 +257,7 @@ cudaError_t launch_gemm_pair_grouped(const PairParams& p, int clusters, cudaStre
 // of one work item, every product as x_hi y_hi + x_lo y_hi + x_hi y_lo.
 // Work items (pair tile, N pass, K segment) are striped over the grid.
 constexpr int kTf32BlockK = 32;               // fp32 elements per 128-byte smem row
-constexpr int kTf32MaxGramSplits = 16;        // K segments of the fp32 Gram (workspace)
+constexpr int kTf32MaxGramSplits = 24;        // K segments of the fp32 Gram (workspace)
 
 struct Tf32Params {
   int rows;              // rows of X: d_out (norm) or r (Gram)
@@ -266,7 +266,7 @@ struct Tf32Params {
   int kt_x;              // K tiles of (X, Y)
   int kt_b;              // K tiles of (B, G') that follow them (norm); 0 for the Gram
   int splits;            // K segments
-  int seg_k[17];         // segment s covers K tiles [seg_k[s], seg_k[s + 1]), none empty
+  int seg_k[kTf32MaxGramSplits + 1];   // segment s covers K tiles [seg_k[s], seg_k[s + 1]), none empty
   int pair_tiles;        // ceil(rows / 256)
   int n_items;           // pair_tiles * passes * splits
   int stages;
@@ -278,6 +278,12 @@ struct Tf32Params {
   float* out_dot;        // [passes * splits][rows], part pass * splits + split
   // Gram
   float* out_g;          // [splits][rows][r] partial G
+  // blocks (pair tile, N pass) computed, n_units of them (0: all); G is
+  // symmetric, so those strictly below the block diagonal are left out
+  int n_units;
+  int unit_tile[4], unit_pass[4];
+  int* zero_p;           // control words this launch zeroes first (heading a norm), or null
+  int zero_n;
   int* status;
   unsigned long long timeout_ns;
 };
@@ -290,9 +296,11 @@ cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const
                              const CUtensorMap& tYb, const Tf32Params& p, bool store,
                              int clusters, cudaStream_t stream);
 // G' [rp x rp] = scale * (sum over the splits of the partials, in split order); zero
-// outside [r x r]
+// outside [r x r].  sym: the partials hold only the blocks (256-row tile, n_pass-column
+// pass) on or above the block diagonal; the others are written as mirror images.
 cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int rp, float scale,
-                                    float* Gp, cudaStream_t stream);
+                                    float* Gp, cudaStream_t stream, int n_pass = 0,
+                                    int sym = 0);
 
 // ------------------------------------------------------------------ small kernels
 // zeroes n ints at p (a norm workspace's control block); the next kernel may

@@ -30,6 +30,7 @@ constexpr int kGramCluster = DORA_GRAM_CLUSTER;   // CTAs (K splits) per Gram bl
 constexpr int kGramClusterGrouped = 2;            // the same for a grouped launch
 constexpr int kGramStages = 6;
 static_assert(kMaxMainSplits <= kMaxFinalParts, "the fused finalize sums at most kMaxFinalParts splits");
+static_assert(kMaxFinalParts <= kTf32MaxGramSplits, "the 3xTF32 segment table holds every split");
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;   // 2 s per pipeline wait
 
@@ -683,9 +684,11 @@ int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, in
 }
 
 // The fp32 (3xTF32) tensor-core path of the norm, in the modes of
-// run_bf16_pass.  kPassFull: G = A A^T in K segments, their sum scaled to
-// G' = (s/2) G, then the pair pass over (W, A) and (B, G') tiles in N passes
-// of up to 256 columns; the finalize kernel adds the partials.  kPassSlice:
+// run_bf16_pass.  kPassFull: G = A A^T in K segments (the blocks on or above
+// the block diagonal; the first CTA zeroes the control words when zero_words
+// is set), their sum scaled to G' = (s/2) G, then the pair pass over (W, A)
+// and (B, G') tiles in N passes of up to 256 columns; the finalize kernel
+// adds the partials.  kPassSlice:
 // the Gram's segments summed unscaled into part_out + 2 d_out, the pass over
 // the W tiles only, the sums of its partials written to part_out.
 // kPassFinal: G' = (s/2) G from part_in + 2 d_out, the pass over the (B, G')
@@ -693,7 +696,8 @@ int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, in
 int run_f32_pass(const void* W, const void* A, const void* B, int64_t d_out, int64_t d_in,
                  int64_t r, float s, const void* m, float eps, float* wnorm, float* g,
                  const Plan& plan, uint8_t* ws, int mode, float* part_out,
-                 const float* part_in, cudaStream_t stream, void* ev_begin, void* ev_end) {
+                 const float* part_in, cudaStream_t stream, void* ev_begin, void* ev_end,
+                 bool zero_words = false) {
   int* status = reinterpret_cast<int*>(ws + plan.off_status);
   float* G = reinterpret_cast<float*>(ws + plan.off_G);
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
@@ -740,19 +744,35 @@ int run_f32_pass(const void* W, const void* A, const void* B, int64_t d_out, int
     pg.kt_b = 0;
     pg.pair_tiles = static_cast<int>(ceil_div(r, 2 * kTcBlockM));
     {
-      const int units = pg.pair_tiles * passes;
-      int sp = static_cast<int>(ceil_div(clusters_max, units));
+      // G is symmetric: the blocks (256-row tile t, N pass q) whose columns
+      // all lie left of the tile's first row are mirror images of computed
+      // ones (8192 x 8192, r = 512: three of the four)
+      int units = 0;
+      for (int t = 0; t < pg.pair_tiles; ++t)
+        for (int q = 0; q < passes; ++q)
+          if ((q + 1) * n_pass > 2 * kTcBlockM * t) {
+            pg.unit_tile[units] = t;
+            pg.unit_pass[units] = q;
+            ++units;
+          }
+      pg.n_units = units;
+      // one item per CTA pair: as many K segments as fill the grid once
+      int sp = clusters_max / units;
       if (sp > kTf32MaxGramSplits) sp = kTf32MaxGramSplits;
       if (sp > kt_x) sp = kt_x;
       if (sp < 1) sp = 1;
       pg.splits = sp;
       for (int i = 0; i <= sp; ++i) pg.seg_k[i] = static_cast<int>((static_cast<int64_t>(kt_x) * i) / sp);
     }
-    pg.n_items = pg.pair_tiles * passes * pg.splits;
+    pg.n_items = pg.n_units * pg.splits;
     pg.stages = tf32_pick_stages(n_pass);
     pg.acc_stride = acc_stride;
     pg.r = static_cast<int>(r);
     pg.out_g = Gpart;
+    if (zero_words && mode == kPassFull) {
+      pg.zero_p = status;
+      pg.zero_n = static_cast<int>(plan.zero_bytes / 4);
+    }
     pg.status = status;
     pg.timeout_ns = kDefaultTimeoutNs;
     DORA_TRY(launch_gemm_tf32(mA_x, mA_y, mA_x, mA_y, pg, true,
@@ -760,10 +780,10 @@ int run_f32_pass(const void* W, const void* A, const void* B, int64_t d_out, int
     if (mode == kPassSlice) {
       // G of this slice, [r x r] unscaled and unpadded
       DORA_TRY(launch_gram_tf32_reduce(Gpart, pg.splits, static_cast<int>(r), static_cast<int>(r),
-                                       1.f, part_out + 2 * d_out, stream));
+                                       1.f, part_out + 2 * d_out, stream, n_pass, 1));
     } else {
       DORA_TRY(launch_gram_tf32_reduce(Gpart, pg.splits, static_cast<int>(r), rp, 0.5f * s, G,
-                                       stream));
+                                       stream, n_pass, 1));
     }
   }
   if (d_out == 0) return DORA_OK;
@@ -845,9 +865,9 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
   float* pbase = reinterpret_cast<float*>(ws + plan.off_pbase);
   float* pcross = reinterpret_cast<float*>(ws + plan.off_pcross);
 
-  // the bf16 tensor-core pass zeroes the control words itself (in its Gram
-  // kernel when it can), every other path with the zeroing kernel here
-  if (!(adapter && bf16 && d_in > 0))
+  // the tensor-core passes zero the control words themselves (in their Gram
+  // kernel when they can), every other path with the zeroing kernel here
+  if (!(adapter && d_in > 0))
     DORA_TRY(launch_zero_words(status, static_cast<int>(plan.zero_bytes / 4), stream));
 
   int n_base = 0;
@@ -864,7 +884,7 @@ int factored_norm_impl(const void* W, const void* A, const void* B, int dtype, i
                          nullptr, nullptr, stream, ev_begin, ev_end, /*zero_words=*/true);
   } else {
     return run_f32_pass(W, A, B, d_out, d_in, r, s, m, eps, wnorm, g, plan, ws, kPassFull,
-                        nullptr, nullptr, stream, ev_begin, ev_end);
+                        nullptr, nullptr, stream, ev_begin, ev_end, /*zero_words=*/true);
   }
   DORA_TRY(launch_finalize(d_out, pbase, n_base, pcross, 0, nullptr, 0, s, m, bf16, eps, wnorm,
                            g, stream));

@@ -24,7 +24,9 @@
 //     0 also write the segment's sum of squares.  A separate finalize adds
 //     the partials in a fixed order;
 //   * Gram: D = A A^T over the item's K range, stored as an fp32 partial; a
-//     reduce kernel adds the segments in order and scales by s/2.
+//     reduce kernel adds the segments in order and scales by s/2.  G is
+//     symmetric: only the (256-row tile, N pass) blocks on or above the block
+//     diagonal are computed, and the reduce writes the others as mirror images.
 //
 // Tiling for sm_103a: CTA pairs (clusters of 2, tcgen05 cta_group::2), M = 256
 // rows of X per pair (128 in each CTA), N = one pass of at most 256 columns
@@ -99,11 +101,19 @@ struct TfItem {
 // work item -> (pair tile, N pass, K segment): segment-major
 __device__ __forceinline__ TfItem tf_item(const Tf32Params& p, int item) {
   TfItem t;
-  const int per_split = p.pair_tiles * p.passes;
-  t.split = item / per_split;
-  const int rem = item - t.split * per_split;
-  t.pass = rem / p.pair_tiles;
-  t.tile = rem - t.pass * p.pair_tiles;
+  if (p.n_units > 0) {
+    // the Gram's blocks on or above the block diagonal
+    t.split = item / p.n_units;
+    const int u = item - t.split * p.n_units;
+    t.tile = p.unit_tile[u];
+    t.pass = p.unit_pass[u];
+  } else {
+    const int per_split = p.pair_tiles * p.passes;
+    t.split = item / per_split;
+    const int rem = item - t.split * per_split;
+    t.pass = rem / p.pair_tiles;
+    t.tile = rem - t.pass * p.pair_tiles;
+  }
   t.kb = p.seg_k[t.split];
   t.ke = p.seg_k[t.split + 1];
   return t;
@@ -154,6 +164,12 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(num_clusters_x());
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+
+  // Heading a norm (a normal launch, so the stream's previous work -- which
+  // may use these words -- has finished): the first CTA zeroes the control
+  // words; the kernels behind this one touch them only after waiting for it.
+  if (kStore && p.zero_n > 0 && blockIdx.x == 0)
+    for (int i = static_cast<int>(threadIdx.x); i < p.zero_n; i += kTfThreads) p.zero_p[i] = 0;
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < nraw; ++s) {
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
 // (r and rp multiples of 4, both arrays 16-byte aligned); the same sums.
 template <bool kVec>
 __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, int r, int rp,
-                                   float scale, float* __restrict__ Gp) {
+                                   float scale, float* __restrict__ Gp, int n_pass, int sym) {
   // a programmatic dependent of the Gram pass: the norm pass behind it may
   // launch now (it waits for this grid before its first G' tile); the sums
   // start once the Gram's partials are complete
@@ -470,10 +486,20 @@ __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, 
   if (idx >= static_cast<int64_t>(rp) * rp) return;
   const int i = static_cast<int>(idx / rp);
   const int j = static_cast<int>(idx - static_cast<int64_t>(i) * rp);
+  // symmetric partials: the block of (row, col) -- 256-row tile, n_pass-column
+  // pass -- lies strictly below the block diagonal when the whole pass is
+  // left of the tile's first row; such an element is the mirror image of one
+  // in a computed block (n_pass is a multiple of 16 and the kW columns are
+  // aligned, so the test is the same for all of them)
+  const bool inside = i < r && j < r;
+  auto below = [&](int row, int col) {
+    return sym != 0 && (col / n_pass + 1) * n_pass <= (row / 256) * 256;
+  };
+  if (inside && below(i, j)) return;     // written by the thread of its mirror image
   float out[kW];
 #pragma unroll
   for (int c = 0; c < kW; ++c) out[c] = 0.f;
-  if (i < r && j < r) {
+  if (inside) {
     // all loads first (they are independent), then the sums in segment order
     float v[kTf32MaxGramSplits][kW];
     const size_t plane = static_cast<size_t>(r) * r;
@@ -507,6 +533,10 @@ __global__ void k_gram_tf32_reduce(const float* __restrict__ parts, int splits, 
     *reinterpret_cast<float4*>(Gp + idx) = make_float4(out[0], out[1], out[2], out[3]);
   } else {
     Gp[idx] = out[0];
+  }
+  if (inside && below(j, i)) {
+#pragma unroll
+    for (int c = 0; c < kW; ++c) Gp[static_cast<int64_t>(j + c) * rp + i] = out[c];
   }
 }
 
@@ -585,7 +615,8 @@ cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const
 }
 
 cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int rp, float scale,
-                                    float* Gp, cudaStream_t stream) {
+                                    float* Gp, cudaStream_t stream, int n_pass, int sym) {
+  if (sym && (n_pass <= 0 || n_pass % 16 != 0)) return cudaErrorInvalidValue;
   const bool vec = r % 4 == 0 && rp % 4 == 0 && (reinterpret_cast<uintptr_t>(parts) & 15u) == 0 &&
                    (reinterpret_cast<uintptr_t>(Gp) & 15u) == 0;
   const int64_t n = static_cast<int64_t>(rp) * rp / (vec ? 4 : 1);
@@ -599,8 +630,10 @@ cudaError_t launch_gram_tf32_reduce(const float* parts, int splits, int r, int r
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const cudaError_t e =
-      vec ? cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce<true>, parts, splits, r, rp, scale, Gp)
-          : cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce<false>, parts, splits, r, rp, scale, Gp);
+      vec ? cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce<true>, parts, splits, r, rp, scale, Gp,
+                               n_pass, sym)
+          : cudaLaunchKernelEx(&cfg, k_gram_tf32_reduce<false>, parts, splits, r, rp, scale, Gp,
+                               n_pass, sym);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
