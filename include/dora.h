@@ -72,9 +72,9 @@ typedef enum dora_dtype {
  * main pass's work counter and per-row-group completion counters, zeroed by
  * every call), the scaled Gram matrix G' = (s/2) A A^T -- as a bf16 split
  * G'_hi + G'_lo for bf16 inputs; in fp32, with the K-segment partials of
- * A A^T (up to 16 x r x r), for fp32 inputs -- and per-segment partial sums
+ * A A^T (up to 24 x r x r), for fp32 inputs -- and per-segment partial sums
  * of the norm terms.  It does not depend on d_in: about 1.6 MB at
- * d_out = 8192, r = 384 (bf16) and 18.9 MB at d_out = 8192, r = 512 (fp32).
+ * d_out = 8192, r = 384 (bf16) and 27.3 MB at d_out = 8192, r = 512 (fp32).
  * Returns 0 for an invalid shape (negative sizes, bad dtype, r > DORA_MAX_RANK).
  */
 size_t dora_norm_workspace_size(int64_t d_out, int64_t d_in, int64_t r, int dtype);
@@ -141,7 +141,7 @@ int dora_factored_norm_timed(const void* W, const void* A, const void* B, int dt
  * (a file-scope __device__ array): every GPU that loads the library holds it
  * until the process exits.  32 MiB covers d_out up to 253 888 rows at
  * r = 512 (257 468 at r = 384, 261 564 at r = 128) for bf16 inputs and
- * 122 848 rows at r = 512 (183 760 at r = 384, 253 376 at r = 128) for fp32
+ * 57 328 rows at r = 512 (146 904 at r = 384, 249 280 at r = 128) for fp32
  * inputs; a shape whose
  * dora_norm_workspace_size exceeds 32 MiB is refused with DORA_ERR_WORKSPACE
  * before anything is enqueued.
