@@ -203,6 +203,24 @@ __device__ __forceinline__ void item_range(const PairParams& p, const ModView& m
                 nsplit);
 }
 
+// The completion counter of a 128-row group, incremented with acquire-release
+// semantics at GPU scope by one thread after a barrier of the epilogue warps:
+// the release publishes every epilogue thread's partial stores (they precede
+// the barrier), the acquire orders the last segment's reads of the other
+// segments' partials (after the next barrier) behind the other segments'
+// releases.  No thread needs a fence of its own.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// global fp32 load that bypasses L1 (data written by other CTAs of this grid)
+__device__ __forceinline__ float ld_cg_f(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per tensor-memory lane quadrant)
 constexpr int kPairThreads = 320;

@@ -253,26 +253,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
-// ------------------------------------------------------------------ completion counters
-// The completion counter of a 128-row group, incremented with acquire-release
-// semantics at GPU scope by one thread after a named barrier of the warps that
-// wrote partials: the release publishes every such thread's partial stores
-// (they precede the barrier), the acquire orders the last contribution's reads
-// of the other contributions' partials (after the next barrier) behind their
-// releases.  No thread needs a fence of its own.
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
-  int old;
-  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-// global fp32 load that bypasses L1 (data written by other CTAs of this grid)
-__device__ __forceinline__ float ld_cg_f(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // 128 consecutive fp32 columns of this thread's TMEM lane (32x32b shape, x128),
 // waited on before returning: one wait for the whole batch.
 __device__ __forceinline__ void tmem_load_128cols(uint32_t taddr, float (&v)[128]) {
