@@ -659,9 +659,9 @@ def run_ours(args):
     main_src = os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "gemm_pair.cu")
     comp_src = os.path.join(ROOT, "dora_parameter_efficient_gb300", "csrc", "compose.cu")
     # the dominant kernel's duration: the period of back-to-back norm calls.
-    # Successive main passes never overlap (the next norm's zeroing kernel
-    # waits for this grid to complete before the next Gram and main pass
-    # start), so the period bounds the kernel's duration from above and the
+    # Successive main passes never overlap (the next norm's Gram kernel, which
+    # zeroes the control words, waits for this grid to complete before the
+    # next main pass starts), so the period bounds the kernel's duration from above and the
     # rate below; the isolated figure times the same kernel with events right
     # around its launch, which removes the overlap with the Gram kernel it is
     # scheduled for and adds a launch.
@@ -680,9 +680,9 @@ def run_ours(args):
                 "frac_of_nominal": main_tflops_chain / NOMINAL["bf16_tflops"],
                 "flops_per_launch": mflops, "ms_per_launch": chain_ms,
                 "timing": f"upper bound of the kernel's duration: the period of {b2b_n} "
-                          f"back-to-back norm calls over the rotating sets (zeroing kernel -> "
-                          f"Gram -> main pass, a programmatic chain; one CUDA event pair on the "
-                          f"launching stream around the loop, none between launches); "
+                          f"back-to-back norm calls over the rotating sets (Gram -> main pass, a "
+                          f"programmatic chain, the Gram kernel zeroing the control words; one "
+                          f"CUDA event pair on the launching stream around the loop, none between launches); "
                           f"successive main passes do not overlap, so the period includes the "
                           f"kernel's whole duration plus the gap to the next one",
                 "isolated": {"ms_per_launch": main_ms_m, "achieved": main_tflops,
