@@ -37,8 +37,10 @@
 //   * warp 0 loads its X tile and its half of the Y tile (TMA) into a raw
 //     slot and counts the bytes on its own `raw_full` barrier;
 //   * warps 2-17 read the raw slot, write x_lo and y_lo into a split slot,
-//     take the sum of squares of X when it is a W tile, fence their writes
-//     for the async proxy and arrive on the even CTA's `sp_ready` barrier;
+//     take the sum of squares of X when it is a W tile and fence their
+//     writes for the async proxy; above N = 128, once all sixteen have (a
+//     named barrier), one of them arrives on the even CTA's `sp_ready`
+//     barrier, otherwise each arrives;
 //   * warp 1 of the even CTA issues the 12 MMAs of the stage (4 K steps x 3
 //     terms, reading hi from the raw slot and lo from the split slot) and
 //     commits `raw_empty` and `sp_empty` to both CTAs, which frees both;
@@ -85,6 +87,15 @@ __device__ __forceinline__ void sts4(uint32_t addr, float4 v) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
                "f"(v.z), "f"(v.w)
                : "memory");
+}
+
+// x^2 + y^2 + z^2 + w^2 of one 16-byte chunk, in that order (one rounding
+// per step, as the row sums of squares elsewhere)
+__device__ __forceinline__ float sumsq4(const float4 v) {
+  float sq4 = __fmul_rn(v.x, v.x);
+  sq4 = fmaf(v.y, v.y, sq4);
+  sq4 = fmaf(v.z, v.z, sq4);
+  return fmaf(v.w, v.w, sq4);
 }
 
 // lo = v - trunc_tf32(v), the part of v the tensor core does not read; the
@@ -136,7 +147,7 @@ __device__ __forceinline__ float dot_b32(const float* brow, int col0, int r, boo
   return acc;
 }
 
-template <bool kStore>
+template <bool kStore, bool kGroupedArrive>
 __global__ void __launch_bounds__(kTfThreads, 1)
     k_gemm_tf32(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tY,
                 const __grid_constant__ CUtensorMap tXb, const __grid_constant__ CUtensorMap tYb,
@@ -164,6 +175,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(num_clusters_x());
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
+  // kGroupedArrive (N > 128): the split warps of a CTA meet at a named
+  // barrier and one of them signals the stage (one cluster-scope arrive per
+  // CTA); at N <= 128 each warp arrives itself (measured faster there)
+  constexpr bool grouped_arrive = kGroupedArrive;
 
   // Heading a norm (a normal launch, so the stream's previous work -- which
   // may use these words -- has finished): the first CTA zeroes the control
@@ -177,7 +192,8 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       mbar_init(&raw_empty[s], 1);               // the MMAs that read it are done
     }
     for (uint32_t s = 0; s < kTfSplitSlots; ++s) {
-      mbar_init(&sp_ready[s], 2 * kTfSplitWarps);   // the split warps of both CTAs
+      // one arrive per CTA after all its split warps, or one per split warp
+      mbar_init(&sp_ready[s], grouped_arrive ? 2 : 2 * kTfSplitWarps);
       mbar_init(&sp_empty[s], 1);                   // the MMAs that read it are done
     }
     for (int b = 0; b < 2; ++b) {
@@ -349,34 +365,67 @@ __global__ void __launch_bounds__(kTfThreads, 1)
           const uint32_t xa = smem0 + s * raw_bytes;
           const uint32_t xd = sp0 + q * sp_bytes;
           const bool sq = do_sq && kt < p.kt_x;
-#pragma unroll
-          for (int i = 0; i < kTfSplitIters; ++i) {
-            const uint32_t off =
-                static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
-            const float4 v = lds4(xa + off);
-            if (sq) {
-              float sq4 = __fmul_rn(v.x, v.x);
-              sq4 = fmaf(v.y, v.y, sq4);
-              sq4 = fmaf(v.z, v.z, sq4);
-              sq4 = fmaf(v.w, v.w, sq4);
-              kahan_add(sacc[i], scmp[i], sq4);
-            }
-            sts4(xd + off, tf32_lo4(v));
-          }
           const uint32_t ya = xa + kTfXBytes;
           const uint32_t yd = xd + kTfXBytes;
+          if constexpr (grouped_arrive) {
+            // every load of the stage first, then the stores: the loads are
+            // independent, so the warp waits out one shared-memory round
+            // trip (slow while the tensor core streams its operands) instead
+            // of one per load (at N <= 128 the load-store order measured
+            // faster)
+            float4 vx[kTfSplitIters], vy[kTfSplitIters];
 #pragma unroll
-          for (int i = 0; i < kTfSplitIters; ++i) {
-            const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
-            if (row < yr) {
-              const uint32_t off = row * 128u + static_cast<uint32_t>(chunk * 16);
-              sts4(yd + off, tf32_lo4(lds4(ya + off)));
+            for (int i = 0; i < kTfSplitIters; ++i)
+              vx[i] = lds4(xa + static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16));
+#pragma unroll
+            for (int i = 0; i < kTfSplitIters; ++i) {
+              const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
+              if (row < yr) vy[i] = lds4(ya + row * 128u + static_cast<uint32_t>(chunk * 16));
+            }
+#pragma unroll
+            for (int i = 0; i < kTfSplitIters; ++i) {
+              const uint32_t off =
+                  static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
+              if (sq) kahan_add(sacc[i], scmp[i], sumsq4(vx[i]));
+              sts4(xd + off, tf32_lo4(vx[i]));
+            }
+#pragma unroll
+            for (int i = 0; i < kTfSplitIters; ++i) {
+              const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
+              if (row < yr) sts4(yd + row * 128u + static_cast<uint32_t>(chunk * 16), tf32_lo4(vy[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < kTfSplitIters; ++i) {
+              const uint32_t off =
+                  static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
+              const float4 v = lds4(xa + off);
+              if (sq) kahan_add(sacc[i], scmp[i], sumsq4(v));
+              sts4(xd + off, tf32_lo4(v));
+            }
+#pragma unroll
+            for (int i = 0; i < kTfSplitIters; ++i) {
+              const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
+              if (row < yr) {
+                const uint32_t off = row * 128u + static_cast<uint32_t>(chunk * 16);
+                sts4(yd + off, tf32_lo4(lds4(ya + off)));
+              }
             }
           }
           fence_async_smem_writes();
         }
         __syncwarp();
-        if (alive && lane == 0) mbar_arrive_cluster(ready0 + q * 8u);
+        if constexpr (grouped_arrive) {
+          // all split warps of this CTA have written (and fenced) their
+          // part: one cluster-scope arrive per CTA, by each warp in turn (a
+          // release per warp cost each warp about 0.7 us per stage, which
+          // paced the MMAs at N = 256)
+          asm volatile("bar.sync 1, %0;" ::"n"(kTfSplitWarps * 32) : "memory");
+          if (w == static_cast<int>(it % kTfSplitWarps) && alive && lane == 0)
+            mbar_arrive_cluster(ready0 + q * 8u);
+        } else if (alive && lane == 0) {
+          mbar_arrive_cluster(ready0 + q * 8u);
+        }
         if (++s == nraw) {
           s = 0;
           phase ^= 1u;
@@ -578,11 +627,12 @@ int tf32_max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaFuncSetAttribute(k_gemm_tf32<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(k_gemm_tf32<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kMaxSmem) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, k_gemm_tf32<false>, &cfg) != cudaSuccess)
+  for (auto fn : {k_gemm_tf32<false, false>, k_gemm_tf32<false, true>, k_gemm_tf32<true, false>,
+                  k_gemm_tf32<true, true>})
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+        cudaSuccess)
+      return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tf32<false, true>, &cfg) != cudaSuccess)
     return 0;
   if (dev < 64) cached[dev] = n;
   return n;
@@ -607,8 +657,14 @@ cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = store ? 1 : 2;
-  cudaError_t e = store ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<true>, tX, tY, tXb, tYb, p)
-                        : cudaLaunchKernelEx(&cfg, k_gemm_tf32<false>, tX, tY, tXb, tYb, p);
+  const bool grouped = p.n_pass > 128;
+  cudaError_t e;
+  if (store)
+    e = grouped ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<true, true>, tX, tY, tXb, tYb, p)
+                : cudaLaunchKernelEx(&cfg, k_gemm_tf32<true, false>, tX, tY, tXb, tYb, p);
+  else
+    e = grouped ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<false, true>, tX, tY, tXb, tYb, p)
+                : cudaLaunchKernelEx(&cfg, k_gemm_tf32<false, false>, tX, tY, tXb, tYb, p);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
