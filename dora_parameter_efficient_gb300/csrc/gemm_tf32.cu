@@ -38,9 +38,11 @@
 //     slot and counts the bytes on its own `raw_full` barrier;
 //   * warps 2-17 read the raw slot, write x_lo and y_lo into a split slot,
 //     take the sum of squares of X when it is a W tile and fence their
-//     writes for the async proxy; above N = 128, once all sixteen have (a
-//     named barrier), one of them arrives on the even CTA's `sp_ready`
-//     barrier, otherwise each arrives;
+//     writes for the async proxy; above N = 128 they hand the stage to
+//     warp 22 through a named barrier (bar.arrive, no wait) and warp 22
+//     makes the one arrive on the even CTA's `sp_ready` barrier (a
+//     cluster-scope release, about 0.7 us, which paced the MMAs when every
+//     split warp made its own), at N <= 128 each split warp arrives itself;
 //   * warp 1 of the even CTA issues the 12 MMAs of the stage (4 K steps x 3
 //     terms, reading hi from the raw slot and lo from the split slot) and
 //     commits `raw_empty` and `sp_empty` to both CTAs, which frees both;
@@ -66,7 +68,7 @@ namespace dora {
 
 namespace {
 
-constexpr int kTfThreads = 704;        // warp 0 TMA, 1 MMA, 2-17 split, 18-21 drain
+constexpr int kTfThreads = 736;        // warp 0 TMA, 1 MMA, 2-17 split, 18-21 drain, 22 signal
 constexpr int kTfSplitWarps = 16;
 constexpr int kTfSplitRows = 128 / kTfSplitWarps;   // tile rows per split warp
 constexpr int kTfSplitIters = kTfSplitRows / 4;     // one warp instruction covers 4 rows
@@ -175,9 +177,10 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(num_clusters_x());
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
-  // kGroupedArrive (N > 128): the split warps of a CTA meet at a named
-  // barrier and one of them signals the stage (one cluster-scope arrive per
-  // CTA); at N <= 128 each warp arrives itself (measured faster there)
+  // kGroupedArrive (N > 128): the split warps of a CTA hand each stage to
+  // the signal warp through named barrier 1 + (split slot), which makes the
+  // stage's one cluster-scope arrive for the CTA; at N <= 128 each split
+  // warp arrives itself (measured faster there)
   constexpr bool grouped_arrive = kGroupedArrive;
 
   // Heading a norm (a normal launch, so the stream's previous work -- which
@@ -416,13 +419,14 @@ __global__ void __launch_bounds__(kTfThreads, 1)
         }
         __syncwarp();
         if constexpr (grouped_arrive) {
-          // all split warps of this CTA have written (and fenced) their
-          // part: one cluster-scope arrive per CTA, by each warp in turn (a
-          // release per warp cost each warp about 0.7 us per stage, which
-          // paced the MMAs at N = 256)
-          asm volatile("bar.sync 1, %0;" ::"n"(kTfSplitWarps * 32) : "memory");
-          if (w == static_cast<int>(it % kTfSplitWarps) && alive && lane == 0)
-            mbar_arrive_cluster(ready0 + q * 8u);
+          // this warp's part is written and fenced: hand the stage to the
+          // signal warp (a split warp runs at most three stages ahead of it:
+          // the split slots; three barriers, one per slot, keep the phases
+          // apart)
+          if (alive)
+            asm volatile("bar.arrive %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
+          else   // a warp whose waits ran out must not run ahead of the signal warp
+            asm volatile("bar.sync %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
         } else if (alive && lane == 0) {
           mbar_arrive_cluster(ready0 + q * 8u);
         }
@@ -447,6 +451,22 @@ __global__ void __launch_bounds__(kTfThreads, 1)
               t.tile * 256 + static_cast<int>(rank) * 128 + kTfSplitRows * w + 4 * i + sub;
           if (alive && chunk == 0 && grow < p.rows)
             p.out_sumsq[static_cast<size_t>(t.split) * p.rows + grow] = v;
+        }
+      }
+    }
+  } else if (warp == 2 + kTfSplitWarps + kTfDrainWarps) {
+    // -------------------------------------------------------------- signal (both CTAs)
+    // once all sixteen split warps of this CTA have handed in a stage, one
+    // cluster-scope arrive on the even CTA's `sp_ready` barrier
+    if constexpr (kGroupedArrive) {
+      const uint32_t ready0 = map_to_rank(smem_u32(sp_ready), 0);
+      uint32_t q = 0;
+      for (int item = cid; item < p.n_items; item += ncl) {
+        const TfItem t = tf_item(p, item);
+        for (int kt = t.kb; kt < t.ke; ++kt) {
+          asm volatile("bar.sync %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
+          if (lane == 0) mbar_arrive_cluster(ready0 + q * 8u);
+          if (++q == kTfSplitSlots) q = 0;
         }
       }
     }
