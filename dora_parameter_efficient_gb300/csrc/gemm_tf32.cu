@@ -38,11 +38,10 @@
 //     slot and counts the bytes on its own `raw_full` barrier;
 //   * warps 2-17 read the raw slot, write x_lo and y_lo into a split slot,
 //     take the sum of squares of X when it is a W tile and fence their
-//     writes for the async proxy; above N = 128 they hand the stage to
-//     warp 22 through a named barrier (bar.arrive, no wait) and warp 22
-//     makes the one arrive on the even CTA's `sp_ready` barrier (a
-//     cluster-scope release, about 0.7 us, which paced the MMAs when every
-//     split warp made its own), at N <= 128 each split warp arrives itself;
+//     writes for the async proxy; they hand the stage to warp 22 through a
+//     named barrier (bar.arrive, no wait) and warp 22 makes the one arrive
+//     on the even CTA's `sp_ready` barrier (a cluster-scope release, about
+//     0.7 us, which paced the MMAs when every split warp made its own);
 //   * warp 1 of the even CTA issues the 12 MMAs of the stage (4 K steps x 3
 //     terms, reading hi from the raw slot and lo from the split slot) and
 //     commits `raw_empty` and `sp_empty` to both CTAs, which frees both;
@@ -149,7 +148,7 @@ __device__ __forceinline__ float dot_b32(const float* brow, int col0, int r, boo
   return acc;
 }
 
-template <bool kStore, bool kGroupedArrive>
+template <bool kStore>
 __global__ void __launch_bounds__(kTfThreads, 1)
     k_gemm_tf32(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tY,
                 const __grid_constant__ CUtensorMap tXb, const __grid_constant__ CUtensorMap tYb,
@@ -177,11 +176,6 @@ __global__ void __launch_bounds__(kTfThreads, 1)
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(num_clusters_x());
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
-  // kGroupedArrive (N > 128): the split warps of a CTA hand each stage to
-  // the signal warp through named barrier 1 + (split slot), which makes the
-  // stage's one cluster-scope arrive for the CTA; at N <= 128 each split
-  // warp arrives itself (measured faster there)
-  constexpr bool grouped_arrive = kGroupedArrive;
 
   // Heading a norm (a normal launch, so the stream's previous work -- which
   // may use these words -- has finished): the first CTA zeroes the control
@@ -195,8 +189,7 @@ __global__ void __launch_bounds__(kTfThreads, 1)
       mbar_init(&raw_empty[s], 1);               // the MMAs that read it are done
     }
     for (uint32_t s = 0; s < kTfSplitSlots; ++s) {
-      // one arrive per CTA after all its split warps, or one per split warp
-      mbar_init(&sp_ready[s], grouped_arrive ? 2 : 2 * kTfSplitWarps);
+      mbar_init(&sp_ready[s], 2);   // the signal warps of both CTAs
       mbar_init(&sp_empty[s], 1);                   // the MMAs that read it are done
     }
     for (int b = 0; b < 2; ++b) {
@@ -343,7 +336,6 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     const int w = warp - 2;
     const int sub = lane >> 3;
     const int chunk = lane & 7;
-    const uint32_t ready0 = map_to_rank(smem_u32(sp_ready), 0);
     const uint32_t sp0 = smem_u32(sp_base);
     uint32_t s = 0, phase = 0;          // raw ring
     uint32_t q = 0, qphase = 0, it = 0; // split ring
@@ -370,66 +362,42 @@ __global__ void __launch_bounds__(kTfThreads, 1)
           const bool sq = do_sq && kt < p.kt_x;
           const uint32_t ya = xa + kTfXBytes;
           const uint32_t yd = xd + kTfXBytes;
-          if constexpr (grouped_arrive) {
-            // every load of the stage first, then the stores: the loads are
-            // independent, so the warp waits out one shared-memory round
-            // trip (slow while the tensor core streams its operands) instead
-            // of one per load (at N <= 128 the load-store order measured
-            // faster)
-            float4 vx[kTfSplitIters], vy[kTfSplitIters];
+          // every load of the stage first, then the stores: the loads are
+          // independent, so the warp waits out one shared-memory round trip
+          // (slow while the tensor core streams its operands) instead of one
+          // per load
+          float4 vx[kTfSplitIters], vy[kTfSplitIters];
 #pragma unroll
-            for (int i = 0; i < kTfSplitIters; ++i)
-              vx[i] = lds4(xa + static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16));
+          for (int i = 0; i < kTfSplitIters; ++i)
+            vx[i] = lds4(xa + static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16));
 #pragma unroll
-            for (int i = 0; i < kTfSplitIters; ++i) {
-              const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
-              if (row < yr) vy[i] = lds4(ya + row * 128u + static_cast<uint32_t>(chunk * 16));
-            }
+          for (int i = 0; i < kTfSplitIters; ++i) {
+            const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
+            if (row < yr) vy[i] = lds4(ya + row * 128u + static_cast<uint32_t>(chunk * 16));
+          }
 #pragma unroll
-            for (int i = 0; i < kTfSplitIters; ++i) {
-              const uint32_t off =
-                  static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
-              if (sq) kahan_add(sacc[i], scmp[i], sumsq4(vx[i]));
-              sts4(xd + off, tf32_lo4(vx[i]));
-            }
+          for (int i = 0; i < kTfSplitIters; ++i) {
+            const uint32_t off =
+                static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
+            if (sq) kahan_add(sacc[i], scmp[i], sumsq4(vx[i]));
+            sts4(xd + off, tf32_lo4(vx[i]));
+          }
 #pragma unroll
-            for (int i = 0; i < kTfSplitIters; ++i) {
-              const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
-              if (row < yr) sts4(yd + row * 128u + static_cast<uint32_t>(chunk * 16), tf32_lo4(vy[i]));
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < kTfSplitIters; ++i) {
-              const uint32_t off =
-                  static_cast<uint32_t>((kTfSplitRows * w + 4 * i + sub) * 128 + chunk * 16);
-              const float4 v = lds4(xa + off);
-              if (sq) kahan_add(sacc[i], scmp[i], sumsq4(v));
-              sts4(xd + off, tf32_lo4(v));
-            }
-#pragma unroll
-            for (int i = 0; i < kTfSplitIters; ++i) {
-              const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
-              if (row < yr) {
-                const uint32_t off = row * 128u + static_cast<uint32_t>(chunk * 16);
-                sts4(yd + off, tf32_lo4(lds4(ya + off)));
-              }
-            }
+          for (int i = 0; i < kTfSplitIters; ++i) {
+            const uint32_t row = static_cast<uint32_t>(kTfSplitRows * w + 4 * i + sub);
+            if (row < yr) sts4(yd + row * 128u + static_cast<uint32_t>(chunk * 16), tf32_lo4(vy[i]));
           }
           fence_async_smem_writes();
         }
         __syncwarp();
-        if constexpr (grouped_arrive) {
-          // this warp's part is written and fenced: hand the stage to the
-          // signal warp (a split warp runs at most three stages ahead of it:
-          // the split slots; three barriers, one per slot, keep the phases
-          // apart)
-          if (alive)
-            asm volatile("bar.arrive %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
-          else   // a warp whose waits ran out must not run ahead of the signal warp
-            asm volatile("bar.sync %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
-        } else if (alive && lane == 0) {
-          mbar_arrive_cluster(ready0 + q * 8u);
-        }
+        // this warp's part is written and fenced: hand the stage to the
+        // signal warp (a split warp runs at most three stages ahead of it:
+        // the split slots; three barriers, one per slot, keep the phases
+        // apart)
+        if (alive)
+          asm volatile("bar.arrive %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
+        else   // a warp whose waits ran out must not run ahead of the signal warp
+          asm volatile("bar.sync %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
         if (++s == nraw) {
           s = 0;
           phase ^= 1u;
@@ -458,16 +426,14 @@ __global__ void __launch_bounds__(kTfThreads, 1)
     // -------------------------------------------------------------- signal (both CTAs)
     // once all sixteen split warps of this CTA have handed in a stage, one
     // cluster-scope arrive on the even CTA's `sp_ready` barrier
-    if constexpr (kGroupedArrive) {
-      const uint32_t ready0 = map_to_rank(smem_u32(sp_ready), 0);
-      uint32_t q = 0;
-      for (int item = cid; item < p.n_items; item += ncl) {
-        const TfItem t = tf_item(p, item);
-        for (int kt = t.kb; kt < t.ke; ++kt) {
-          asm volatile("bar.sync %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
-          if (lane == 0) mbar_arrive_cluster(ready0 + q * 8u);
-          if (++q == kTfSplitSlots) q = 0;
-        }
+    const uint32_t ready0 = map_to_rank(smem_u32(sp_ready), 0);
+    uint32_t q = 0;
+    for (int item = cid; item < p.n_items; item += ncl) {
+      const TfItem t = tf_item(p, item);
+      for (int kt = t.kb; kt < t.ke; ++kt) {
+        asm volatile("bar.sync %0, %1;" ::"r"(1u + q), "n"(kTfSplitWarps * 32 + 32) : "memory");
+        if (lane == 0) mbar_arrive_cluster(ready0 + q * 8u);
+        if (++q == kTfSplitSlots) q = 0;
       }
     }
   } else {
@@ -647,12 +613,11 @@ int tf32_max_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  for (auto fn : {k_gemm_tf32<false, false>, k_gemm_tf32<false, true>, k_gemm_tf32<true, false>,
-                  k_gemm_tf32<true, true>})
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
-        cudaSuccess)
-      return 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tf32<false, true>, &cfg) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_gemm_tf32<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_gemm_tf32<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMaxSmem) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, k_gemm_tf32<false>, &cfg) != cudaSuccess)
     return 0;
   if (dev < 64) cached[dev] = n;
   return n;
@@ -677,14 +642,8 @@ cudaError_t launch_gemm_tf32(const CUtensorMap& tX, const CUtensorMap& tY, const
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = store ? 1 : 2;
-  const bool grouped = p.n_pass > 128;
-  cudaError_t e;
-  if (store)
-    e = grouped ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<true, true>, tX, tY, tXb, tYb, p)
-                : cudaLaunchKernelEx(&cfg, k_gemm_tf32<true, false>, tX, tY, tXb, tYb, p);
-  else
-    e = grouped ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<false, true>, tX, tY, tXb, tYb, p)
-                : cudaLaunchKernelEx(&cfg, k_gemm_tf32<false, false>, tX, tY, tXb, tYb, p);
+  cudaError_t e = store ? cudaLaunchKernelEx(&cfg, k_gemm_tf32<true>, tX, tY, tXb, tYb, p)
+                        : cudaLaunchKernelEx(&cfg, k_gemm_tf32<false>, tX, tY, tXb, tYb, p);
   note_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
