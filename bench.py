@@ -462,7 +462,13 @@ def run_fp32(api, dev, peaks, calls=20):
            "main_pass_us": main_ms * 1e3,
            "main_pass_tf32_TFLOP/s": mma_flops / (main_ms * 1e-3) / 1e12,
            "main_pass_frac_of_measured_derived_tf32": mma_flops / (main_ms * 1e-3) / 1e12 / tf32_peak,
-           "tf32_peak_note": "measured bf16 burst x the nominal tf32 / bf16 ratio (1100 / 2250)",
+           "tf32_peak_note": "measured bf16 burst x the nominal tf32 / bf16 ratio (1100 / 2250); "
+                             "the bf16 figure is cuBLAS's achieved rate, so a kernel may read "
+                             "a little above 1.0 against it",
+           # against the issue rate the tensor counter implies for TF32 (4096
+           # FLOP per clock per SM, half the bf16 rate) at the maximum SM clock
+           "main_pass_frac_of_tf32_issue_rate": mma_flops / (main_ms * 1e-3) / 1e12
+           / (4096 * 152 * 2.07e9 / 1e12),
            # W, A, B, G' once; the segment partials (at most 16 + 16 fp32 per row)
            "main_pass_algorithmic_bytes": 4 * (d_out * d_in + r * d_in + d_out * r + rp * rp),
            "main_pass_traffic": recorded_traffic(
