@@ -51,12 +51,17 @@
 // The split slots are busy only from the split to the MMAs: three of them
 // give the split of the next stages slack against the MMAs and leave the
 // rest of shared memory to raw slots, so the loads run several stages ahead
-// (8192 x 8192, r = 512 on one GB300: 322 us per norm with 3 split + 4 raw
-// slots, 338 with 2 + 5, 343 with 4 + 3).
+// (8192 x 8192, r = 512 on one GB300: 269 us per norm with 3 split + 4 raw
+// slots, 302 with 2 + 5, 297 with 4 + 3, measured with all sixteen split
+// warps meeting at a barrier each stage before the signal warp existed).
 // The grid is persistent and the items are striped over it (cluster c takes
 // items c, c + clusters, ...): they are of equal size, and every role walks
-// the same sequence with no hand-off.  Every wait is bounded by %globaltimer;
-// on expiry the kernel records a timeout in the status word and stops.
+// the same sequence with no hand-off.  Every mbarrier wait is bounded by
+// %globaltimer; on expiry the kernel records a timeout in the status word and
+// stops.  The named barriers between the split warps and the signal warp
+// complete as long as every one of them walks its stages, which they do
+// whether their bounded waits succeed or not (a split warp whose wait ran out
+// syncs instead of arriving, so it cannot run ahead of the signal warp).
 #include <cstring>
 
 #include "common.cuh"
