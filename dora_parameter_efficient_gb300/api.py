@@ -462,7 +462,8 @@ def dora_selftest_schedule(d_out: int, d_in: int, r: int, clusters: int):
     """Host-only check of the main pass's work decomposition for a bf16
     d_out x d_in module at rank r on `clusters` CTA pairs: returns
     (schedule, most_pieces_of_one_tile, defects) with schedule one of
-    SCHEDULE_SEGMENTS, SCHEDULE_RANGES, SCHEDULE_TABLE; defects is 0 when
+    SCHEDULE_SEGMENTS, SCHEDULE_RANGES, SCHEDULE_TABLE, SCHEDULE_WHOLE_TABLE;
+    defects is 0 when
     every pair tile's K range is covered once, in order, by at most 16
     numbered pieces."""
     sc, mp, df = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
@@ -475,6 +476,7 @@ def dora_selftest_schedule(d_out: int, d_in: int, r: int, clusters: int):
 SCHEDULE_SEGMENTS = 0   # K segments handed out one by one
 SCHEDULE_RANGES = 1     # one static range of (pair tile, K tile) iterations per pair
 SCHEDULE_TABLE = 2      # piece table: one K range of one pair tile per pair
+SCHEDULE_WHOLE_TABLE = 3  # whole pair tiles per pair, then a piece table over the rest
 
 
 def dora_selftest_grouped_schedule(shapes, r: int, clusters: int):

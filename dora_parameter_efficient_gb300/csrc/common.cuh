@@ -152,10 +152,13 @@ struct PairParams {
   int ktot;              // K tiles per pair tile: kt_w + 2 * kt_b
   int iters;             // pair_tiles * ktot
   int n_early, len_early, len_late;
-  // piece table (single-module launch, n_tab != 0): work item i is the piece
-  // tab[i] = {tile | split << 16 | nsplit << 24, kb, ke}; used with fewer
-  // pair tiles than pairs, one piece per pair, the long pieces first
+  // piece table (single-module launch, n_tab != 0 or n_whole != 0): pair c
+  // runs n_whole whole pair tiles (c * n_whole ..), then the piece tab[c] =
+  // {tile | split << 16 | nsplit << 24, kb, ke} if c < n_tab; the pieces cut
+  // the tiles after the whole ones, one per pair, the long pieces first
   int n_tab;
+  int n_whole;
+  int n_tab_early;       // host: the table's first n_tab_early pieces are the early ones
   uint32_t tab[kPairTabMax][3];
   // grouped launch: the per-module fields above are unused, these are
   const PairModule* mods;
@@ -206,9 +209,28 @@ __host__ __device__ inline int64_t range_next(const PairParams& p, int64_t lo, i
   return cur;
 }
 
+// Piece table: the n-th work item of pair c (its whole tiles first, then its
+// piece), or -1.  A whole tile is an item with kWholeItem set.
+constexpr int kWholeItem = 1 << 30;
+__host__ __device__ inline bool table_mode(const PairParams& p) { return p.n_tab > 0 || p.n_whole > 0; }
+constexpr uint32_t kNoPiece = 0xFFFFFFFFu;     // a table entry of a pair without a piece
+__host__ __device__ inline int table_item(const PairParams& p, int c, int n) {
+  if (n < p.n_whole) return kWholeItem | (c * p.n_whole + n);
+  if (n == p.n_whole && c < p.n_tab && p.tab[c][0] != kNoPiece) return c;
+  return -1;
+}
+
 // Piece table: work item -> its piece.
 __host__ __device__ inline void table_piece(const PairParams& p, int item, int& tile, int& split,
                                             int& kb, int& ke, int& nsplit) {
+  if (item & kWholeItem) {
+    tile = item & (kWholeItem - 1);
+    split = 0;
+    nsplit = 1;
+    kb = 0;
+    ke = p.kt_w + 2 * p.kt_b;
+    return;
+  }
   const uint32_t w = p.tab[item][0];
   tile = static_cast<int>(w & 0xFFFFu);
   split = static_cast<int>((w >> 16) & 0xFFu);

@@ -323,20 +323,27 @@ struct PieceKey {
 struct PieceEntry {
   PieceKey key;
   bool ok;
-  int n_tab;
+  int n_tab, n_tab_early;
   uint32_t tab[kPairTabMax][3];
 };
 std::mutex g_piece_mu;
 PieceEntry g_piece_cache[16];
 int g_piece_used = 0, g_piece_next = 0;
 
-bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64_t lag);
+bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64_t lag, int64_t T);
 
-bool plan_pair_pieces(PairParams& pp, int clusters, int64_t late, int64_t lag) {
+// T tiles (the pass's own, or the ones left after whole tiles), numbered
+// from tile_offset in the table.
+bool plan_pair_pieces(PairParams& pp, int clusters, int64_t late, int64_t lag, int64_t T,
+                      int64_t tile_offset) {
   pp.n_tab = 0;
-  const int64_t T = pp.pair_tiles;
   const int64_t K = pp.kt_w + 2 * static_cast<int64_t>(pp.kt_b);
-  if (!DORA_PIECE_TABLE || T <= 0 || K <= 0 || T >= clusters || clusters > kPairTabMax) return false;
+  if (!DORA_PIECE_TABLE || T <= 0 || K <= 0 || T >= clusters || clusters > kPairTabMax ||
+      tile_offset + T > 0xFFFF)
+    return false;
+  auto shift = [&]() {
+    for (int i = 0; i < pp.n_tab; ++i) pp.tab[i][0] += static_cast<uint32_t>(tile_offset);
+  };
   if (late >= clusters || lag <= 0) late = 0;
   if (late == 0) lag = 0;
   const PieceKey key{T, K, clusters, late, lag};
@@ -346,24 +353,28 @@ bool plan_pair_pieces(PairParams& pp, int clusters, int64_t late, int64_t lag) {
     if (e.key == key) {
       if (!e.ok) return false;
       pp.n_tab = e.n_tab;
+      pp.n_tab_early = e.n_tab_early;
       std::memcpy(pp.tab, e.tab, sizeof(uint32_t) * 3 * static_cast<size_t>(e.n_tab));
+      shift();
       return true;
     }
   }
-  const bool ok = plan_pair_pieces_uncached(pp, clusters, late, lag);
+  const bool ok = plan_pair_pieces_uncached(pp, clusters, late, lag, T);
   PieceEntry& e = g_piece_cache[g_piece_next];
   g_piece_next = (g_piece_next + 1) % 16;
   if (g_piece_used < 16) ++g_piece_used;
   e.key = key;
   e.ok = ok;
   e.n_tab = ok ? pp.n_tab : 0;
+  e.n_tab_early = ok ? pp.n_tab_early : 0;
   if (ok) std::memcpy(e.tab, pp.tab, sizeof(uint32_t) * 3 * static_cast<size_t>(pp.n_tab));
+  if (ok) shift();
   return ok;
 }
 
-bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64_t lag) {
+bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64_t lag,
+                               int64_t T) {
   pp.n_tab = 0;
-  const int64_t T = pp.pair_tiles;
   const int64_t K = pp.kt_w + 2 * static_cast<int64_t>(pp.kt_b);
   const int64_t ne = clusters - late;
   constexpr int64_t kNone = int64_t(1) << 40;
@@ -453,6 +464,7 @@ bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64
   };
   std::stable_sort(early.begin(), early.end(), longer);
   std::stable_sort(latep.begin(), latep.end(), longer);
+  pp.n_tab_early = static_cast<int>(early.size());
   early.insert(early.end(), latep.begin(), latep.end());
   for (size_t i = 0; i < early.size(); ++i) {
     const Piece& q = early[i];
@@ -462,6 +474,56 @@ bool plan_pair_pieces_uncached(PairParams& pp, int clusters, int64_t late, int64
     pp.tab[i][2] = static_cast<uint32_t>(q.ke);
   }
   pp.n_tab = static_cast<int>(early.size());
+  return true;
+}
+
+// Whole tiles and a piece table, with at least as many pair tiles as pairs:
+// every pair runs w = T / pairs whole pair tiles (one item each, no partial
+// sums), then one piece of the R = T - w pairs tiles left over, cut by the
+// piece table's dynamic program (the late pairs' pieces shorter by the lag).
+// Against static ranges (one contiguous run per pair, up to three pieces
+// with a drain between each), a pair changes items once.  Used when the
+// remainder is at least a quarter of the pairs (a few tiles left over would
+// be cut into pieces shorter than the drain they cost) and the longest pair
+// is at most kWholeSlack K tiles longer than a static range.
+#ifndef DORA_WHOLE_PIECES
+#define DORA_WHOLE_PIECES 1
+#endif
+constexpr int64_t kWholeSlack = 12;
+
+bool plan_whole_pieces(PairParams& pp, int clusters, int64_t late, int64_t lag) {
+  pp.n_whole = 0;
+  pp.n_tab = 0;
+  const int64_t T = pp.pair_tiles;
+  const int64_t K = pp.kt_w + 2 * static_cast<int64_t>(pp.kt_b);
+  const int64_t n = clusters;
+  if (!DORA_WHOLE_PIECES || n <= 0 || T < n || T > 0xFFFF || K <= 0) return false;
+  const int64_t w = T / n, R = T - w * n;
+  if (4 * R < n) return false;
+  if (late >= n || lag <= 0) late = 0;
+  if (late == 0) lag = 0;
+  if (!plan_pair_pieces(pp, clusters, late, lag, R, w * n)) return false;
+  int64_t longest = 0;
+  for (int i = 0; i < pp.n_tab; ++i) {
+    const int64_t len = static_cast<int64_t>(pp.tab[i][2]) - pp.tab[i][1];
+    longest = len > longest ? len : longest;
+  }
+  const int64_t range_len = (T * K + late * lag + n - 1) / n;
+  const int n_early = pp.n_tab_early, n_late = pp.n_tab - pp.n_tab_early;
+  if (w * K + longest > range_len + kWholeSlack || n_early > n - n_late) {
+    pp.n_tab = 0;
+    return false;
+  }
+  // one entry per pair: the early pieces for the first pairs, the late ones
+  // for the last (the pairs that start behind the Gram kernel), none between
+  uint32_t tab[kPairTabMax][3];
+  std::memcpy(tab, pp.tab, sizeof(tab));
+  for (int c = 0; c < n; ++c) {
+    const int from = c < n_early ? c : (c >= n - n_late ? n_early + (c - (static_cast<int>(n) - n_late)) : -1);
+    for (int k = 0; k < 3; ++k) pp.tab[c][k] = from >= 0 ? tab[from][k] : (k == 0 ? kNoPiece : 0u);
+  }
+  pp.n_tab = static_cast<int>(n);
+  pp.n_whole = static_cast<int>(w);
   return true;
 }
 
@@ -526,10 +588,11 @@ int plan_main_pass(PairParams& pp, int64_t d_out, int64_t d_in, int64_t r, int c
   const int gnb = gram_nb(rp), gcl = gram_cluster_for(pp.kt_w);
   const int gram_ctas = mode == kPassFinal ? 0 : gnb * (gnb + 1) / 2 * gcl;
   const int gram_kt = static_cast<int>(ceil_div(pp.kt_w, gcl));
+  const int64_t late = gram_ctas > 0 ? (gram_ctas + 1) / 2 : 0;
+  const int64_t lag = gram_ctas > 0 ? gram_lag_tiles(pp, gram_kt) : 0;
+  if (plan_whole_pieces(pp, clusters_max, late, lag)) return clusters_max;
   if (plan_pair_ranges(pp, clusters_max, gram_ctas, gram_kt)) return pp.ranges;
-  if (plan_pair_pieces(pp, clusters_max, gram_ctas > 0 ? (gram_ctas + 1) / 2 : 0,
-                       gram_ctas > 0 ? gram_lag_tiles(pp, gram_kt) : 0))
-    return pp.n_tab;
+  if (plan_pair_pieces(pp, clusters_max, late, lag, pp.pair_tiles, 0)) return pp.n_tab;
   const int items = pp.pair_tiles * pp.splits;
   return items < clusters_max ? items : clusters_max;
 }
@@ -620,7 +683,7 @@ int run_bf16_pass(const void* W, const void* A, const void* B, int64_t d_out, in
     clusters = plan_main_pass(pp, d_out, d_in, r, clusters_max, mode);
     if (pp.n0 != n0 || pp.n1 != n1) return DORA_ERR_UNSUPPORTED;
   }
-  const bool gram_zeroes = zero_words && mode != kPassFinal && d_out > 0 && pp.n_tab > 0;
+  const bool gram_zeroes = zero_words && mode != kPassFinal && d_out > 0 && table_mode(pp);
   if (zero_words && !gram_zeroes)
     DORA_TRY(launch_zero_words(status, static_cast<int>(plan.zero_bytes / 4), stream));
 
@@ -1698,12 +1761,17 @@ int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
         add(tile, split, kb, ke, nsplit);
       }
     }
-  } else if (pp.n_tab > 0) {
-    if (launch != pp.n_tab || launch > clusters || pp.n_tab > kPairTabMax) ++bad;
-    for (int item = 0; item < pp.n_tab; ++item) {
-      table_piece(pp, item, tile, split, kb, ke, nsplit);
-      add(tile, split, kb, ke, nsplit);
-    }
+  } else if (table_mode(pp)) {
+    if (pp.n_tab > kPairTabMax || launch > clusters) ++bad;
+    if (pp.n_whole == 0 && launch != pp.n_tab) ++bad;
+    if (pp.n_whole > 0 && launch != clusters) ++bad;
+    for (int c = 0; c < launch; ++c)
+      for (int n = 0;; ++n) {
+        const int item = table_item(pp, c, n);
+        if (item < 0) break;
+        table_piece(pp, item, tile, split, kb, ke, nsplit);
+        add(tile, split, kb, ke, nsplit);
+      }
   } else {
     if (launch < 1 || launch > clusters) ++bad;
     for (int item = 0; item < pp.pair_tiles * pp.splits; ++item) {
@@ -1727,7 +1795,7 @@ int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,
     }
     if (at != ktot) ++bad;
   }
-  *schedule = pp.ranges > 0 ? 1 : (pp.n_tab > 0 ? 2 : 0);
+  *schedule = pp.ranges > 0 ? 1 : (pp.n_whole > 0 ? 3 : (pp.n_tab > 0 ? 2 : 0));
   *max_pieces = most;
   *defects = bad;
   return DORA_OK;

@@ -195,7 +195,7 @@ __device__ __forceinline__ void item_range(const PairParams& p, const ModView& m
     range_piece(p, item, tile, split, kb, ke, nsplit);
     return;
   }
-  if (!kGrouped && p.n_tab > 0) {
+  if (!kGrouped && table_mode(p)) {
     table_piece(p, item, tile, split, kb, ke, nsplit);
     return;
   }
@@ -243,11 +243,11 @@ __device__ __forceinline__ void record_timeout(int* status) {
 // ring; the reader releases the slot on the even CTA's `item_empty`.
 __device__ __forceinline__ int read_item(uint32_t n, uint64_t* item_full, const volatile int* item_slot,
                                          uint32_t item_empty0, uint64_t deadline, int* status,
-                                         bool by_index) {
-  // piece table: every role of both CTAs knows the pair's one piece (its
+                                         const PairParams* table) {
+  // piece table: every role of both CTAs knows the pair's items (from its
   // cluster index) without the ring, so no role waits for a publication
-  // across the pair at the start
-  if (by_index) return n == 0 ? static_cast<int>(blockIdx.x >> 1) : -1;
+  // across the pair
+  if (table) return table_item(*table, static_cast<int>(blockIdx.x >> 1), static_cast<int>(n));
   const uint32_t slot = n % kItemRing;
   if (!mbar_wait_cluster(&item_full[slot], (n / kItemRing) & 1u, deadline)) {
     record_timeout(status);
@@ -293,15 +293,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();          // 0: issues the MMAs, 1: its peer
-  const int n_items = kGrouped ? p.n_items : (p.n_tab > 0 ? p.n_tab : p.pair_tiles * p.splits);
+  const int n_items = kGrouped ? p.n_items : p.pair_tiles * p.splits;
   const ModView single = single_view(p, &tW, &tA, &tB, &tGhi, &tGlo);
   const uint32_t item_empty0 = map_to_rank(smem_u32(item_empty), 0);
   const uint64_t deadline = global_timer_ns() + p.timeout_ns;
-  // piece table: pair c runs piece c and nothing else (the table lists the
-  // long pieces first, and clusters start in index order, so the pairs
-  // behind the Gram kernel get the short ones): no claim on the counter, and
-  // no item ring -- every role derives the item from the cluster index
-  const bool by_index = !kGrouped && p.n_tab > 0;
+  // piece table: pair c runs its n_whole whole tiles, then piece c (the table
+  // lists the long pieces first, and clusters start in index order, so the
+  // pairs behind the Gram kernel get the short ones): no claim on the
+  // counter, and no item ring -- every role derives its items from the
+  // cluster index
+  const bool by_index = !kGrouped && table_mode(p);
+  const PairParams* const table = by_index ? &p : nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (uint32_t n = 0; !stop; ++n) {
         int item;
         if (by_index) {
-          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, true);
+          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, table);
         } else if (rank == 0) {
           // publish the claimed item (or the end) to both CTAs
           const uint32_t slot = n % kItemRing;
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           mbar_arrive(&item_full[slot]);
           mbar_arrive_cluster(full1 + slot * 8u);
         } else {
-          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, by_index);
+          item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, table);
         }
         if (item < 0) break;
         const ModView mv = view_of<kGrouped>(p, single, mod_begin, item);
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       int icount = 0;
       bool stop = false;
       for (uint32_t n = 0; !stop; ++n, ++icount) {
-        const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, by_index);
+        const int item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, table);
         if (item < 0) break;
         int tile, split, kb, ke, nsplit;
         item_range<kGrouped>(p, view_of<kGrouped>(p, single, mod_begin, item), item, tile, split, kb, ke,
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     int icount = 0;
     for (uint32_t n = 0;; ++n, ++icount) {
       int item = -1;
-      if (alive && lane == 0) item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, by_index);
+      if (alive && lane == 0) item = read_item(n, item_full, item_slot, item_empty0, deadline, p.status, table);
       item = __shfl_sync(0xFFFFFFFFu, item, 0);
       {
         // the 8 warps read the same item sequence; decide together anyway, as

@@ -420,14 +420,16 @@ int dora_selftest_timeout(void* workspace, size_t workspace_bytes, unsigned time
  * exactly as dora_factored_norm does on a device with `clusters` co-resident
  * CTA pairs (1 .. 65535; 76 on a GB300), enumerates every piece of work the
  * launched pairs would run -- K segments handed out in item order, the static
- * ranges of each pair (issued from the last piece to the first), or the
- * piece table (one piece per pair, with fewer pair tiles than pairs) -- and
- * checks that the pieces of every 256-row pair tile cover its K tiles once,
- * in K order, numbered 0 .. n - 1 with n <= 16 (the partial planes of the
- * workspace), and that a piece table gives each launched pair one piece.
- * Writes the schedule chosen (*schedule: 0 K segments, 1 static ranges,
- * 2 piece table), the largest number of pieces of one tile, and the number
- * of defects found (0 when the plan is sound).  Returns DORA_ERR_INVALID_ARG
+ * ranges of each pair (issued from the last piece to the first), the piece
+ * table (one piece per pair, with fewer pair tiles than pairs), or whole
+ * tiles and a piece table (each pair w whole pair tiles, then at most one
+ * piece of the tiles left over) -- and checks that the pieces of every
+ * 256-row pair tile cover its K tiles once, in K order, numbered 0 .. n - 1
+ * with n <= 16 (the partial planes of the workspace), and that a piece table
+ * gives each launched pair at most one piece.  Writes the schedule chosen
+ * (*schedule: 0 K segments, 1 static ranges, 2 piece table, 3 whole tiles
+ * and a piece table), the largest number of pieces of one tile, and the
+ * number of defects found (0 when the plan is sound).  Returns DORA_ERR_INVALID_ARG
  * for bad arguments, else DORA_OK.
  */
 int dora_selftest_schedule(int64_t d_out, int64_t d_in, int64_t r, int clusters,

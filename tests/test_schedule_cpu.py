@@ -25,6 +25,7 @@ GB300_PAIRS = 76
 
 
 TABLE, RANGES, SEGMENTS = api.SCHEDULE_TABLE, api.SCHEDULE_RANGES, api.SCHEDULE_SEGMENTS
+WHOLE = api.SCHEDULE_WHOLE_TABLE
 
 
 @pytest.mark.parametrize("d_out,d_in,r,schedule", [
@@ -36,7 +37,7 @@ TABLE, RANGES, SEGMENTS = api.SCHEDULE_TABLE, api.SCHEDULE_RANGES, api.SCHEDULE_
     (19500, 4104, 40, RANGES),    # 77 pair tiles: static ranges
     (19500, 4104, 296, RANGES),
     (20000, 4096, 384, RANGES),
-    (28672, 8192, 384, RANGES),
+    (28672, 8192, 384, WHOLE),    # 112 pair tiles: one whole tile per pair + pieces of 36
 ])
 def test_known_shapes(d_out, d_in, r, schedule):
     got, most, defects = api.dora_selftest_schedule(d_out, d_in, r, GB300_PAIRS)
@@ -56,7 +57,7 @@ def test_piece_table_of_the_metric_workload():
 
 def test_seeded_sweep_of_shapes_and_grids():
     rng = random.Random(2026)
-    seen = {TABLE: 0, RANGES: 0, SEGMENTS: 0}
+    seen = {TABLE: 0, RANGES: 0, SEGMENTS: 0, WHOLE: 0}
     for _ in range(4000):
         d_out = rng.choice([rng.randint(1, 300), rng.randint(1, 5000), rng.randint(1, 200000)])
         d_in = rng.choice([rng.randint(1, 64), rng.randint(1, 20000), rng.randint(1, 100000)])
