@@ -55,6 +55,20 @@ def test_piece_table_of_the_metric_workload():
     assert (got, most, defects) == (TABLE, 4, 0)
 
 
+def test_whole_tiles_of_the_moe_shaped_module():
+    """28672 x 8192, r = 384 on 76 pairs: 112 pair tiles of 140 K tiles.
+    Every pair runs one whole tile (76 tiles); the 36 left over are cut into
+    at most one piece per pair by the piece table (early pieces for the
+    first pairs, shorter late pieces for the pairs behind the Gram kernel),
+    so no tile has more than two pieces."""
+    got, most, defects = api.dora_selftest_schedule(28672, 8192, 384, GB300_PAIRS)
+    assert (got, most, defects) == (WHOLE, 2, 0)
+    # a few tiles left over would be cut into pieces shorter than the drain
+    # they cost: static ranges there (79 pair tiles, 3 left over)
+    got, _, defects = api.dora_selftest_schedule(20000, 8192, 384, GB300_PAIRS)
+    assert (got, defects) == (RANGES, 0)
+
+
 def test_seeded_sweep_of_shapes_and_grids():
     rng = random.Random(2026)
     seen = {TABLE: 0, RANGES: 0, SEGMENTS: 0, WHOLE: 0}
