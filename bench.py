@@ -27,7 +27,9 @@ Printed (rank 0, one JSON line):
              d_lora, dmag) at the same shape, GB/s
   stack      the 196-module 7B-like stack at r = 128: grouped norm through a
              plan and grouped compose, modules per second
-  fp32_norm  the fp32 norm at 8192 x 8192, r = 512 (3xTF32 tensor-core pass)
+  fp32_norm  the fp32 norm at 8192 x 8192, r = 512 (3xTF32 tensor-core pass):
+             per call with events and back to back, the pass alone against
+             the derived TF32 peak and the counter's TF32 issue rate
 
 --impl reference times the CPU oracle (the method's write-ups ship no code to
 run) on the same metric, per step a bounded sample sized so the run ends in
